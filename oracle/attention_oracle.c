@@ -1,0 +1,263 @@
+/*
+ * Exact softmax attention and its analytic gradient, in fp64, on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the GPU kernels
+ * are checked against.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load it.  It shares no code, header or
+ * constant with the CUDA library, and the library never calls it.
+ *
+ * What it computes is the plain definition of the operation, not the tiled
+ * method: the whole score row of one query is formed, the two-pass stable
+ * softmax is taken over it, and the products are plain sums.  Loops run in
+ * the order of the formulas; nothing is blocked, fused or reordered.
+ *
+ * Sources (page title, then the place on the page):
+ *  - "FlashAttention-2: Faster Attention with Better Parallelism and Work
+ *    Partitioning" (paper digest), section 3 "Target operation":
+ *    O = softmax(Q K^T) V with an optional causal mask, fp16/bf16 inputs.
+ *    The scale factor the configurations use (1/sqrt(d)) multiplies Q K^T.
+ *  - same digest, section 4 notation table: L = m + log(l), the logsumexp
+ *    of a score row, and D = rowsum(dO o O), the backward auxiliary.
+ *  - same digest, section 4 "logsumexp fusion": P = exp(S - L).
+ *  - same digest, section 3 "FLOPs": the backward pass is five matrix
+ *    products; below they are S = Q K^T, dV = P^T dO, dP = dO V^T,
+ *    dQ = dS K and dK = dS^T Q with dS = P o (dP - D), the gradient of the
+ *    scalar sum(O o dO) through the softmax.
+ *  - same digest, section 4 "six checks", GQA/MQA: several query heads share
+ *    one key/value head by index, and dK, dV sum over the sharing heads.
+ *
+ * Readings where the pages are silent:
+ *  - the mask keeps key k for query i when k <= i + (Nk - Nq) (aligned to
+ *    the bottom-right corner; with Nq == Nk this is k <= i);
+ *  - L is the natural logarithm, of the scaled scores;
+ *  - a query row with no allowed key (only possible when Nq > Nk under the
+ *    mask) has O = 0, L = -inf and zero gradients;
+ *  - query head h reads key/value head h / G, G = H / Hkv.
+ *
+ * Layout: every array is row-major.  One call works on one "group": the G
+ * query heads that share one key/value head.
+ *   q, o, dout, dq : [G][Nq][d]      k, v, dk, dv : [Nk][d]
+ *   lse            : [G][Nq]
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Whether query row i may attend to key k. */
+static int allowed(long i, long k, long Nq, long Nk, int causal)
+{
+    if (!causal)
+        return 1;
+    return k <= i + (Nk - Nq);
+}
+
+static double dot(const double *x, const double *y, long d)
+{
+    double acc = 0.0;
+    for (long c = 0; c < d; ++c)
+        acc += x[c] * y[c];
+    return acc;
+}
+
+/*
+ * Scores of one query row: s[k] = scale * q_i . k_k for allowed keys,
+ * -inf elsewhere.  Returns the row logsumexp L = m + ln(sum_k exp(s_k - m))
+ * (two passes: max, then the shifted sum), or -inf for an empty row.
+ */
+static double score_row(const double *qi, const double *k, long i, long Nq,
+                        long Nk, long d, int causal, double scale, double *s)
+{
+    double m = -INFINITY;
+    for (long kk = 0; kk < Nk; ++kk) {
+        if (allowed(i, kk, Nq, Nk, causal)) {
+            s[kk] = scale * dot(qi, k + kk * d, d);
+            if (s[kk] > m)
+                m = s[kk];
+        } else {
+            s[kk] = -INFINITY;
+        }
+    }
+    if (m == -INFINITY)
+        return -INFINITY;
+    double l = 0.0;
+    for (long kk = 0; kk < Nk; ++kk)
+        if (allowed(i, kk, Nq, Nk, causal))
+            l += exp(s[kk] - m);
+    return m + log(l);
+}
+
+/* Softmax weight of one score given the row logsumexp: P = exp(S - L). */
+static double weight(double s, double lse)
+{
+    if (lse == -INFINITY || s == -INFINITY)
+        return 0.0;
+    return exp(s - lse);
+}
+
+/* One query row of the forward pass: O_i = sum_k P_ik V_k, and L_i. */
+static void forward_row(const double *qi, const double *k, const double *v,
+                        long i, long Nq, long Nk, long d, int causal,
+                        double scale, double *s, double *oi, double *lse_i)
+{
+    double L = score_row(qi, k, i, Nq, Nk, d, causal, scale, s);
+    for (long c = 0; c < d; ++c)
+        oi[c] = 0.0;
+    for (long kk = 0; kk < Nk; ++kk) {
+        double p = weight(s[kk], L);
+        if (p == 0.0)
+            continue;
+        for (long c = 0; c < d; ++c)
+            oi[c] += p * v[kk * d + c];
+    }
+    *lse_i = L;
+}
+
+/*
+ * Forward pass for one group of G query heads.
+ * q [G][Nq][d], k/v [Nk][d] -> o [G][Nq][d], lse [G][Nq].
+ */
+void oracle_fwd_group(const double *q, const double *k, const double *v,
+                      long G, long Nq, long Nk, long d, int causal,
+                      double scale, double *o, double *lse)
+{
+    long rows = G * Nq;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < rows; ++r) {
+            long i = r % Nq;
+            forward_row(q + r * d, k, v, i, Nq, Nk, d, causal, scale, s,
+                        o + r * d, lse + r);
+        }
+        free(s);
+    }
+}
+
+/*
+ * Forward pass for a list of query rows of one group (used to check single
+ * outputs of very large problems).  rows[2*t] = head within the group,
+ * rows[2*t+1] = query index.  o [n][d], lse [n].
+ */
+void oracle_fwd_rows(const double *q, const double *k, const double *v,
+                     long G, long Nq, long Nk, long d, int causal,
+                     double scale, long n, const long *rows, double *o,
+                     double *lse)
+{
+    (void)G;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long t = 0; t < n; ++t) {
+            long g = rows[2 * t], i = rows[2 * t + 1];
+            forward_row(q + (g * Nq + i) * d, k, v, i, Nq, Nk, d, causal,
+                        scale, s, o + t * d, lse + t);
+        }
+        free(s);
+    }
+}
+
+/*
+ * Backward pass for one group, given the upstream gradient dO of the scalar
+ * sum(O o dO).  The oracle recomputes its own fp64 O and L first.
+ *   dV_k = sum_{g,i} P_ik dO_i
+ *   dP_ik = dO_i . V_k,   D_i = dO_i . O_i,   dS_ik = P_ik (dP_ik - D_i)
+ *   dQ_i = scale * sum_k dS_ik K_k
+ *   dK_k = scale * sum_{g,i} dS_ik Q_i
+ * Optional outputs o_out / lse_out / delta_out receive O, L and D (may be
+ * NULL).
+ */
+void oracle_bwd_group(const double *q, const double *k, const double *v,
+                      const double *dout, long G, long Nq, long Nk, long d,
+                      int causal, double scale, double *dq, double *dk,
+                      double *dv, double *o_out, double *lse_out,
+                      double *delta_out)
+{
+    long rows = G * Nq;
+    double *o = (double *)malloc(sizeof(double) * (size_t)(rows * d + 1));
+    double *L = (double *)malloc(sizeof(double) * (size_t)(rows + 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(rows + 1));
+
+    /* Pass 1: O, L and D = rowsum(dO o O) for every query row. */
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < rows; ++r) {
+            long i = r % Nq;
+            forward_row(q + r * d, k, v, i, Nq, Nk, d, causal, scale, s,
+                        o + r * d, L + r);
+            D[r] = dot(dout + r * d, o + r * d, d);
+        }
+        free(s);
+    }
+
+    /* Pass 2: dQ_i = scale * sum_k P_ik (dP_ik - D_i) K_k, row by row. */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long r = 0; r < rows; ++r) {
+        long i = r % Nq;
+        const double *qi = q + r * d, *doi = dout + r * d;
+        double *dqi = dq + r * d;
+        for (long c = 0; c < d; ++c)
+            dqi[c] = 0.0;
+        for (long kk = 0; kk < Nk; ++kk) {
+            if (!allowed(i, kk, Nq, Nk, causal))
+                continue;
+            double sik = scale * dot(qi, k + kk * d, d);
+            double p = weight(sik, L[r]);
+            double dp = dot(doi, v + kk * d, d);
+            double ds = p * (dp - D[r]);
+            for (long c = 0; c < d; ++c)
+                dqi[c] += scale * ds * k[kk * d + c];
+        }
+    }
+
+    /* Pass 3: dK_k and dV_k, key by key, summed over the G heads. */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long kk = 0; kk < Nk; ++kk) {
+        double *dkk = dk + kk * d, *dvk = dv + kk * d;
+        for (long c = 0; c < d; ++c) {
+            dkk[c] = 0.0;
+            dvk[c] = 0.0;
+        }
+        for (long r = 0; r < rows; ++r) {
+            long i = r % Nq;
+            if (!allowed(i, kk, Nq, Nk, causal))
+                continue;
+            const double *qi = q + r * d, *doi = dout + r * d;
+            double sik = scale * dot(qi, k + kk * d, d);
+            double p = weight(sik, L[r]);
+            double dp = dot(doi, v + kk * d, d);
+            double ds = p * (dp - D[r]);
+            for (long c = 0; c < d; ++c) {
+                dvk[c] += p * doi[c];
+                dkk[c] += scale * ds * qi[c];
+            }
+        }
+    }
+
+    if (o_out)
+        memcpy(o_out, o, sizeof(double) * (size_t)(rows * d));
+    if (lse_out)
+        memcpy(lse_out, L, sizeof(double) * (size_t)rows);
+    if (delta_out)
+        memcpy(delta_out, D, sizeof(double) * (size_t)rows);
+    free(o);
+    free(L);
+    free(D);
+}
+
+/* Number of threads the parallel loops above use. */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
