@@ -1,0 +1,152 @@
+"""ctypes binding of libfa_gb300.so (include/fa.h).
+
+Argument marshalling only: torch tensors are checked for dtype, device and
+layout, and their data pointers are handed to the C entry points, which run
+every step on the GPU.  There is no fallback: if the library is missing or a
+call fails, a ``FaError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
+
+FA_F16, FA_BF16 = 0, 1
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_WORKSPACE = range(6)
+
+# Symbols include/fa.h declares, with their ctypes signatures.
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
+                    _vp, _sz, _vp]),
+    "fa_get_device_status": (_i, [_vp]),
+    "fa_strerror": (ctypes.c_char_p, [_i]),
+}
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed with status {status}: {strerror(status)}")
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise FaError(-1, f"loading {path}: library not built (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().fa_strerror(status).decode()
+    except Exception:
+        return "library not loaded"
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FA_F16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; fp16 and bf16 are supported")
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _check(st: int, what: str):
+    if st != FA_OK:
+        raise FaError(st, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+# ---------------------------------------------------------------- raw entry points
+def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, dtype, stream=None) -> int:
+    return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                         int(causal), float(scale), dtype, _stream_ptr(stream))
+
+
+def fa_bwd_workspace_size(B, H, Hkv, N, d) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, Hkv, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype, workspace,
+           workspace_bytes, stream=None) -> int:
+    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, Hkv, N, d, int(causal), float(scale), dtype,
+                         _ptr(workspace), int(workspace_bytes), _stream_ptr(stream))
+
+
+def fa_get_device_status(stream=None) -> int:
+    return load().fa_get_device_status(_stream_ptr(stream))
+
+
+# ---------------------------------------------------------------- tensor helpers
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("expected q [B,H,N,d], k and v [B,Hkv,N,d]")
+    B, H, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)}")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    return B, H, k.shape[1], N, d
+
+
+def forward(q, k, v, causal: bool, scale: float, out=None, lse=None, stream=None):
+    """(o, lse) of exact attention; outputs are allocated unless given."""
+    B, H, Hkv, N, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, causal, scale, _dtype_code(q), stream),
+           "fa_fwd")
+    return out, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """(dq, dk, dv) of sum(O o dO); outputs and scratch are allocated unless given."""
+    B, H, Hkv, N, d = _shapes(q, k, v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+                  _dtype_code(q), workspace, workspace.numel() * workspace.element_size(),
+                  stream), "fa_bwd")
+    return dq, dk, dv
+
+
+def device_status(stream=None):
+    """Synchronise the stream and raise if a kernel reported a bounded-wait timeout."""
+    _check(fa_get_device_status(stream), "fa_get_device_status")

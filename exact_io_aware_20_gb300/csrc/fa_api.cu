@@ -1,0 +1,212 @@
+// C-ABI layer of libfa_gb300.so: argument validation, variant dispatch,
+// tensor-map encoding and error reporting.  See include/fa.h for the contract.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Device-side error word; kernels receive its address and set bit 0 when a
+// bounded wait expired.
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+thread_local char g_cuda_msg[256] = "no CUDA error recorded";
+
+int cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_cuda_msg, sizeof(g_cuda_msg), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return FA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+void load_encoder() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                  cudaEnableDefault, &q);
+  if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+    g_encode_err = cudaErrorNotSupported;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// Per-device answer to "is this an sm_103 device?", cached.
+int g_dev_ok[64];   // 0 = unknown, 1 = yes, 2 = no
+std::mutex g_dev_mu;
+
+unsigned int* g_err_ptr[64];
+
+// Checks that the current device is an sm_103 part and returns the device
+// address of its error word in *err (both cached per device).
+int check_device(unsigned int** err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major == 10 && minor == 3) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_device_error);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+      g_err_ptr[dev] = static_cast<unsigned int*>(ptr);
+      g_dev_ok[dev] = 1;
+    } else {
+      g_dev_ok[dev] = 2;
+    }
+  }
+  if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  *err = g_err_ptr[dev];
+  return FA_OK;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int validate(int B, int H, int Hkv, int N, int d, int causal, float scale, int dtype,
+             Problem* pr) {
+  if (B < 1 || H < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;   // grid y/z limits
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  // Every tensor-map dimension and every flat index must fit the kernels'
+  // 32-bit coordinates.
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (static_cast<long long>(B) * H > INT32_MAX || rows > (1ll << 31) - 1 ||
+      static_cast<long long>(N) * d > INT32_MAX)
+    return FA_ERR_INVALID_ARG;
+  pr->B = B;
+  pr->H = H;
+  pr->Hkv = Hkv;
+  pr->N = N;
+  pr->d = d;
+  pr->causal = causal;
+  pr->bf16 = dtype == FA_BF16 ? 1 : 0;
+  pr->scale = scale;
+  pr->err = nullptr;
+  return FA_OK;
+}
+
+}  // namespace
+
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int cols, int rows, int outer,
+                         int box_cols, int box_rows) {
+  std::call_once(g_encode_once, load_encoder);
+  if (g_encode_err != cudaSuccess) return g_encode_err;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                           static_cast<cuuint64_t>(cols) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+size_t bwd_workspace_bytes(int B, int H, int N, int d) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
+  const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
+  return delta + acc;
+}
+
+}  // namespace fa
+
+using fa::Problem;
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Hkv, int N, int d, int causal, float scale, int dtype,
+                      fa_stream_t stream) {
+  Problem pr;
+  int st = fa::validate(B, H, Hkv, N, d, causal, scale, dtype, &pr);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned(q, 16) || !fa::aligned(k, 16) || !fa::aligned(v, 16) || !fa::aligned(o, 16) ||
+      !fa::aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  if ((st = fa::check_device(&pr.err)) != FA_OK) return st;
+  fa::FwdArgs a{q, k, v, o, lse};
+  cudaError_t e = fa::launch_fwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fa::cuda_fail(e, "fa_fwd launch");
+  return FA_OK;
+}
+
+extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
+  Problem pr;
+  if (fa::validate(B, H, Hkv, N, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
+  return fa::bwd_workspace_bytes(B, H, N, d);
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int H, int Hkv, int N, int d, int causal, float scale, int dtype,
+                      void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Problem pr;
+  int st = fa::validate(B, H, Hkv, N, d, causal, scale, dtype, &pr);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned(q, 16) || !fa::aligned(k, 16) || !fa::aligned(v, 16) || !fa::aligned(o, 16) ||
+      !fa::aligned(dout, 16) || !fa::aligned(dq, 16) || !fa::aligned(dk, 16) ||
+      !fa::aligned(dv, 16) || !fa::aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  const size_t need = fa::bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need || !fa::aligned(workspace, 256))
+    return FA_ERR_WORKSPACE;
+  if ((st = fa::check_device(&pr.err)) != FA_OK) return st;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  float* delta = static_cast<float*>(workspace);
+  float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        (rows * sizeof(float) + 255) / 256 * 256);
+  fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc};
+  cudaError_t e = fa::launch_bwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fa::cuda_fail(e, "fa_bwd launch");
+  return FA_OK;
+}
+
+extern "C" int fa_get_device_status(fa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fa::cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, fa::g_device_error, sizeof(word));
+  if (e != cudaSuccess) return fa::cuda_fail(e, "read device error word");
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(fa::g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fa::cuda_fail(e, "clear device error word");
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+extern "C" const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "success";
+    case FA_ERR_INVALID_ARG: return "invalid argument (pointer, alignment, size or scale)";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dim, dtype or device (needs sm_103)";
+    case FA_ERR_CUDA: return fa::g_cuda_msg;
+    case FA_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case FA_ERR_WORKSPACE: return "backward workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}

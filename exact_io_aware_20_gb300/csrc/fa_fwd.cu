@@ -1,0 +1,404 @@
+// Forward pass of exact attention on sm_103a: O = softmax(scale * Q K^T) V
+// and the row logsumexp L, computed tile by tile without writing the score
+// matrix to memory.
+//
+// Method ("FlashAttention-2: Faster Attention with Better Parallelism and
+// Work Partitioning", paper digest):
+//  - section 2 Q2, improvement 2: the outer loop runs over query tiles, which
+//    are independent, so work units are (batch, head, query tile);
+//  - section 2 Q2, tweak 1: the output is kept unnormalised,
+//    O~(j) = diag(exp(m(j-1) - m(j))) O~(j-1) + exp(S(j) - m(j)) V(j), and is
+//    divided by the row sum l once at the end;
+//  - section 2 Q2, tweak 2: only L = m + log(l) is written for the backward;
+//  - section 2 Q2, causal masking: key tiles entirely above the diagonal are
+//    skipped and the mask is applied only on tiles that cross it;
+//  - section 4 "six checks", GQA/MQA: query head h reads key/value head
+//    h / (H / Hkv) by index, with no copy.
+//
+// GB300 design (not the pages' A100 design): one CTA per 128-row query tile,
+// warp-specialised:
+//   warp 0      TMA producer: Q once, then K_j / V_j through two smem rings;
+//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM score buffers,
+//               O += P_j V_j with P_j read from TMEM (tcgen05 "TS" form);
+//   warps 2..5  softmax: one query row per thread, read S_j from TMEM, mask,
+//               running max / sum, write P_j back into the score buffer as
+//               16-bit, rescale O in TMEM when the max moved, epilogue.
+// The O rescale is skipped while the running max has grown by at most 2^8
+// (log2 units); the final division and L use the same stale maximum, so the
+// result is unchanged.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kBR = 128;             // query rows per tile (= MMA M)
+constexpr int kThreads = 192;        // 6 warps
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int BC, int KST, int VST>
+struct FwdLayout {
+  static constexpr int kNch = D / 64;                 // 64-column (128-byte) chunks
+  static constexpr int kQBytes = kBR * D * 2;
+  static constexpr int kKVBytes = BC * D * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQBytes;
+  static constexpr int kVOff = kKOff + KST * kKVBytes;
+  static constexpr int kBarOff = kVOff + VST * kKVBytes;
+  // barrier indices
+  static constexpr int kQFull = 0;
+  static constexpr int kKFull = 1;
+  static constexpr int kKEmpty = kKFull + KST;
+  static constexpr int kVFull = kKEmpty + KST;
+  static constexpr int kVEmpty = kVFull + VST;
+  static constexpr int kSFull = kVEmpty + VST;   // 2
+  static constexpr int kPFull = kSFull + 2;      // 2
+  static constexpr int kODone = kPFull + 2;
+  static constexpr int kDrain = kODone + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
+  // TMEM columns
+  static constexpr uint32_t kS0 = 0, kS1 = BC, kO = 2 * BC;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kO + D <= kTmemCols, "TMEM budget");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct FwdParams {
+  void* o;
+  float* lse;
+  int H, Hkv, N, G;
+  int num_q_tiles;
+  float scale_log2;   // scale * log2(e)
+  unsigned int* err;
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, volatile int* abort) {
+  bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used only while winding down (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  int never = 0;
+  mbar_wait(bar, parity, &never);
+}
+
+template <int D, int BC, bool CAUSAL, bool BF16, int KST, int VST>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdLayout<D, BC, KST, VST>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = CAUSAL ? (p.num_q_tiles - 1 - static_cast<int>(blockIdx.x))
+                        : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kh = h / p.G;
+  int n_kv = (p.N + BC - 1) / BC;
+  if (CAUSAL) n_kv = min(n_kv, ((qt + 1) * kBR + BC - 1) / BC);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQFull), 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kSFull + s), 1);
+      mbar_init(bar(L::kPFull + s), 128);
+    }
+    mbar_init(bar(L::kODone), 1);
+    mbar_init(bar(L::kDrain), 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS0 = tmem + L::kS0, tS1 = tmem + L::kS1, tO = tmem + L::kO;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
+      mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
+      #pragma unroll
+      for (int c = 0; c < L::kNch; ++c)
+        tma_load_3d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, qt * kBR, zq);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % KST;
+        if (j >= KST && !mbar_wait(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
+        #pragma unroll
+        for (int c = 0; c < L::kNch; ++c)
+          tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
+                      bar(L::kKFull + s), c * 64, j * BC, zkv);
+        ++k_issued;
+        const int sv = j % VST;
+        if (j >= VST && !mbar_wait(bar(L::kVEmpty + sv), ((j / VST) + 1) & 1, abort)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
+        #pragma unroll
+        for (int c = 0; c < L::kNch; ++c)
+          tma_load_3d(sbase + L::kVOff + sv * L::kKVBytes + c * (BC * 128), &tm_v,
+                      bar(L::kVFull + sv), c * 64, j * BC, zkv);
+        ++v_issued;
+      }
+      // Never leave the CTA with copies in flight: wait for every load this
+      // thread issued (they have completed already on the normal path).
+      drain_wait(bar(L::kQFull), 0);
+      for (int j = max(0, k_issued - KST); j < k_issued; ++j)
+        drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
+      for (int j = max(0, v_issued - VST); j < v_issued; ++j)
+        drain_wait(bar(L::kVFull + j % VST), (j / VST) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(kBR, BC, BF16 ? 1 : 0, 0, 0);
+      constexpr uint32_t kIdO = idesc_f16(kBR, D, BF16 ? 1 : 0, 0, 1);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % KST;
+        if (!mbar_wait(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
+        #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk >> 2, w = kk & 3;
+          const uint64_t ad = smem_desc_sw128(sbase + L::kQOff + c * (kBR * 128) + w * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(
+              sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128) + w * 32, 16, 1024);
+          mma_ss(d_tmem, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kSFull + (j & 1)));
+        mma_commit(bar(L::kKEmpty + s));
+        return true;
+      };
+      bool ok = mbar_wait(bar(L::kQFull), 0, abort);
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) break;
+        if (!mbar_wait(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
+        const int sv = j % VST;
+        if (!mbar_wait(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
+        tc_fence_after();
+        const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
+        #pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk) {
+          const uint64_t bd =
+              smem_desc_sw128(sbase + L::kVOff + sv * L::kKVBytes + kk * 2048, BC * 128, 1024);
+          mma_ts(tO, a_tmem + kk * 8, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(L::kODone));
+        mma_commit(bar(L::kVEmpty + sv));
+      }
+      // Every MMA issued above completes before TMEM is released.
+      mma_commit(bar(L::kDrain));
+      drain_wait(bar(L::kDrain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;                 // TMEM lanes this warp may access
+    const int r_tile = quarter * 32 + lane;
+    const int row = qt * kBR + r_tile;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
+      if (!wait_uniform(bar(L::kSFull + (j & 1)), (j >> 1) & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[BC];
+      #pragma unroll
+      for (int c = 0; c < BC / 32; ++c)
+        tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      tmem_ld_wait();
+      reg_fence(sr);
+      float* s = reinterpret_cast<float*>(sr);
+      const int col0 = j * BC;
+      const bool need_mask = (CAUSAL && col0 + BC - 1 > qt * kBR) || (col0 + BC > p.N);
+      if (need_mask) {
+        #pragma unroll
+        for (int i = 0; i < BC; ++i) {
+          const int col = col0 + i;
+          if (col >= p.N || (CAUSAL && col > row)) s[i] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+      #pragma unroll
+      for (int i = 1; i < BC; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+      const bool need = m_new > m_ref + kRescaleThreshold;
+      const bool any = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (any) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+        l *= alpha;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      uint32_t pk[BC / 2];
+      float rs = 0.f;
+      #pragma unroll
+      for (int i = 0; i < BC / 2; ++i) {
+        const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
+        const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
+        rs += p0 + p1;
+        pk[i] = pack2<BF16>(p0, p1);
+      }
+      l += rs;
+      #pragma unroll
+      for (int c = 0; c < BC / 64; ++c)
+        tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
+      tmem_st_wait();
+      if (any && j > 0) {
+        // O holds P_0..P_{j-1} V: wait for the last of those products.
+        if (!wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o2[64];
+          tmem_ld32(tO + lane_off + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
+          tmem_ld32(tO + lane_off + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
+          tmem_ld_wait();
+          reg_fence(o2);
+          #pragma unroll
+          for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
+          tmem_st32(tO + lane_off + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
+          tmem_st32(tO + lane_off + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull + (j & 1)));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.N;
+      const bool in_range = row < p.N;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                             (row_base + (in_range ? row : 0)) * D);
+      #pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o1[32];
+        tmem_ld32(tO + lane_off + 32 * c, o1);
+        tmem_ld_wait();
+        reg_fence(o1);
+        uint32_t w[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l, __uint_as_float(o1[2 * i + 1]) * inv_l);
+        if (in_range) {
+          #pragma unroll
+          for (int i = 0; i < 4; ++i)
+            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (in_range) p.lse[row_base + row] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, int BC, bool CAUSAL, bool BF16, int KST, int VST>
+cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<D, BC, KST, VST>;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e;
+  if ((e = make_tmap_3d(&tq, a.q, D, pr.N, pr.B * pr.H, 64, kBR)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tk, a.k, D, pr.N, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tv, a.v, D, pr.N, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
+  auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  FwdParams p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.N = pr.N;
+  p.G = pr.H / pr.Hkv;
+  p.num_q_tiles = (pr.N + kBR - 1) / kBR;
+  p.scale_log2 = pr.scale * 1.4426950408889634f;
+  p.err = pr.err;
+  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D, int BC, int KST, int VST>
+cudaError_t dispatch_flags(const Problem& pr, const FwdArgs& a, cudaStream_t s) {
+  if (pr.causal) {
+    return pr.bf16 ? launch_variant<D, BC, true, true, KST, VST>(pr, a, s)
+                   : launch_variant<D, BC, true, false, KST, VST>(pr, a, s);
+  }
+  return pr.bf16 ? launch_variant<D, BC, false, true, KST, VST>(pr, a, s)
+                 : launch_variant<D, BC, false, false, KST, VST>(pr, a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
+  switch (pr.d) {
+    case 64: return dispatch_flags<64, 128, 3, 3>(pr, a, stream);
+    case 128: return dispatch_flags<128, 128, 2, 2>(pr, a, stream);
+    case 256: return dispatch_flags<256, 64, 2, 2>(pr, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

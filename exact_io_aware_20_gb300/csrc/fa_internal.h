@@ -1,0 +1,53 @@
+// Host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Shapes and pointers of one call, after validation.
+struct Problem {
+  int B, H, Hkv, N, d;
+  int causal;
+  int bf16;       // 1 = bf16, 0 = f16
+  float scale;
+  unsigned int* err;   // device error word (bit 0: a bounded wait expired)
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;    // [B, H, N] fp32 scratch
+  float* dq_acc;   // [B, H, N, d] fp32 scratch
+};
+
+// Encode a 3-D tiled tensor map over a [outer, rows, cols] 16-bit tensor
+// (cols contiguous) with a box of box_cols x box_rows and 128-byte swizzle.
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int cols, int rows, int outer,
+                         int box_cols, int box_rows);
+
+cudaError_t launch_fwd(const Problem& p, const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, cudaStream_t stream);
+
+// Bytes of backward scratch for a problem (delta + dq accumulator, each
+// rounded up to 256 bytes).
+size_t bwd_workspace_bytes(int B, int H, int N, int d);
+
+}  // namespace fa

@@ -1,0 +1,108 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library libfa_gb300.so.
+ *
+ * The operation ("FlashAttention-2: Faster Attention with Better Parallelism
+ * and Work Partitioning", paper digest, section 3 "Target operation"):
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ *
+ * for every batch b and query head h, with fp16 or bf16 inputs and fp32
+ * accumulation.  Query head h reads key/value head h / (H / Hkv), so
+ * Hkv == H is multi-head, 1 < Hkv < H grouped-query and Hkv == 1 multi-query
+ * attention (same digest, section 4 "six checks", GQA/MQA).  The causal mask
+ * keeps key k for query i when k <= i.  The forward pass also writes the row
+ * logsumexp L = m + log(l) (natural log, of the scaled scores; same digest,
+ * section 2 Q2, tweak 2), which the backward pass uses to rebuild the softmax
+ * weights as P = exp(S - L) (section 4).  The backward pass returns the
+ * gradients of sum(O o dO) (dQ, dK, dV) using D = rowsum(dO o O) (section 4
+ * notation table).
+ *
+ * Layout (all tensors contiguous, head dimension innermost):
+ *   q, o, dout, dq : [B][H][N][d]        16-bit, the `dtype` of the call
+ *   k, v, dk, dv   : [B][Hkv][N][d]      16-bit
+ *   lse            : [B][H][N]           fp32
+ * Supported: d in {64, 128, 256}; any N >= 1 (a length that is not a multiple
+ * of the tile size is handled inside the kernels); H % Hkv == 0.
+ *
+ * Ownership: the caller allocates every buffer (device memory) and keeps it
+ * alive until the work on `stream` has finished.  The library allocates no
+ * device memory; the backward pass takes its scratch from the caller's
+ * `workspace`.
+ *
+ * Semantics: every call only enqueues work on `stream` (NULL is the legacy
+ * default stream) and returns; nothing is synchronised.  Outputs are
+ * overwritten, never accumulated into.
+ *
+ * Errors: each call returns an fa_status; nothing is thrown.  Argument errors
+ * are found on the host before anything is enqueued.  Kernels never trap:
+ * every wait on the device is bounded, and an expired wait is recorded in a
+ * device-side error word that fa_get_device_status() reports and clears.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *fa_stream_t;
+
+enum fa_dtype { FA_F16 = 0, FA_BF16 = 1 };
+
+enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size, H % Hkv != 0, scale <= 0 */
+  FA_ERR_UNSUPPORTED = 2, /* head dim, dtype or device (not sm_103) not supported */
+  FA_ERR_CUDA = 3,        /* a CUDA call failed; fa_strerror(FA_ERR_CUDA) has its text */
+  FA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (from fa_get_device_status) */
+  FA_ERR_WORKSPACE = 5    /* backward workspace missing or smaller than fa_bwd_workspace_size */
+};
+
+/*
+ * Forward pass.  Writes o [B][H][N][d] (dtype) and lse [B][H][N] (fp32).
+ * q, k, v, o must be 16-byte aligned device pointers, lse 4-byte aligned.
+ * scale must be finite and > 0 (1/sqrt(d) is the usual value); B and H are
+ * at most 65535.  causal is 0 or 1.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+           int Hkv, int N, int d, int causal, float scale, int dtype, fa_stream_t stream);
+
+/*
+ * Bytes of device scratch fa_bwd needs for this shape: the fp32 row vector
+ * D = rowsum(dO o O) [B][H][N] and an fp32 dQ accumulator [B][H][N][d].
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
+
+/*
+ * Backward pass of the forward above, for the same arguments.  o and lse are
+ * the forward's outputs; dout is the upstream gradient dO.  Writes dq
+ * [B][H][N][d], dk and dv [B][Hkv][N][d] (dtype; dk/dv summed over the query
+ * heads that share each key/value head).  workspace must be a device buffer
+ * of at least fa_bwd_workspace_size(...) bytes, 256-byte aligned; its
+ * contents on entry do not matter and are garbage on exit.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
+           int causal, float scale, int dtype, void *workspace, size_t workspace_bytes,
+           fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports (and clears) the device-side error
+ * word: FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, FA_ERR_CUDA if the stream itself failed, FA_OK otherwise.
+ */
+int fa_get_device_status(fa_stream_t stream);
+
+/* Static text for a status; for FA_ERR_CUDA, the text of the last CUDA error
+ * seen by this thread. */
+const char *fa_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,49 @@
+"""Error metrics and tolerances for GPU-vs-oracle parity.
+
+Tolerances (fp16/bf16 inputs, fp32 accumulation):
+  O    max |x - y| <= 1e-2 and ||x - y||_2 / ||y||_2 <= 5e-3
+  L    max |x - y| <= 1e-3
+  dQ, dK, dV   ||x - y||_2 / ||y||_2 <= 2e-2
+with y the fp64 oracle.
+"""
+import numpy as np
+
+O_MAX_ABS = 1e-2
+O_REL_L2 = 5e-3
+LSE_MAX_ABS = 1e-3
+GRAD_REL_L2 = 2e-2
+
+
+def to_np(t):
+    if hasattr(t, "detach"):
+        return t.detach().double().cpu().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def max_abs(x, ref) -> float:
+    x, ref = to_np(x), to_np(ref)
+    return float(np.abs(x - ref).max()) if x.size else 0.0
+
+
+def rel_l2(x, ref) -> float:
+    x, ref = to_np(x), to_np(ref)
+    den = float(np.linalg.norm(ref))
+    return float(np.linalg.norm(x - ref)) / (den if den > 0 else 1.0)
+
+
+def check_forward(o, lse, o_ref, lse_ref, what=""):
+    e1, e2, e3 = max_abs(o, o_ref), rel_l2(o, o_ref), max_abs(lse, lse_ref)
+    assert np.isfinite(to_np(o)).all(), f"{what}: non-finite O"
+    assert e1 <= O_MAX_ABS and e2 <= O_REL_L2 and e3 <= LSE_MAX_ABS, \
+        f"{what}: O max_abs {e1:.3e} rel_l2 {e2:.3e}, LSE max_abs {e3:.3e}"
+    return e1, e2, e3
+
+
+def check_grads(pairs, what=""):
+    errs = {}
+    for name, x, ref in pairs:
+        assert np.isfinite(to_np(x)).all(), f"{what}: non-finite {name}"
+        errs[name] = rel_l2(x, ref)
+    bad = {k: v for k, v in errs.items() if v > GRAD_REL_L2}
+    assert not bad, f"{what}: gradient rel_l2 over {GRAD_REL_L2}: {errs}"
+    return errs

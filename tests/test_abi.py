@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_20_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        from exact_io_aware_20_gb300 import build
+        build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(binding.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr), name
+
+
+def test_strerror(lib):
+    for st in range(6):
+        assert binding.strerror(st)
+    assert binding.strerror(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    B, H, N, d = 2, 4, 100, 64
+    want = (-(-B * H * N * 4 // 256)) * 256 + (-(-B * H * N * d * 4 // 256)) * 256
+    assert binding.fa_bwd_workspace_size(B, H, 2, N, d) == want
+    assert binding.fa_bwd_workspace_size(B, H, 3, N, d) == 0   # H % Hkv
+    assert binding.fa_bwd_workspace_size(0, H, 2, N, d) == 0
+    assert binding.fa_bwd_workspace_size(B, H, 2, N, 96) == 0
+
+
+FAKE = 1 << 20   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(B=0), binding.FA_ERR_INVALID_ARG),
+    (dict(N=0), binding.FA_ERR_INVALID_ARG),
+    (dict(Hkv=3), binding.FA_ERR_INVALID_ARG),
+    (dict(causal=2), binding.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), binding.FA_ERR_INVALID_ARG),
+    (dict(B=65536), binding.FA_ERR_INVALID_ARG),
+    (dict(d=96), binding.FA_ERR_UNSUPPORTED),
+    (dict(d=32), binding.FA_ERR_UNSUPPORTED),
+    (dict(dtype=2), binding.FA_ERR_UNSUPPORTED),
+    (dict(q=None), binding.FA_ERR_INVALID_ARG),
+    (dict(lse=None), binding.FA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), binding.FA_ERR_INVALID_ARG),   # not 16-byte aligned
+])
+def test_fwd_rejects(lib, case, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=4, Hkv=2, N=64, d=64, causal=0,
+             scale=0.125, dtype=binding.FA_BF16)
+    a.update(case)
+    st = lib.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["N"],
+                    a["d"], a["causal"], a["scale"], a["dtype"], None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(H=5), binding.FA_ERR_INVALID_ARG),
+    (dict(dout=None), binding.FA_ERR_INVALID_ARG),
+    (dict(dk=FAKE + 4), binding.FA_ERR_INVALID_ARG),
+    (dict(ws=None), binding.FA_ERR_WORKSPACE),
+    (dict(ws_bytes=16), binding.FA_ERR_WORKSPACE),
+    (dict(ws=FAKE + 16), binding.FA_ERR_WORKSPACE),   # not 256-byte aligned
+    (dict(d=48), binding.FA_ERR_UNSUPPORTED),
+])
+def test_bwd_rejects(lib, case, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, H=4, Hkv=2, N=64, d=64, causal=1, scale=0.125, dtype=binding.FA_F16,
+             ws=FAKE, ws_bytes=1 << 30)
+    a.update(case)
+    st = lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"],
+                    a["dv"], a["B"], a["H"], a["Hkv"], a["N"], a["d"], a["causal"], a["scale"],
+                    a["dtype"], a["ws"], a["ws_bytes"], None)
+    assert st == expect
