@@ -80,28 +80,6 @@ struct FwdParams {
   unsigned int* err;
 };
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
-
-__device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, volatile int* abort) {
-  bool ok = mbar_wait(bar, parity, abort);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Bounded wait used only while winding down (ignores the abort flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  int never = 0;
-  mbar_wait(bar, parity, &never);
-}
-
 template <int D, int BC, bool CAUSAL, bool BF16, int KST, int VST>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -282,17 +260,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int i = 0; i < BC / 2; ++i) {
         const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
         const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
-        rs += p0 + p1;
         pk[i] = pack2<BF16>(p0, p1);
+        // l sums the rounded weights the P V product uses, so the final
+        // division normalises exactly those weights.
+        rs += sum_packed<BF16>(pk[i]);
       }
       l += rs;
       #pragma unroll
       for (int c = 0; c < BC / 64; ++c)
         tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
       tmem_st_wait();
+      // O_DONE completes once per P V product; every phase is consumed here,
+      // in order, so a parity wait can never be confused by a skipped phase.
+      // PV_j cannot start before this thread arrives on P_FULL below, so the
+      // barrier is at most one phase ahead.
+      if (j > 0 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
       if (any && j > 0) {
-        // O holds P_0..P_{j-1} V: wait for the last of those products.
-        if (!wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
+        // O holds P_0..P_{j-1} V, all complete: rescale it.
         tc_fence_after();
         #pragma unroll
         for (int c = 0; c < D / 64; ++c) {

@@ -6,6 +6,9 @@ Tolerances (fp16/bf16 inputs, fp32 accumulation):
   dQ, dK, dV   ||x - y||_2 / ||y||_2 <= 2e-2
 with y the fp64 oracle.
 """
+import json
+import os
+
 import numpy as np
 
 O_MAX_ABS = 1e-2
@@ -31,8 +34,17 @@ def rel_l2(x, ref) -> float:
     return float(np.linalg.norm(x - ref)) / (den if den > 0 else 1.0)
 
 
+def record(what, **errs):
+    """Append the measured errors to $FA_PARITY_LOG (JSON lines), if set."""
+    path = os.environ.get("FA_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": what, **errs}) + "\n")
+
+
 def check_forward(o, lse, o_ref, lse_ref, what=""):
     e1, e2, e3 = max_abs(o, o_ref), rel_l2(o, o_ref), max_abs(lse, lse_ref)
+    record(what, o_max_abs=e1, o_rel_l2=e2, lse_max_abs=e3)
     assert np.isfinite(to_np(o)).all(), f"{what}: non-finite O"
     assert e1 <= O_MAX_ABS and e2 <= O_REL_L2 and e3 <= LSE_MAX_ABS, \
         f"{what}: O max_abs {e1:.3e} rel_l2 {e2:.3e}, LSE max_abs {e3:.3e}"
@@ -44,6 +56,7 @@ def check_grads(pairs, what=""):
     for name, x, ref in pairs:
         assert np.isfinite(to_np(x)).all(), f"{what}: non-finite {name}"
         errs[name] = rel_l2(x, ref)
+    record(what, **{f"{k}_rel_l2": v for k, v in errs.items()})
     bad = {k: v for k, v in errs.items() if v > GRAD_REL_L2}
     assert not bad, f"{what}: gradient rel_l2 over {GRAD_REL_L2}: {errs}"
     return errs
