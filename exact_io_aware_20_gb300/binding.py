@@ -27,7 +27,10 @@ SIGNATURES = {
                     _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
+    "fa_timing_enable": (_i, [_i]),
+    "fa_timing_read": (_i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
+KERNEL_KINDS = ("fwd", "bwd_pre", "bwd_main", "bwd_convert")
 
 _lib = None
 
@@ -150,3 +153,16 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None
 def device_status(stream=None):
     """Synchronise the stream and raise if a kernel reported a bounded-wait timeout."""
     _check(fa_get_device_status(stream), "fa_get_device_status")
+
+
+def timing_enable(capacity: int):
+    """Start (capacity > 0) or stop (0) per-kernel event timing inside the library."""
+    _check(load().fa_timing_enable(int(capacity)), "fa_timing_enable")
+
+
+def timing_read():
+    """{kind: (summed ms, launches)} of the kernels timed since the last read."""
+    ms = (ctypes.c_double * len(KERNEL_KINDS))()
+    n = (ctypes.c_int * len(KERNEL_KINDS))()
+    _check(load().fa_timing_read(ms, n), "fa_timing_read")
+    return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_KINDS)}

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -124,6 +125,31 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int cols, int rows,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+struct TimingState {
+  std::mutex mu;
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int> kind;     // kind of each used slot
+  bool enabled = false;
+};
+TimingState g_timing;
+}  // namespace
+
+int timing_begin(int kind, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  if (!g_timing.enabled || g_timing.kind.size() >= g_timing.start.size()) return -1;
+  const int slot = static_cast<int>(g_timing.kind.size());
+  g_timing.kind.push_back(kind);
+  cudaEventRecord(g_timing.start[slot], stream);
+  return slot;
+}
+
+void timing_end(int slot, cudaStream_t stream) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  if (slot < static_cast<int>(g_timing.stop.size())) cudaEventRecord(g_timing.stop[slot], stream);
+}
+
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
@@ -209,4 +235,50 @@ extern "C" const char* fa_strerror(int status) {
     case FA_ERR_WORKSPACE: return "backward workspace missing, misaligned or too small";
     default: return "unknown status";
   }
+}
+
+extern "C" int fa_timing_enable(int capacity) {
+  std::lock_guard<std::mutex> lk(fa::g_timing.mu);
+  for (cudaEvent_t e : fa::g_timing.start) cudaEventDestroy(e);
+  for (cudaEvent_t e : fa::g_timing.stop) cudaEventDestroy(e);
+  fa::g_timing.start.clear();
+  fa::g_timing.stop.clear();
+  fa::g_timing.kind.clear();
+  fa::g_timing.enabled = false;
+  if (capacity < 0) return FA_ERR_INVALID_ARG;
+  for (int i = 0; i < capacity; ++i) {
+    cudaEvent_t a, b;
+    cudaError_t e = cudaEventCreate(&a);
+    if (e == cudaSuccess) {
+      e = cudaEventCreate(&b);
+      if (e != cudaSuccess) cudaEventDestroy(a);
+    }
+    if (e != cudaSuccess) return fa::cuda_fail(e, "cudaEventCreate");
+    fa::g_timing.start.push_back(a);
+    fa::g_timing.stop.push_back(b);
+  }
+  fa::g_timing.enabled = capacity > 0;
+  return FA_OK;
+}
+
+extern "C" int fa_timing_read(double* ms, int* launches) {
+  if (!ms || !launches) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(fa::g_timing.mu);
+  for (int i = 0; i < FA_NUM_KERNEL_KINDS; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  for (size_t i = 0; i < fa::g_timing.kind.size(); ++i) {
+    cudaError_t e = cudaEventSynchronize(fa::g_timing.stop[i]);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, fa::g_timing.start[i], fa::g_timing.stop[i]);
+    if (e != cudaSuccess) return fa::cuda_fail(e, "timing event");
+    const int k = fa::g_timing.kind[i];
+    if (k >= 0 && k < FA_NUM_KERNEL_KINDS) {
+      ms[k] += t;
+      launches[k] += 1;
+    }
+  }
+  fa::g_timing.kind.clear();
+  return FA_OK;
 }

@@ -35,6 +35,7 @@
 //   d = 128, 256: 64 query rows per step; dQ^T = K^T dS^T (d on lanes).
 //   d = 256 is split over two CTAs by output half of d (S^T and dP^T are
 //   computed by both), because dK + dV for all 256 columns would fill TMEM.
+#include "fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -491,9 +492,11 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   cudaError_t e;
   const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.N;
   // 1. preprocess
+  int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
   bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta, a.dq_acc,
       rows);
+  timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 2. main kernel
   CUtensorMap tq, tk, tv, tdo;
@@ -525,7 +528,9 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.err = pr.err;
   const int n_kv_tiles = (pr.N + kBC - 1) / kBC;
   dim3 grid(n_kv_tiles * (D / DH), pr.Hkv, pr.B);
+  slot = timing_begin(FA_KERNEL_BWD_MAIN, stream);
   kern<<<grid, kBwdThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
+  timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 3. dQ conversion
   if (g_num_sms == 0) {
@@ -537,8 +542,10 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   const size_t n8 = rows * D / 8;
   const unsigned blocks = static_cast<unsigned>(
       std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(g_num_sms) * 8));
+  slot = timing_begin(FA_KERNEL_BWD_CONVERT, stream);
   bwd_convert_dq<BF16><<<blocks, 256, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8,
                                                    pr.scale);
+  timing_end(slot, stream);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -219,7 +220,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int r_tile = quarter * 32 + lane;
     const int row = qt * kBR + r_tile;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
@@ -252,20 +253,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
         m_ref = m_new;
         l *= alpha;
+        l_r *= alpha;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       uint32_t pk[BC / 2];
-      float rs = 0.f;
+      float rs = 0.f, rs_r = 0.f;
       #pragma unroll
       for (int i = 0; i < BC / 2; ++i) {
         const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
         const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
         pk[i] = pack2<BF16>(p0, p1);
-        // l sums the rounded weights the P V product uses, so the final
-        // division normalises exactly those weights.
-        rs += sum_packed<BF16>(pk[i]);
+        rs += p0 + p1;
+        // l_r sums the rounded weights the P V product uses, so the final
+        // division of O normalises exactly those weights; L uses the exact l.
+        rs_r += sum_packed<BF16>(pk[i]);
       }
       l += rs;
+      l_r += rs_r;
       #pragma unroll
       for (int c = 0; c < BC / 64; ++c)
         tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
@@ -298,7 +302,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ------------------------------------------------------------ epilogue
     if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.N;
       const bool in_range = row < p.N;
@@ -360,7 +364,9 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.err = pr.err;
   dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
+  timing_end(slot, stream);
   return cudaGetLastError();
 }
 

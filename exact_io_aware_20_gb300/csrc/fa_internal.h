@@ -43,6 +43,11 @@ struct BwdArgs {
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int cols, int rows, int outer,
                          int box_cols, int box_rows);
 
+// Diagnostics timing (see fa_timing_enable in fa.h): returns a slot to pass
+// to timing_end, or -1 when timing is off or out of event pairs.
+int timing_begin(int kind, cudaStream_t stream);
+void timing_end(int slot, cudaStream_t stream);
+
 cudaError_t launch_fwd(const Problem& p, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 

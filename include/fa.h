@@ -101,6 +101,30 @@ int fa_get_device_status(fa_stream_t stream);
  * seen by this thread. */
 const char *fa_strerror(int status);
 
+/*
+ * Diagnostics: per-kernel timing with CUDA events (not part of the
+ * attention operation; used by the benchmark to time single kernels).
+ *
+ * fa_timing_enable(capacity), capacity > 0, creates `capacity` pairs of CUDA
+ * events on the current device and clears the record; from then on every
+ * kernel launched by fa_fwd / fa_bwd is bracketed by one pair, recorded on
+ * the call's stream, until the pairs run out.  fa_timing_enable(0) stops
+ * recording and destroys the events.  fa_timing_read() waits for the
+ * recorded events, writes the summed elapsed milliseconds and the number of
+ * timed launches per kernel kind into ms[FA_NUM_KERNEL_KINDS] and
+ * launches[FA_NUM_KERNEL_KINDS], and clears the record (recording goes on).
+ * Both return an fa_status.  Timing is process-wide, not per thread.
+ */
+enum fa_kernel_kind {
+  FA_KERNEL_FWD = 0,         /* the forward kernel */
+  FA_KERNEL_BWD_PRE = 1,     /* backward preprocess: D and the zeroed dQ accumulator */
+  FA_KERNEL_BWD_MAIN = 2,    /* backward main kernel: dK, dV and dQ accumulation */
+  FA_KERNEL_BWD_CONVERT = 3, /* backward dQ conversion */
+  FA_NUM_KERNEL_KINDS = 4
+};
+int fa_timing_enable(int capacity);
+int fa_timing_read(double *ms, int *launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,6 +72,10 @@ def load(path: str | None = None):
                                      ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                      _dp, _dp, _dp, _dp, _dp, _dp]
     lib.oracle_bwd_group.restype = None
+    lib.oracle_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                    ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
+                                    ctypes.c_long, ctypes.c_long, _dp, _dp, _dp]
+    lib.oracle_bwd_rows.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     if path is None:
@@ -192,4 +196,25 @@ def backward(q, k, v, dout, causal: bool, scale: float, lib=None):
             dq[b, sl] = g_dq
             dk[b, kh] = g_dk
             dv[b, kh] = g_dv
+    return dq, dk, dv
+
+
+def backward_rows(q_group, k_head, v_head, dout_group, r0: int, r1: int, causal: bool,
+                  scale: float, dk=None, dv=None, lib=None):
+    """Rows [r0, r1) of the flattened G*Nq query rows of one group: their dQ
+    [r1-r0, d], and their contributions added into dk, dv [Nk, d] (new zero
+    arrays unless given).  Returns (dq_rows, dk, dv)."""
+    lib = lib or load()
+    qg, kh, vh, dg = _f64(q_group), _f64(k_head), _f64(v_head), _f64(dout_group)
+    G, Nq, d = qg.shape
+    Nk = kh.shape[0]
+    if not (0 <= r0 <= r1 <= G * Nq):
+        raise ValueError("row range out of bounds")
+    dq = np.zeros((r1 - r0, d))
+    dk = np.zeros((Nk, d)) if dk is None else dk
+    dv = np.zeros((Nk, d)) if dv is None else dv
+    assert dk.dtype == np.float64 and dk.flags.c_contiguous and dk.shape == (Nk, d)
+    assert dv.dtype == np.float64 and dv.flags.c_contiguous and dv.shape == (Nk, d)
+    lib.oracle_bwd_rows(_ptr(qg), _ptr(kh), _ptr(vh), _ptr(dg), G, Nq, Nk, d, int(bool(causal)),
+                        float(scale), int(r0), int(r1), _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv

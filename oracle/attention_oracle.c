@@ -252,6 +252,82 @@ void oracle_bwd_group(const double *q, const double *k, const double *v,
     free(D);
 }
 
+/*
+ * The backward sums run over query rows, so they split by rows.  For the
+ * flattened rows r = g * Nq + i in [r0, r1) of one group, this writes dQ of
+ * those rows into dq [(r - r0)][d] and ADDS their contributions to dk and dv
+ * ([Nk][d], zeroed by the caller).  Summing the calls over any partition of
+ * the G * Nq rows gives oracle_bwd_group's dK and dV.  (Used to time a
+ * bounded sample of a large problem.)
+ */
+void oracle_bwd_rows(const double *q, const double *k, const double *v,
+                     const double *dout, long G, long Nq, long Nk, long d,
+                     int causal, double scale, long r0, long r1, double *dq,
+                     double *dk, double *dv)
+{
+    (void)G;
+    long n = r1 - r0;
+    if (n <= 0)
+        return;
+    double *o = (double *)malloc(sizeof(double) * (size_t)(n * d));
+    double *L = (double *)malloc(sizeof(double) * (size_t)n);
+    double *D = (double *)malloc(sizeof(double) * (size_t)n);
+
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (long t = 0; t < n; ++t) {
+            long r = r0 + t, i = r % Nq;
+            forward_row(q + r * d, k, v, i, Nq, Nk, d, causal, scale, s,
+                        o + t * d, L + t);
+            D[t] = dot(dout + r * d, o + t * d, d);
+        }
+        free(s);
+    }
+
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long t = 0; t < n; ++t) {
+        long r = r0 + t, i = r % Nq;
+        const double *qi = q + r * d, *doi = dout + r * d;
+        double *dqi = dq + t * d;
+        for (long c = 0; c < d; ++c)
+            dqi[c] = 0.0;
+        for (long kk = 0; kk < Nk; ++kk) {
+            if (!allowed(i, kk, Nq, Nk, causal))
+                continue;
+            double sik = scale * dot(qi, k + kk * d, d);
+            double p = weight(sik, L[t]);
+            double dp = dot(doi, v + kk * d, d);
+            double ds = p * (dp - D[t]);
+            for (long c = 0; c < d; ++c)
+                dqi[c] += scale * ds * k[kk * d + c];
+        }
+    }
+
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long kk = 0; kk < Nk; ++kk) {
+        double *dkk = dk + kk * d, *dvk = dv + kk * d;
+        for (long t = 0; t < n; ++t) {
+            long r = r0 + t, i = r % Nq;
+            if (!allowed(i, kk, Nq, Nk, causal))
+                continue;
+            const double *qi = q + r * d, *doi = dout + r * d;
+            double sik = scale * dot(qi, k + kk * d, d);
+            double p = weight(sik, L[t]);
+            double dp = dot(doi, v + kk * d, d);
+            double ds = p * (dp - D[t]);
+            for (long c = 0; c < d; ++c) {
+                dvk[c] += p * doi[c];
+                dkk[c] += scale * ds * qi[c];
+            }
+        }
+    }
+    free(o);
+    free(L);
+    free(D);
+}
+
 /* Number of threads the parallel loops above use. */
 int oracle_num_threads(void)
 {

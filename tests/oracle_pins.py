@@ -354,7 +354,26 @@ def pin_rows_match_group(lib):
             assert np.array_equal(orows[t], o[g, i]) and lrows[t] == lse[g, i]
 
 
+def pin_row_slabs_sum_to_group(lib):
+    """backward_rows over a partition of the query rows reproduces the whole
+    group's gradients (the sums over rows split exactly)."""
+    rng = _rng(23)
+    G, N, d = 2, 19, 5
+    q, k, v, do = _rand(rng, G, N, d), _rand(rng, N, d), _rand(rng, N, d), _rand(rng, G, N, d)
+    for causal in (False, True):
+        dq, dk, dv = oracle.backward_group(q, k, v, do, causal, 0.45, lib)
+        dk_s, dv_s = np.zeros((N, d)), np.zeros((N, d))
+        dq_s = []
+        for (r0, r1) in ((0, 7), (7, 8), (8, 30), (30, 38)):
+            dq_part, _, _ = oracle.backward_rows(q, k, v, do, r0, r1, causal, 0.45, dk_s, dv_s, lib)
+            dq_s.append(dq_part)
+        np.testing.assert_allclose(np.concatenate(dq_s).reshape(G, N, d), dq, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(dk_s, dk, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv_s, dv, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [pin_identical_keys, pin_zero_queries, pin_dominant_score, pin_causal_first_row,
             pin_two_keys_forward, pin_two_keys_backward, pin_rows_are_probabilities,
             pin_permutation_and_shift, pin_gqa_equals_repeated_mha, pin_delta_and_extras,
-            pin_finite_differences, pin_torch_fp64, pin_bottom_right_mask, pin_rows_match_group]
+            pin_finite_differences, pin_torch_fp64, pin_bottom_right_mask, pin_rows_match_group,
+            pin_row_slabs_sum_to_group]
