@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of one attention step (forward + backward) on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+fa_fwd (O, L) then fa_bwd (D, dK, dV, dQ) through the C ABI.  The default
+workload is the GQA long-sequence shape: B=2, Hq=32, Hkv=8, N=8192, d=128,
+bf16, causal.  Throughput counts FLOPs as 4*B*H*N^2*d for the forward
+(halved under the causal mask) plus 2.5x that for the backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own copy of
+the workload (its shard of an N-times larger batch: the (batch, kv-head)
+units are independent, so there is no collective on the data path) and
+`value` is the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_io_aware_20_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (4·B·H·N²·d) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "gqa8k"
+L2_BYTES = 129 * 2**20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_fwd.cu", "exact_io_aware_20_gb300/csrc/fa_bwd.cu",
+                  "exact_io_aware_20_gb300/csrc/sm103_ptx.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from profiles/traffic.txt, if taken on this exact source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kind and \
+                parts[1] == workload and parts[2] == src:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) >= 9:
+                self.rows.append([c.strip() for c in row])
+        return False
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1])]
+        mx = [num(r[2]) for r in self.rows if num(r[2])]
+        power = [num(r[3]) for r in self.rows if num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[5 + i].lower() in ("active", "0x1", "1")})
+        top = max(mx) if mx else None
+        loaded = [s for s in sm if top and s > 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": top,
+                "power_w_max": max(power) if power else None, "samples": len(self.rows),
+                "reasons": reasons}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(w: Workload, target_pairs: float):
+    """A bounded sample of the workload for the CPU oracle: whole (batch,
+    kv-head) groups in order, the last one cut to its final rows (the rows
+    with the most keys under the mask).  Returns ([(b, kh, r0, r1)], pairs)
+    with r0..r1 flattened rows g*N + i of the group, and the number of
+    unmasked query-key pairs it covers."""
+    G = w.H // w.Hkv
+
+    def row_pairs(r):
+        i = r % w.N
+        return (i + 1) if w.causal else w.N
+
+    segments, pairs = [], 0
+    for u in range(w.B * w.Hkv):
+        b, kh = divmod(u, w.Hkv)
+        r1 = G * w.N
+        r0 = r1
+        while r0 > 0 and pairs < target_pairs:
+            r0 -= 1
+            pairs += row_pairs(r0)
+        segments.append((b, kh, r0, r1))
+        if pairs >= target_pairs:
+            break
+    return segments, pairs
+
+
+def run_oracle_sample(w: Workload, q, k, v, do, segments):
+    import oracle
+    G = w.H // w.Hkv
+    t0 = time.perf_counter()
+    for (b, kh, r0, r1) in segments:
+        sl = slice(kh * G, (kh + 1) * G)
+        oracle.backward_rows(q[b, sl], k[b, kh], v[b, kh], do[b, sl], r0, r1, w.causal, w.scale)
+    return time.perf_counter() - t0
+
+
+def describe(segments, pairs, w):
+    G = w.H // w.Hkv
+    parts = [f"(b{b},kvh{kh}) rows {r0}..{r1 - 1} of {G * w.N}" for b, kh, r0, r1 in segments]
+    return (f"fp64 C oracle forward+backward over {len(segments)} (batch, kv-head) group(s) of "
+            f"the {w.name} shape: " + "; ".join(parts) + f" ({pairs} unmasked query-key pairs)")
+
+
+def cpu_baseline(w: Workload, target_seconds: float):
+    """The oracle as it stands, on this host's cores, over a bounded sample."""
+    import oracle
+    q, k, v, do = make_inputs(w)
+    threads = oracle.num_threads()
+    # calibrate on a small slab, then size the sample for ~target_seconds
+    seg, pairs = oracle_sample(w, 4e6)
+    dt = run_oracle_sample(w, q, k, v, do, seg)
+    seg, pairs = oracle_sample(w, pairs / max(dt, 1e-6) * target_seconds)
+    dt = run_oracle_sample(w, q, k, v, do, seg)
+    flops = pairs * 4.0 * w.d * 3.5      # metric FLOPs of these pairs: fwd + 2.5x bwd
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 3), "sample": describe(seg, pairs, w) + f", {threads} threads"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    q, k, v, do = make_inputs(w)
+    import oracle
+    threads = oracle.num_threads()
+    seg, pairs = oracle_sample(w, 16e6)
+    flops = pairs * 4.0 * w.d * 3.5
+    for _ in range(args.warmup):
+        run_oracle_sample(w, q, k, v, do, seg)
+    times = []
+    for _ in range(args.steps):
+        times.append(run_oracle_sample(w, q, k, v, do, seg))
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d} "
+                               f"{w.dtype} causal={int(w.causal)}",
+                   "sample_per_step": describe(seg, pairs, w)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "per step: " + describe(seg, pairs, w)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from exact_io_aware_20_gb300 import binding
+    binding.load()
+
+    w = WORKLOADS[args.workload].with_(seed=WORKLOADS[args.workload].seed + 7919 * rank)
+    q_h, k_h, v_h, do_h = make_inputs(w)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o, lse = binding.forward(q, k, v, w.causal, w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.forward(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream)
+        binding.backward(q, k, v, o, lse, do, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
+                         workspace=ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    binding.device_status()
+
+    # ------------------------------------------------ device-timed region
+    binding.timing_enable(4 * args.steps + 8)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    binding.device_status()
+    kernel_times = binding.timing_read()
+    binding.timing_enable(0)
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops_step = w.flops_fwd() + w.flops_bwd()
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # ------------------------------------------------ end to end through the public API
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    q_p, k_p, v_p, do_p = (pin(t) for t in (q_h, k_h, v_h, do_h))
+    outs_p = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p, do_p))
+    d2h = sum(t.numel() * t.element_size() for t in outs_p)
+
+    def e2e_step():
+        for dst, src in ((q, q_p), (k, k_p), (v, v_p), (do, do_p)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs_p, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    binding.device_status()
+
+    if rank != 0:
+        return 0
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    dom = max(kernel_times, key=lambda kk: kernel_times[kk][0])
+    dom_ms, dom_n = kernel_times[dom]
+    per_launch_ms = dom_ms / max(dom_n, 1)
+    if dom in ("fwd", "bwd_main"):
+        fl = w.flops_fwd() if dom == "fwd" else w.flops_bwd()
+        achieved = fl / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)",
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
+    else:
+        rows = w.B * w.H * w.N
+        by = rows * w.d * 2 * 2 + rows * 4 + rows * w.d * 4 if dom == "bwd_pre" else \
+            rows * w.d * (4 + 2)
+        achieved = by / (per_launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peak_src} copy bandwidth"}
+    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["ms_per_launch"] = round(per_launch_ms, 4)
+
+    kernels = {}
+    for kind, (ms, n) in kernel_times.items():
+        if n:
+            kernels[kind] = {"ms_per_launch": round(ms / n, 4), "launches": n,
+                             "share": round(ms / sum(x[0] for x in kernel_times.values()), 4)}
+    fwd_ms = kernel_times["fwd"][0] / max(kernel_times["fwd"][1], 1)
+    bwd_ms = sum(kernel_times[kk][0] for kk in ("bwd_pre", "bwd_main", "bwd_convert")) / \
+        max(kernel_times["bwd_main"][1], 1)
+    gpu_launches = sum(n for _, n in kernel_times.values())
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d} "
+                               f"{w.dtype} causal={int(w.causal)}, N(0,1) inputs, seed {w.seed}",
+                   "step": "fa_fwd + fa_bwd (O, L, dQ, dK, dV)",
+                   "l2": f"inputs larger than L2: {round(step_bytes(w) / 2**20)} MiB touched per "
+                         f"step vs {L2_BYTES // 2**20} MiB L2",
+                   "parallelism": f"{world} rank(s), one workload copy each, no collective"},
+        "pct_of_peak": {
+            "step": round(value / world / peaks["bf16_tflops"], 4),
+            "fwd": round(w.flops_fwd() / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "bwd": round(w.flops_bwd() / (bwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "denominator": f"{peak_src} bf16 burst {peaks['bf16_tflops']} TFLOP/s"},
+        "fwd_tflops": round(w.flops_fwd() / (fwd_ms * 1e-3) / 1e12, 1),
+        "bwd_tflops": round(w.flops_bwd() / (bwd_ms * 1e-3) / 1e12, 1),
+        "kernels": kernels,
+        "roofline": roof,
+        "e2e": {"value": round(world * flops_step / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
+                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "path": "pinned host Q,K,V,dO -> device, fa_fwd + fa_bwd, O,L,dQ,dK,dV -> pinned host"},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(WORKLOADS[args.workload], args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def step_bytes(w: Workload) -> int:
+    q = w.B * w.H * w.N * w.d * 2
+    kv = w.B * w.Hkv * w.N * w.d * 2
+    rows = w.B * w.H * w.N
+    # fwd: Q,K,V in, O,L out; bwd: Q,K,V,O,dO,L in, dQ,dK,dV out, D and dQ accumulator
+    return (q + 2 * kv + q + rows * 4) + (3 * q + 2 * kv + rows * 4 + q + 2 * kv + rows * 4
+                                          + 2 * rows * w.d * 4)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
