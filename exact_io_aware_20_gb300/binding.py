@@ -25,6 +25,8 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
                     _vp, _sz, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
+                            _i, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_timing_enable": (_i, [_i]),
@@ -103,6 +105,14 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dt
     return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                          _ptr(dk), _ptr(dv), B, H, Hkv, N, d, int(causal), float(scale), dtype,
                          _ptr(workspace), int(workspace_bytes), _stream_ptr(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
+                   stream=None) -> int:
+    """fa_bwd with the library's own fixed device scratch (no allocation)."""
+    return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d, int(causal),
+                                 float(scale), dtype, _stream_ptr(stream))
 
 
 def fa_get_device_status(stream=None) -> int:

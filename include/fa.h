@@ -91,6 +91,27 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            fa_stream_t stream);
 
 /*
+ * fa_bwd for callers that cannot allocate device memory (no counterpart in
+ * the paper: it exists for the caller's memory rules, not for the method).
+ * Plugins whose host interface passes only inputs and outputs, and processes
+ * that must not call cudaMalloc after start-up, have no way to hand fa_bwd
+ * its workspace; this entry point uses a fixed array of
+ * FA_BWD_NOALLOC_SCRATCH_BYTES in the library's own device memory instead
+ * (held on every GPU that loads the library until exit) and allocates
+ * nothing.  Arguments, outputs and semantics are those of fa_bwd without the
+ * workspace.  Problems with fa_bwd_workspace_size(...) above the maximum are
+ * rejected with FA_ERR_WORKSPACE before anything is enqueued.  All calls
+ * share the one array: calls whose work overlaps on the GPU (two streams,
+ * two threads) race and must be ordered by the caller.  The first call on a
+ * device looks up the array's address with that device current, so make it
+ * before any stream capture.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N,
+                   int d, int causal, float scale, int dtype, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device-side error
  * word: FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
  * call, FA_ERR_CUDA if the stream itself failed, FA_OK otherwise.
