@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (smaller profiling captures)")
     return ap.parse_args()
 
 
@@ -266,7 +268,10 @@ def main():
     from exact_io_aware_20_gb300 import binding
     binding.load()
 
-    w = WORKLOADS[args.workload].with_(seed=WORKLOADS[args.workload].seed + 7919 * rank)
+    base = WORKLOADS[args.workload]
+    if args.batch:
+        base = base.with_(B=args.batch)
+    w = base.with_(seed=base.seed + 7919 * rank)
     q_h, k_h, v_h, do_h = make_inputs(w)
     q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     o, lse = binding.forward(q, k, v, w.causal, w.scale)
@@ -411,7 +416,7 @@ def main():
         "clocks": clocks.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(WORKLOADS[args.workload], args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(base, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     return 0
 

@@ -59,13 +59,16 @@ struct BwdLayout {
   static constexpr int kQOff = kVOff + kKBytes;
   static constexpr int kDOOff = kQOff + QST * kQBytes;
   static constexpr int kDSOff = kDOOff + QST * kQBytes;
-  static constexpr int kLDOff = kDSOff + kDSBytes;        // 4 warps x {L*log2e [BR], D [BR]}
-  static constexpr int kBarOff = kLDOff + 4 * 2 * BR * 4;
+  // Two score buffers in TMEM when there is room for them and the Q/dO ring
+  // can hold the next tile while the current one is still in use.
+  static constexpr int kSBuf = (kDqT && QST >= 2) ? 2 : 1;
+  static constexpr int kLDOff = kDSOff + kDSBytes;   // 4 warps x 2 bufs x {-L*log2e, -D} [BR]
+  static constexpr int kBarOff = kLDOff + 4 * 2 * 2 * BR * 4;
   static constexpr int kKVFull = 0;
   static constexpr int kQDFull = 1;
   static constexpr int kQDEmpty = kQDFull + QST;
-  static constexpr int kSFull = kQDEmpty + QST;
-  static constexpr int kDPFull = kSFull + 1;
+  static constexpr int kSFull = kQDEmpty + QST;     // one per score buffer
+  static constexpr int kDPFull = kSFull + 2;
   static constexpr int kPFull = kDPFull + 1;
   static constexpr int kDSFull = kPFull + 1;
   static constexpr int kDSEmpty = kDSFull + 1;
@@ -78,8 +81,8 @@ struct BwdLayout {
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns
-  static constexpr uint32_t kTdV = 0, kTdK = DH, kTS = 2 * DH, kTdP = 2 * DH + BR,
-                            kTdQ = 2 * DH + 2 * BR;
+  static constexpr uint32_t kTdV = 0, kTdK = DH, kTS = 2 * DH, kTdP = 2 * DH + kSBuf * BR,
+                            kTdQ = 2 * DH + (kSBuf + 1) * BR;
   static constexpr uint32_t kDqCols = kDqT ? BR : D;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kTdQ + kDqCols <= kTmemCols, "TMEM budget");
@@ -96,6 +99,7 @@ struct BwdParams {
   int H, Hkv, N, G;
   int n_q_tiles;
   float scale, scale_log2;
+  int heavy_first;   // dispatch order, see bwd_kernel
   unsigned int* err;
 };
 
@@ -115,8 +119,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int jt = blockIdx.x / kNSplit, dh = blockIdx.x % kNSplit;
-  const int kh = blockIdx.y, b = blockIdx.z;
+  // Two dispatch orders (chosen on the host):
+  //  - key tiles vary fastest, so the CTAs of one (batch, kv head) group run
+  //    together and share its Q / dO tiles in L2;
+  //  - heavy first: under the mask the work of a CTA falls with its key tile,
+  //    so when single CTAs are long, every group's heaviest tiles go first and
+  //    the last wave holds only short CTAs.
+  int jt, dh, kh, b;
+  if (p.heavy_first) {
+    jt = blockIdx.y;
+    dh = blockIdx.x % kNSplit;
+    kh = (blockIdx.x / kNSplit) % p.Hkv;
+    b = blockIdx.x / (kNSplit * p.Hkv);
+  } else {
+    jt = blockIdx.x / kNSplit;
+    dh = blockIdx.x % kNSplit;
+    kh = blockIdx.y;
+    b = blockIdx.z;
+  }
   const int kv0 = jt * kBC;
   const int i0 = CAUSAL ? kv0 / BR : 0;        // first query tile with a row >= kv0
   const int n_i = p.n_q_tiles - i0;
@@ -129,6 +149,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_init(bar(L::kQDEmpty + s), 1);
     }
     mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kSFull + 1), 1);
     mbar_init(bar(L::kDPFull), 1);
     mbar_init(bar(L::kPFull), 128);
     mbar_init(bar(L::kDSFull), 128);
@@ -148,7 +169,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tdV = tmem + L::kTdV, tdK = tmem + L::kTdK, tS = tmem + L::kTS,
+  const uint32_t tdV = tmem + L::kTdV, tdK = tmem + L::kTdK, tS0 = tmem + L::kTS,
                  tdP = tmem + L::kTdP, tdQ = tmem + L::kTdQ;
 
   if (warp == 0) {
@@ -193,38 +214,57 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       constexpr uint32_t kIdQ = L::kDqT ? idesc_f16(DH, BR, BF16 ? 1 : 0, 1, 1)
                                         : idesc_f16(BR, D, BF16 ? 1 : 0, 1, 1);
       const uint32_t dh_chunk = static_cast<uint32_t>(dh * (DH / 64));
-      bool ok = mbar_wait(bar(L::kKVFull), 0, abort);
-      for (int t = 0; ok && t < n_steps; ++t) {
-        const int st = t % QST;
-        if (!mbar_wait(bar(L::kQDFull + st), (t / QST) & 1, abort)) break;
+      auto q_smem = [&](int t) { return sbase + L::kQOff + (t % QST) * L::kQBytes; };
+      auto do_smem = [&](int t) { return sbase + L::kDOOff + (t % QST) * L::kQBytes; };
+      auto s_tmem = [&](int t) { return tS0 + (t % L::kSBuf) * BR; };
+      // S^T_t = K Q_t^T (waits for the (Q_t, dO_t) tile).
+      auto issue_s = [&](int t) -> bool {
+        if (!mbar_wait(bar(L::kQDFull + t % QST), (t / QST) & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t q_s = sbase + L::kQOff + st * L::kQBytes;
-        const uint32_t do_s = sbase + L::kDOOff + st * L::kQBytes;
-        // S^T = K Q^T and dP^T = V dO^T (contraction over all of d)
         #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (kBC * 128) + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
-          mma_ss(tS, smem_desc_sw128(sbase + L::kKOff + koff, 16, 1024),
-                 smem_desc_sw128(q_s + qoff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          mma_ss(s_tmem(t), smem_desc_sw128(sbase + L::kKOff + koff, 16, 1024),
+                 smem_desc_sw128(q_smem(t) + qoff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kSFull));
+        mma_commit(bar(L::kSFull + t % L::kSBuf));
+        return true;
+      };
+      // dP^T_t = V dO_t^T (the tile is known to be loaded).
+      auto issue_dp = [&](int t) {
         #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (kBC * 128) + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
           mma_ss(tdP, smem_desc_sw128(sbase + L::kVOff + koff, 16, 1024),
-                 smem_desc_sw128(do_s + qoff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                 smem_desc_sw128(do_smem(t) + qoff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kDPFull));
+      };
+      bool ok = mbar_wait(bar(L::kKVFull), 0, abort);
+      if (ok && L::kSBuf == 2 && n_steps > 0) {
+        ok = issue_s(0);
+        if (ok) issue_dp(0);
+      }
+      for (int t = 0; ok && t < n_steps; ++t) {
+        const int st = t % QST;
+        if constexpr (L::kSBuf == 2) {
+          // The next scores go to the other buffer now, so the P / dS warps
+          // can start on them while this step's products run.
+          if (t + 1 < n_steps && !issue_s(t + 1)) break;
+        } else {
+          if (!issue_s(t)) break;
+          issue_dp(t);
+        }
         // dV += P^T dO (P^T from TMEM, dO MN-major)
         if (!mbar_wait(bar(L::kPFull), t & 1, abort)) break;
         tc_fence_after();
         #pragma unroll
         for (int kk = 0; kk < BR / 16; ++kk) {
           const uint64_t bd =
-              smem_desc_sw128(do_s + dh_chunk * (BR * 128) + kk * 2048, BR * 128, 1024);
-          mma_ts(tdV, tS + kk * 8, bd, kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
+              smem_desc_sw128(do_smem(t) + dh_chunk * (BR * 128) + kk * 2048, BR * 128, 1024);
+          mma_ts(tdV, s_tmem(t) + kk * 8, bd, kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
         }
         // dK += dS^T Q (dS^T K-major in shared memory, Q MN-major)
         if (!mbar_wait(bar(L::kDSFull), t & 1, abort)) break;
@@ -234,7 +274,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           const uint64_t ad = smem_desc_sw128(
               sbase + L::kDSOff + (kk >> 2) * (kBC * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t bd =
-              smem_desc_sw128(q_s + dh_chunk * (BR * 128) + kk * 2048, BR * 128, 1024);
+              smem_desc_sw128(q_smem(t) + dh_chunk * (BR * 128) + kk * 2048, BR * 128, 1024);
           mma_ss(tdK, ad, bd, kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
         }
         // dQ contribution of this key tile
@@ -258,6 +298,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mma_commit(bar(L::kDQFull));
         mma_commit(bar(L::kDSEmpty));
         mma_commit(bar(L::kQDEmpty + st));
+        // The P / dS warps are done with dP^T_t (they signalled dS_t), so the
+        // next dP^T can overwrite it.
+        if constexpr (L::kSBuf == 2) {
+          if (t + 1 < n_steps) issue_dp(t + 1);
+        }
       }
       mma_commit(bar(L::kFinal));
       mma_commit(bar(L::kDrain));
@@ -269,27 +314,50 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int r = quarter * 32 + lane;           // key row within the tile
     const int kv = kv0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // Each warp stages the L (log2 units) and D values of the current query
-    // tile in its own shared-memory slice, so only __syncwarp is needed.
-    float* sL = reinterpret_cast<float*>(smem + L::kLDOff) + (warp - 2) * 2 * BR;
-    float* sD = sL + BR;
+    // Each warp stages -L*log2(e) and -D of a query tile in its own
+    // shared-memory slice (two buffers), loading the next tile's values into
+    // registers while the current tile is processed; only __syncwarp is
+    // needed.
+    float* ld_base = reinterpret_cast<float*>(smem + L::kLDOff) + (warp - 2) * 2 * 2 * BR;
+    constexpr int kPer = BR / 32;
+    float rl[kPer], rd[kPer];
+    auto load_ld = [&](int t) {
+      const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
+      const size_t base = (static_cast<size_t>(b) * p.H + h) * p.N;
+      #pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int q = q0 + lane + 32 * u;
+        rl[u] = q < p.N ? -p.lse[base + q] * kLog2e : -INFINITY;
+        rd[u] = q < p.N ? -p.delta[base + q] : 0.f;
+      }
+    };
+    auto store_ld = [&](int t) {
+      float* dst = ld_base + (t & 1) * 2 * BR;
+      #pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        dst[lane + 32 * u] = rl[u];
+        dst[BR + lane + 32 * u] = rd[u];
+      }
+    };
+    if (n_steps > 0) {
+      load_ld(0);
+      store_ld(0);
+    }
+    __syncwarp();
     bool ok = true;
     for (int t = 0; t < n_steps; ++t) {
-      const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
-      __syncwarp();   // every lane is done with the previous tile's values
-      #pragma unroll
-      for (int c = lane; c < BR; c += 32) {
-        const int q = q0 + c;
-        const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.N + q;
-        sL[c] = q < p.N ? p.lse[idx] * kLog2e : INFINITY;
-        sD[c] = q < p.N ? p.delta[idx] : 0.f;
-      }
-      __syncwarp();
+      const int q0 = (i0 + t % n_i) * BR;
+      const float* sL = ld_base + (t & 1) * 2 * BR;   // -L * log2(e)
+      const float* sD = sL + BR;                       // -D
+      if (t + 1 < n_steps) load_ld(t + 1);             // in flight during this step
+      const uint32_t tS = tS0 + (t % L::kSBuf) * BR;
       // P^T = exp(S^T * scale - L), masked
-      if (!wait_uniform(bar(L::kSFull), t & 1, abort)) { ok = false; break; }
+      if (!wait_uniform(bar(L::kSFull + t % L::kSBuf), (t / L::kSBuf) & 1, abort)) { ok = false; break; }
       tc_fence_after();
       const bool kv_out = kv >= p.N;
       const bool diag = CAUSAL && (q0 < kv0 + kBC);   // tile crosses the diagonal
+      const bool masked = __any_sync(0xffffffffu, kv_out || diag);
+      const f2 cs = {p.scale_log2, p.scale_log2};
       float P[BR];
       #pragma unroll
       for (int c0 = 0; c0 < BR; c0 += 32) {
@@ -297,13 +365,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tmem_ld32(tS + lane_off + c0, sr);
         tmem_ld_wait();
         reg_fence(sr);
-        uint32_t pk[16];
         #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), p.scale_log2, -sL[c0 + c]));
-          if (kv_out || (diag && kv > q0 + c0 + c)) pv = 0.f;
-          P[c0 + c] = pv;
+        for (int c = 0; c < 32; c += 2) {
+          const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs,
+                               f2{sL[c0 + c], sL[c0 + c + 1]});
+          P[c0 + c] = ex2_approx(arg.x);
+          P[c0 + c + 1] = ex2_approx(arg.y);
         }
+        if (masked) {
+          #pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (kv_out || (diag && kv > q0 + c0 + c)) P[c0 + c] = 0.f;
+        }
+        uint32_t pk[16];
         #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(P[c0 + 2 * c], P[c0 + 2 * c + 1]);
         // P^T (16-bit) goes over the first BR/2 columns of the S^T tile,
@@ -328,9 +402,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         uint32_t w[16];
         #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float a = P[c0 + 2 * c] * (__uint_as_float(dr[2 * c]) - sD[c0 + 2 * c]);
-          const float bb = P[c0 + 2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - sD[c0 + 2 * c + 1]);
-          w[c] = pack2<BF16>(a, bb);
+          const f2 diff = fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])},
+                                f2{sD[c0 + 2 * c], sD[c0 + 2 * c + 1]});
+          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]}, diff);
+          w[c] = pack2<BF16>(ds.x, ds.y);
         }
         #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
@@ -343,6 +418,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar(L::kDSFull));
+      if (t + 1 < n_steps) {
+        store_ld(t + 1);   // the other buffer: last read during step t - 1
+        __syncwarp();
+      }
     }
     // ------------------------------------------------------------ dK, dV epilogue
     if (ok && wait_uniform(bar(L::kFinal), 0, abort)) {
@@ -527,18 +606,29 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.scale_log2 = pr.scale * kLog2e;
   p.err = pr.err;
   const int n_kv_tiles = (pr.N + kBC - 1) / kBC;
-  dim3 grid(n_kv_tiles * (D / DH), pr.Hkv, pr.B);
-  slot = timing_begin(FA_KERNEL_BWD_MAIN, stream);
-  kern<<<grid, kBwdThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
-  timing_end(slot, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // 3. dQ conversion
   if (g_num_sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (g_num_sms <= 0) g_num_sms = 148;
   }
+  // Heavy-first order when the longest CTA holds more than a fifth of one
+  // SM's share of the work (long causal rows); otherwise L2 locality wins.
+  p.heavy_first = 0;
+  if (CAUSAL && n_kv_tiles <= 65535) {
+    double total = 0.0;
+    for (int j = 0; j < n_kv_tiles; ++j) total += p.n_q_tiles - (j * kBC) / BR;
+    total *= static_cast<double>(p.G) * (D / DH) * pr.Hkv * pr.B;
+    const double longest = static_cast<double>(p.G) * p.n_q_tiles;
+    p.heavy_first = longest > 0.2 * total / g_num_sms ? 1 : 0;
+  }
+  dim3 grid = p.heavy_first ? dim3((D / DH) * pr.Hkv * pr.B, n_kv_tiles, 1)
+                            : dim3(n_kv_tiles * (D / DH), pr.Hkv, pr.B);
+  slot = timing_begin(FA_KERNEL_BWD_MAIN, stream);
+  kern<<<grid, kBwdThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
+  timing_end(slot, stream);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // 3. dQ conversion
   const size_t n8 = rows * D / 8;
   const unsigned blocks = static_cast<unsigned>(
       std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(g_num_sms) * 8));

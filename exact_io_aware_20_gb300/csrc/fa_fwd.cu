@@ -242,9 +242,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           if (col >= p.N || (CAUSAL && col > row)) s[i] = -INFINITY;
         }
       }
-      float mx = s[0];
+      // Row max as a tree of three-input maxima (independent partial maxima
+      // keep the single warp per sub-partition busy instead of waiting on a
+      // 127-long dependent chain).
+      static_assert(BC % 16 == 0, "row max tree covers 16 columns per step");
+      float mpart[8];
       #pragma unroll
-      for (int i = 1; i < BC; ++i) mx = fmaxf(mx, s[i]);
+      for (int u = 0; u < 8; ++u) mpart[u] = fmaxf(s[2 * u], s[2 * u + 1]);
+      #pragma unroll
+      for (int i = 16; i < BC; i += 16) {
+        #pragma unroll
+        for (int u = 0; u < 8; ++u) mpart[u] = fmax3(mpart[u], s[i + 2 * u], s[i + 2 * u + 1]);
+      }
+      const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
+                             fmaxf(mpart[6], mpart[7]));
       const float m_new = fmaxf(m_ref, mx * p.scale_log2);
       const bool need = m_new > m_ref + kRescaleThreshold;
       const bool any = __any_sync(0xffffffffu, need);
@@ -257,19 +268,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       uint32_t pk[BC / 2];
-      float rs = 0.f, rs_r = 0.f;
+      // Exponent arguments two at a time (packed FMA); four independent
+      // partial sums of each kind (exact, and of the rounded weights).
+      f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      float rs_r[4] = {0.f, 0.f, 0.f, 0.f};
+      const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
       #pragma unroll
       for (int i = 0; i < BC / 2; ++i) {
-        const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
-        const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
-        pk[i] = pack2<BF16>(p0, p1);
-        rs += p0 + p1;
+        const f2 arg = ffma2(f2{s[2 * i], s[2 * i + 1]}, cs, cm);
+        const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
+        pk[i] = pack2<BF16>(pe.x, pe.y);
+        rs[i & 3] = fadd2(rs[i & 3], pe);
         // l_r sums the rounded weights the P V product uses, so the final
         // division of O normalises exactly those weights; L uses the exact l.
-        rs_r += sum_packed<BF16>(pk[i]);
+        rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
       }
-      l += rs;
-      l_r += rs_r;
+      const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+      l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
+      l_r += (rs_r[0] + rs_r[1]) + (rs_r[2] + rs_r[3]);
       #pragma unroll
       for (int c = 0; c < BC / 64; ++c)
         tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));

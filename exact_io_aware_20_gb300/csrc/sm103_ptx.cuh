@@ -261,6 +261,62 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+struct f2 {
+  float x, y;
+};
+__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ f2 fadd2(f2 a, f2 b) {
+  f2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ f2 fmul2(f2 a, f2 b) {
+  f2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// acc + (both 16-bit values packed in w, widened to fp32), with the
+// mixed-precision add (16-bit operand, fp32 accumulator).
+template <bool BF16>
+__device__ __forceinline__ float add_packed(float acc, uint32_t w) {
+  float d;
+  if constexpr (BF16) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %1;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "=f"(d) : "f"(acc), "r"(w));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %1;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+        : "=f"(d) : "f"(acc), "r"(w));
+  }
+  return d;
+}
+
 // Sum of the two 16-bit values packed in w, widened to fp32.
 template <bool BF16>
 __device__ __forceinline__ float sum_packed(uint32_t w) {
