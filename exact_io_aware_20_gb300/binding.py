@@ -29,6 +29,7 @@ SIGNATURES = {
                             _i, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
+    "fa_selftest_expired_wait": (_i, [_i, _vp]),
     "fa_timing_enable": (_i, [_i]),
     "fa_timing_read": (_i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }

@@ -150,6 +150,24 @@ void timing_end(int slot, cudaStream_t stream) {
   if (slot < static_cast<int>(g_timing.stop.size())) cudaEventRecord(g_timing.stop[slot], stream);
 }
 
+// One thread waits, through the attention kernels' bounded wait, on a
+// barrier that nothing completes; the expired wait is reported exactly as in
+// those kernels (bit 0 of the error word).
+__global__ void expired_wait_kernel(unsigned int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t never_done;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&never_done), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool completed = mbar_wait_limit(smem_u32(&never_done), 0, &abort_flag, limit_ns);
+    if (!completed && abort_flag == 2) atomicOr(err, kErrTimeout);
+  }
+}
+
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
@@ -281,4 +299,15 @@ extern "C" int fa_timing_read(double* ms, int* launches) {
   }
   fa::g_timing.kind.clear();
   return FA_OK;
+}
+
+extern "C" int fa_selftest_expired_wait(int limit_us, fa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000) return FA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int st = fa::check_device(&err);
+  if (st != FA_OK) return st;
+  fa::expired_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      err, static_cast<uint64_t>(limit_us) * 1000ull);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : fa::cuda_fail(e, "selftest launch");
 }

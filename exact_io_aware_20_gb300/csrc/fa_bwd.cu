@@ -174,24 +174,28 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the copies.
+    const int zkv = b * p.Hkv + kh;
+    if (elect_one()) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      const int zkv = b * p.Hkv + kh;
       mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kKBytes);
       #pragma unroll
       for (int c = 0; c < L::kNch; ++c) {
         tma_load_3d(sbase + L::kKOff + c * (kBC * 128), &tm_k, bar(L::kKVFull), c * 64, kv0, zkv);
         tma_load_3d(sbase + L::kVOff + c * (kBC * 128), &tm_v, bar(L::kKVFull), c * 64, kv0, zkv);
       }
-      int issued = 0;
-      for (int t = 0; t < n_steps; ++t) {
-        const int st = t % QST;
-        if (t >= QST && !mbar_wait(bar(L::kQDEmpty + st), ((t / QST) + 1) & 1, abort)) break;
-        const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
-        const int zq = b * p.H + h;
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int t = 0; t < n_steps; ++t) {
+      const int st = t % QST;
+      if (t >= QST && !wait_uniform(bar(L::kQDEmpty + st), ((t / QST) + 1) & 1, abort)) break;
+      const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
+      const int zq = b * p.H + h;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kQDFull + st), 2 * L::kQBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c) {
@@ -200,55 +204,68 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           tma_load_3d(sbase + L::kDOOff + st * L::kQBytes + c * (BR * 128), &tm_do,
                       bar(L::kQDFull + st), c * 64, q0, zq);
         }
-        ++issued;
       }
-      drain_wait(bar(L::kKVFull), 0);
-      for (int t = max(0, issued - QST); t < issued; ++t)
-        drain_wait(bar(L::kQDFull + t % QST), (t / QST) & 1);
+      __syncwarp();
+      ++issued;
     }
+    drain_wait(bar(L::kKVFull), 0);
+    for (int t = max(0, issued - QST); t < issued; ++t)
+      drain_wait(bar(L::kQDFull + t % QST), (t / QST) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Warp-wide; each tcgen05 instruction is issued by one elected lane.
+    // Descriptors are built once and advanced by constant offsets.
+    {
       constexpr uint32_t kIdS = idesc_f16(kBC, BR, BF16 ? 1 : 0, 0, 0);
       constexpr uint32_t kIdKV = idesc_f16(kBC, DH, BF16 ? 1 : 0, 0, 1);
       constexpr uint32_t kIdQ = L::kDqT ? idesc_f16(DH, BR, BF16 ? 1 : 0, 1, 1)
                                         : idesc_f16(BR, D, BF16 ? 1 : 0, 1, 1);
       const uint32_t dh_chunk = static_cast<uint32_t>(dh * (DH / 64));
-      auto q_smem = [&](int t) { return sbase + L::kQOff + (t % QST) * L::kQBytes; };
-      auto do_smem = [&](int t) { return sbase + L::kDOOff + (t % QST) * L::kQBytes; };
+      // K-major views (LBO unused): K, V, Q stages, dO stages, dS^T.
+      const uint64_t k_kmaj = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
+      const uint64_t v_kmaj = smem_desc_sw128(sbase + L::kVOff, 16, 1024);
+      const uint64_t q_kmaj = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+      const uint64_t do_kmaj = smem_desc_sw128(sbase + L::kDOOff, 16, 1024);
+      const uint64_t ds_kmaj = smem_desc_sw128(sbase + L::kDSOff, 16, 1024);
+      // MN-major views: LBO = distance between 64-column chunks.
+      const uint64_t q_mn = smem_desc_sw128(sbase + L::kQOff, BR * 128, 1024);
+      const uint64_t do_mn = smem_desc_sw128(sbase + L::kDOOff, BR * 128, 1024);
+      const uint64_t k_mn = smem_desc_sw128(sbase + L::kKOff, kBC * 128, 1024);
+      const uint64_t ds_mn = smem_desc_sw128(sbase + L::kDSOff, kBC * 128, 1024);
       auto s_tmem = [&](int t) { return tS0 + (t % L::kSBuf) * BR; };
       // S^T_t = K Q_t^T (waits for the (Q_t, dO_t) tile).
       auto issue_s = [&](int t) -> bool {
-        if (!mbar_wait(bar(L::kQDFull + t % QST), (t / QST) & 1, abort)) return false;
+        if (!wait_uniform(bar(L::kQDFull + t % QST), (t / QST) & 1, abort)) return false;
         tc_fence_after();
+        const uint32_t qs = (t % QST) * L::kQBytes;
         #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (kBC * 128) + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
-          mma_ss(s_tmem(t), smem_desc_sw128(sbase + L::kKOff + koff, 16, 1024),
-                 smem_desc_sw128(q_smem(t) + qoff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t c = kk >> 2, w = kk & 3;
+          mma_ss(s_tmem(t), desc_add(k_kmaj, c * (kBC * 128) + w * 32),
+                 desc_add(q_kmaj, qs + c * (BR * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kSFull + t % L::kSBuf));
         return true;
       };
       // dP^T_t = V dO_t^T (the tile is known to be loaded).
       auto issue_dp = [&](int t) {
+        const uint32_t qs = (t % QST) * L::kQBytes;
         #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (kBC * 128) + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * (BR * 128) + (kk & 3) * 32;
-          mma_ss(tdP, smem_desc_sw128(sbase + L::kVOff + koff, 16, 1024),
-                 smem_desc_sw128(do_smem(t) + qoff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t c = kk >> 2, w = kk & 3;
+          mma_ss(tdP, desc_add(v_kmaj, c * (kBC * 128) + w * 32),
+                 desc_add(do_kmaj, qs + c * (BR * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kDPFull));
       };
-      bool ok = mbar_wait(bar(L::kKVFull), 0, abort);
+      bool ok = wait_uniform(bar(L::kKVFull), 0, abort);
       if (ok && L::kSBuf == 2 && n_steps > 0) {
         ok = issue_s(0);
         if (ok) issue_dp(0);
       }
       for (int t = 0; ok && t < n_steps; ++t) {
         const int st = t % QST;
+        const uint32_t qs = st * L::kQBytes;
         if constexpr (L::kSBuf == 2) {
           // The next scores go to the other buffer now, so the P / dS warps
           // can start on them while this step's products run.
@@ -258,46 +275,39 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           issue_dp(t);
         }
         // dV += P^T dO (P^T from TMEM, dO MN-major)
-        if (!mbar_wait(bar(L::kPFull), t & 1, abort)) break;
+        if (!wait_uniform(bar(L::kPFull), t & 1, abort)) break;
         tc_fence_after();
         #pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk) {
-          const uint64_t bd =
-              smem_desc_sw128(do_smem(t) + dh_chunk * (BR * 128) + kk * 2048, BR * 128, 1024);
-          mma_ts(tdV, s_tmem(t) + kk * 8, bd, kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ts(tdV, s_tmem(t) + kk * 8, desc_add(do_mn, qs + dh_chunk * (BR * 128) + kk * 2048),
+                 kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q (dS^T K-major in shared memory, Q MN-major)
-        if (!mbar_wait(bar(L::kDSFull), t & 1, abort)) break;
+        if (!wait_uniform(bar(L::kDSFull), t & 1, abort)) break;
         tc_fence_after();
         #pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(
-              sbase + L::kDSOff + (kk >> 2) * (kBC * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd =
-              smem_desc_sw128(q_smem(t) + dh_chunk * (BR * 128) + kk * 2048, BR * 128, 1024);
-          mma_ss(tdK, ad, bd, kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ss(tdK, desc_add(ds_kmaj, (kk >> 2) * (kBC * 128) + (kk & 3) * 32),
+                 desc_add(q_mn, qs + dh_chunk * (BR * 128) + kk * 2048), kIdKV,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        // dK was the last reader of Q_t and dO_t: the stage can be refilled.
+        mma_commit(bar(L::kQDEmpty + st));
         // dQ contribution of this key tile
-        if (t > 0 && !mbar_wait(bar(L::kDQEmpty), (t - 1) & 1, abort)) break;
+        if (t > 0 && !wait_uniform(bar(L::kDQEmpty), (t - 1) & 1, abort)) break;
         tc_fence_after();
         #pragma unroll
         for (int kk = 0; kk < kBC / 16; ++kk) {
-          uint64_t ad, bd;
           if constexpr (L::kDqT) {
             // dQ^T = K^T dS^T: A = K^T (d x keys, MN-major), B = dS^T (keys x q, MN-major)
-            ad = smem_desc_sw128(sbase + L::kKOff + dh_chunk * (kBC * 128) + kk * 2048,
-                                 kBC * 128, 1024);
-            bd = smem_desc_sw128(sbase + L::kDSOff + kk * 2048, kBC * 128, 1024);
+            mma_ss(tdQ, desc_add(k_mn, dh_chunk * (kBC * 128) + kk * 2048),
+                   desc_add(ds_mn, kk * 2048), kIdQ, kk > 0 ? 1u : 0u);
           } else {
             // dQ = dS K: A = dS (q x keys, MN-major), B = K (keys x d, MN-major)
-            ad = smem_desc_sw128(sbase + L::kDSOff + kk * 2048, kBC * 128, 1024);
-            bd = smem_desc_sw128(sbase + L::kKOff + kk * 2048, kBC * 128, 1024);
+            mma_ss(tdQ, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), kIdQ,
+                   kk > 0 ? 1u : 0u);
           }
-          mma_ss(tdQ, ad, bd, kIdQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kDQFull));
         mma_commit(bar(L::kDSEmpty));
-        mma_commit(bar(L::kQDEmpty + st));
         // The P / dS warps are done with dP^T_t (they signalled dS_t), so the
         // next dP^T can overwrite it.
         if constexpr (L::kSBuf == 2) {
@@ -652,8 +662,8 @@ cudaError_t dispatch_flags(const Problem& pr, const BwdArgs& a, cudaStream_t s) 
 
 cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
   switch (pr.d) {
-    case 64: return dispatch_flags<64, 64, 128, 2>(pr, a, stream);
-    case 128: return dispatch_flags<128, 128, 64, 2>(pr, a, stream);
+    case 64: return dispatch_flags<64, 64, 128, 3>(pr, a, stream);
+    case 128: return dispatch_flags<128, 128, 64, 3>(pr, a, stream);
     case 256: return dispatch_flags<256, 128, 64, 1>(pr, a, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -133,87 +133,94 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the copies.
+    const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
+    if (elect_one()) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
       mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
       #pragma unroll
       for (int c = 0; c < L::kNch; ++c)
         tma_load_3d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, qt * kBR, zq);
-      int k_issued = 0, v_issued = 0;
-      bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % KST;
-        if (j >= KST && !mbar_wait(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) { ok = false; break; }
+    }
+    __syncwarp();
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j % KST;
+      if (j >= KST && !wait_uniform(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
           tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
                       bar(L::kKFull + s), c * 64, j * BC, zkv);
-        ++k_issued;
-        const int sv = j % VST;
-        if (j >= VST && !mbar_wait(bar(L::kVEmpty + sv), ((j / VST) + 1) & 1, abort)) { ok = false; break; }
+      }
+      __syncwarp();
+      ++k_issued;
+      const int sv = j % VST;
+      if (j >= VST && !wait_uniform(bar(L::kVEmpty + sv), ((j / VST) + 1) & 1, abort)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
           tma_load_3d(sbase + L::kVOff + sv * L::kKVBytes + c * (BC * 128), &tm_v,
                       bar(L::kVFull + sv), c * 64, j * BC, zkv);
-        ++v_issued;
       }
-      // Never leave the CTA with copies in flight: wait for every load this
-      // thread issued (they have completed already on the normal path).
-      drain_wait(bar(L::kQFull), 0);
-      for (int j = max(0, k_issued - KST); j < k_issued; ++j)
-        drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
-      for (int j = max(0, v_issued - VST); j < v_issued; ++j)
-        drain_wait(bar(L::kVFull + j % VST), (j / VST) & 1);
+      __syncwarp();
+      ++v_issued;
     }
+    // Never leave the CTA with copies in flight: wait for every load issued
+    // (they have completed already on the normal path).
+    drain_wait(bar(L::kQFull), 0);
+    for (int j = max(0, k_issued - KST); j < k_issued; ++j)
+      drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
+    for (int j = max(0, v_issued - VST); j < v_issued; ++j)
+      drain_wait(bar(L::kVFull + j % VST), (j / VST) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16(kBR, BC, BF16 ? 1 : 0, 0, 0);
-      constexpr uint32_t kIdO = idesc_f16(kBR, D, BF16 ? 1 : 0, 0, 1);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % KST;
-        if (!mbar_wait(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
-        #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int c = kk >> 2, w = kk & 3;
-          const uint64_t ad = smem_desc_sw128(sbase + L::kQOff + c * (kBR * 128) + w * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(
-              sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128) + w * 32, 16, 1024);
-          mma_ss(d_tmem, ad, bd, kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kSFull + (j & 1)));
-        mma_commit(bar(L::kKEmpty + s));
-        return true;
-      };
-      bool ok = mbar_wait(bar(L::kQFull), 0, abort);
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
-        const int sv = j % VST;
-        if (!mbar_wait(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
-        tc_fence_after();
-        const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
-        #pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk) {
-          const uint64_t bd =
-              smem_desc_sw128(sbase + L::kVOff + sv * L::kKVBytes + kk * 2048, BC * 128, 1024);
-          mma_ts(tO, a_tmem + kk * 8, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(L::kODone));
-        mma_commit(bar(L::kVEmpty + sv));
+    // Warp-wide; each tcgen05 instruction is issued by one elected lane.
+    // Descriptors are built once and advanced by constant offsets.
+    constexpr uint32_t kIdS = idesc_f16(kBR, BC, BF16 ? 1 : 0, 0, 0);
+    constexpr uint32_t kIdO = idesc_f16(kBR, D, BF16 ? 1 : 0, 0, 1);
+    const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+    const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
+    const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
+    auto issue_s = [&](int j) -> bool {
+      const int s = j % KST;
+      if (!wait_uniform(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
+      tc_fence_after();
+      const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
+      const uint64_t ks = desc_add(k_desc, s * L::kKVBytes);
+      #pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t c = kk >> 2, w = kk & 3;
+        mma_ss(d_tmem, desc_add(q_desc, c * (kBR * 128) + w * 32),
+               desc_add(ks, c * (BC * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
       }
-      // Every MMA issued above completes before TMEM is released.
-      mma_commit(bar(L::kDrain));
-      drain_wait(bar(L::kDrain), 0);
+      mma_commit(bar(L::kSFull + (j & 1)));
+      mma_commit(bar(L::kKEmpty + s));
+      return true;
+    };
+    bool ok = wait_uniform(bar(L::kQFull), 0, abort);
+    if (ok) ok = issue_s(0);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      if (j + 1 < n_kv && !issue_s(j + 1)) break;
+      if (!wait_uniform(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
+      const int sv = j % VST;
+      if (!wait_uniform(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
+      tc_fence_after();
+      const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
+      const uint64_t vs = desc_add(v_desc, sv * L::kKVBytes);
+      #pragma unroll
+      for (int kk = 0; kk < BC / 16; ++kk)
+        mma_ts(tO, a_tmem + kk * 8, desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar(L::kODone));
+      mma_commit(bar(L::kVEmpty + sv));
     }
+    // Every MMA issued above completes before TMEM is released.
+    mma_commit(bar(L::kDrain));
+    drain_wait(bar(L::kDrain), 0);
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;                 // TMEM lanes this warp may access

@@ -136,6 +136,16 @@ const char *fa_strerror(int status);
  * launches[FA_NUM_KERNEL_KINDS], and clears the record (recording goes on).
  * Both return an fa_status.  Timing is process-wide, not per thread.
  */
+/*
+ * Diagnostics: checks the failure-detection path.  Launches one thread that
+ * waits, through the same bounded wait the attention kernels use, on an
+ * mbarrier that nothing ever completes; after limit_us microseconds (1 to
+ * 2,000,000) the wait gives up and records the expiry in the device error
+ * word, so the next fa_get_device_status(stream) returns FA_ERR_TIMEOUT and
+ * the CUDA context stays usable.  Returns an fa_status for the launch.
+ */
+int fa_selftest_expired_wait(int limit_us, fa_stream_t stream);
+
 enum fa_kernel_kind {
   FA_KERNEL_FWD = 0,         /* the forward kernel */
   FA_KERNEL_BWD_PRE = 1,     /* backward preprocess: D and the zeroed dQ accumulator */
