@@ -47,10 +47,16 @@ struct FwdLayout {
   static constexpr int kNch = D / 64;                 // 64-column (128-byte) chunks
   static constexpr int kQBytes = kBR * D * 2;
   static constexpr int kKVBytes = BC * D * 2;
+  // For d <= 128 each V stage is followed by a 64-column chunk of ones, so
+  // the P V product, widened to N = d + 16, also sums the rounded weights of
+  // every row into 16 extra TMEM columns (the row sum l_r without ALU work).
+  static constexpr bool kOnes = D <= 128;
+  static constexpr int kOnesCols = kOnes ? 16 : 0;
+  static constexpr int kVStage = kKVBytes + (kOnes ? BC * 128 : 0);
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBytes;
   static constexpr int kVOff = kKOff + KST * kKVBytes;
-  static constexpr int kBarOff = kVOff + VST * kKVBytes;
+  static constexpr int kBarOff = kVOff + VST * kVStage;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kKFull = 1;
@@ -68,7 +74,7 @@ struct FwdLayout {
   // TMEM columns
   static constexpr uint32_t kS0 = 0, kS1 = BC, kO = 2 * BC;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kO + D <= kTmemCols, "TMEM budget");
+  static_assert(kO + D + kOnesCols <= kTmemCols, "TMEM budget");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -125,6 +131,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (L::kOnes) {
+    if (warp >= 2) {
+      // the ones chunks (any layout of all-ones is all-ones), written once
+      const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
+      for (int sv = 0; sv < VST; ++sv) {
+        uint4* dst = reinterpret_cast<uint4*>(smem + L::kVOff + sv * L::kVStage + L::kKVBytes);
+        for (int i = threadIdx.x - 64; i < BC * 128 / 16; i += 128)
+          dst[i] = make_uint4(one2, one2, one2, one2);
+      }
+      fence_proxy_async_smem();
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -164,7 +182,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kVOff + sv * L::kKVBytes + c * (BC * 128), &tm_v,
+          tma_load_3d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
                       bar(L::kVFull + sv), c * 64, j * BC, zkv);
       }
       __syncwarp();
@@ -182,7 +200,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // Warp-wide; each tcgen05 instruction is issued by one elected lane.
     // Descriptors are built once and advanced by constant offsets.
     constexpr uint32_t kIdS = idesc_f16(kBR, BC, BF16 ? 1 : 0, 0, 0);
-    constexpr uint32_t kIdO = idesc_f16(kBR, D, BF16 ? 1 : 0, 0, 1);
+    constexpr uint32_t kIdO = idesc_f16(kBR, D + L::kOnesCols, BF16 ? 1 : 0, 0, 1);
     const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
     const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
     const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
@@ -211,7 +229,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (!wait_uniform(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
       tc_fence_after();
       const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
-      const uint64_t vs = desc_add(v_desc, sv * L::kKVBytes);
+      const uint64_t vs = desc_add(v_desc, sv * L::kVStage);
       #pragma unroll
       for (int kk = 0; kk < BC / 16; ++kk)
         mma_ts(tO, a_tmem + kk * 8, desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
@@ -288,7 +306,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         rs[i & 3] = fadd2(rs[i & 3], pe);
         // l_r sums the rounded weights the P V product uses, so the final
         // division of O normalises exactly those weights; L uses the exact l.
-        rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
+        // With the ones chunk the tensor core forms l_r next to O instead.
+        if constexpr (!L::kOnes) rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
       }
       const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
       l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
@@ -317,6 +336,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           tmem_st32(tO + lane_off + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
           tmem_st32(tO + lane_off + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
         }
+        if constexpr (L::kOnes) {
+          uint32_t lr[16];
+          tmem_ld16(tO + lane_off + D, lr);
+          tmem_ld_wait();
+          reg_fence(lr);
+          #pragma unroll
+          for (int i = 0; i < 16; ++i) lr[i] = __float_as_uint(__uint_as_float(lr[i]) * alpha);
+          tmem_st16(tO + lane_off + D, lr);
+        }
         tmem_st_wait();
       }
       tc_fence_before();
@@ -325,6 +353,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ------------------------------------------------------------ epilogue
     if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
       tc_fence_after();
+      if constexpr (L::kOnes) {
+        uint32_t lr[16];
+        tmem_ld16(tO + lane_off + D, lr);
+        tmem_ld_wait();
+        reg_fence(lr);
+        l_r = __uint_as_float(lr[0]);
+      }
       const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.N;
