@@ -25,6 +25,8 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
                     _vp, _sz, _vp]),
+    "fa_bwd_deterministic": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                  _i, _f, _i, _vp, _sz, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
                             _i, _vp]),
     "fa_get_device_status": (_i, [_vp]),
@@ -33,7 +35,7 @@ SIGNATURES = {
     "fa_timing_enable": (_i, [_i]),
     "fa_timing_read": (_i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
-KERNEL_KINDS = ("fwd", "bwd_pre", "bwd_main", "bwd_convert")
+KERNEL_KINDS = ("fwd", "bwd_pre", "bwd_main", "bwd_convert", "bwd_dq")
 
 _lib = None
 
@@ -108,6 +110,14 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dt
                          _ptr(workspace), int(workspace_bytes), _stream_ptr(stream))
 
 
+def fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
+                         workspace, workspace_bytes, stream=None) -> int:
+    return load().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d, int(causal),
+                                       float(scale), dtype, _ptr(workspace), int(workspace_bytes),
+                                       _stream_ptr(stream))
+
+
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
                    stream=None) -> int:
     """fa_bwd with the library's own fixed device scratch (no allocation)."""
@@ -146,8 +156,9 @@ def forward(q, k, v, causal: bool, scale: float, out=None, lse=None, stream=None
 
 
 def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
-    """(dq, dk, dv) of sum(O o dO); outputs and scratch are allocated unless given."""
+             workspace=None, stream=None, deterministic: bool = False):
+    """(dq, dk, dv) of sum(O o dO); outputs and scratch are allocated unless given.
+    deterministic=True uses fa_bwd_deterministic (bitwise reproducible dQ)."""
     B, H, Hkv, N, d = _shapes(q, k, v)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -155,9 +166,10 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None
     need = fa_bwd_workspace_size(B, H, Hkv, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    _check(fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
-                  _dtype_code(q), workspace, workspace.numel() * workspace.element_size(),
-                  stream), "fa_bwd")
+    fn = fa_bwd_deterministic if deterministic else fa_bwd
+    _check(fn(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
+              _dtype_code(q), workspace, workspace.numel() * workspace.element_size(),
+              stream), "fa_bwd_deterministic" if deterministic else "fa_bwd")
     return dq, dk, dv
 
 

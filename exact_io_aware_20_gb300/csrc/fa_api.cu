@@ -202,10 +202,38 @@ extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   return fa::bwd_workspace_bytes(B, H, N, d);
 }
 
+namespace fa {
+namespace {
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+               int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+               fa_stream_t stream, int deterministic);
+}  // namespace
+}  // namespace fa
+
 extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o,
                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                       int H, int Hkv, int N, int d, int causal, float scale, int dtype,
                       void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
+                        workspace, workspace_bytes, stream, 0);
+}
+
+extern "C" int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk,
+                                    void* dv, int B, int H, int Hkv, int N, int d, int causal,
+                                    float scale, int dtype, void* workspace,
+                                    size_t workspace_bytes, fa_stream_t stream) {
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
+                        workspace, workspace_bytes, stream, 1);
+}
+
+namespace fa {
+namespace {
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+               int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+               fa_stream_t stream, int deterministic) {
   Problem pr;
   int st = fa::validate(B, H, Hkv, N, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
@@ -222,11 +250,13 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   float* delta = static_cast<float*>(workspace);
   float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);
-  fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc};
+  fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};
   cudaError_t e = fa::launch_bwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fa::cuda_fail(e, "fa_bwd launch");
   return FA_OK;
 }
+}  // namespace
+}  // namespace fa
 
 extern "C" int fa_get_device_status(fa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

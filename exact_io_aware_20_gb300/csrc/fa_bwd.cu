@@ -100,6 +100,7 @@ struct BwdParams {
   int n_q_tiles;
   float scale, scale_log2;
   int heavy_first;   // dispatch order, see bwd_kernel
+  int with_dq;       // 0: dK and dV only (dQ comes from the query-outer kernel)
   unsigned int* err;
 };
 
@@ -292,6 +293,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // dK was the last reader of Q_t and dO_t: the stage can be refilled.
         mma_commit(bar(L::kQDEmpty + st));
         // dQ contribution of this key tile
+        if (p.with_dq) {
         if (t > 0 && !wait_uniform(bar(L::kDQEmpty), (t - 1) & 1, abort)) break;
         tc_fence_after();
         #pragma unroll
@@ -307,6 +309,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           }
         }
         mma_commit(bar(L::kDQFull));
+        }
         mma_commit(bar(L::kDSEmpty));
         // The P / dS warps are done with dP^T_t (they signalled dS_t), so the
         // next dP^T can overwrite it.
@@ -469,7 +472,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    for (int t = 0; t < n_steps; ++t) {
+    for (int t = 0; p.with_dq && t < n_steps; ++t) {
       const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
       if (!wait_uniform(bar(L::kDQFull), t & 1, abort)) break;
       tc_fence_after();
@@ -554,6 +557,7 @@ bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout
   #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) delta[row] = acc;
+  if (dq_acc == nullptr) return;
   float* arow = dq_acc + row * D + lane * kPer;
   #pragma unroll
   for (int i = 0; i < kPer; i += 2) *reinterpret_cast<float2*>(arow + i) = make_float2(0.f, 0.f);
@@ -583,8 +587,8 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   // 1. preprocess
   int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
   bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta, a.dq_acc,
-      rows);
+      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
+      a.deterministic ? nullptr : a.dq_acc, rows);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 2. main kernel
@@ -615,6 +619,7 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.err = pr.err;
+  p.with_dq = a.deterministic ? 0 : 1;
   const int n_kv_tiles = (pr.N + kBC - 1) / kBC;
   if (g_num_sms == 0) {
     int dev = 0;
@@ -638,7 +643,8 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   kern<<<grid, kBwdThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // 3. dQ conversion
+  // 3. dQ: the query-outer kernel (deterministic) or the accumulator's conversion
+  if (a.deterministic) return launch_bwd_dq(pr, a, stream);
   const size_t n8 = rows * D / 8;
   const unsigned blocks = static_cast<unsigned>(
       std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(g_num_sms) * 8));

@@ -35,7 +35,8 @@ struct BwdArgs {
   void* dk;
   void* dv;
   float* delta;    // [B, H, N] fp32 scratch
-  float* dq_acc;   // [B, H, N, d] fp32 scratch
+  float* dq_acc;   // [B, H, N, d] fp32 scratch (unused when deterministic)
+  int deterministic;   // dQ from the query-outer kernel, without atomics
 };
 
 // Encode a 3-D tiled tensor map over a [outer, rows, cols] 16-bit tensor
@@ -50,6 +51,8 @@ void timing_end(int slot, cudaStream_t stream);
 
 cudaError_t launch_fwd(const Problem& p, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, cudaStream_t stream);
+// Deterministic dQ (query-outer, no atomics); needs D in a.delta.
+cudaError_t launch_bwd_dq(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 
 // Bytes of backward scratch for a problem (delta + dq accumulator, each
 // rounded up to 256 bytes).

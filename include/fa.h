@@ -91,6 +91,23 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            fa_stream_t stream);
 
 /*
+ * fa_bwd with a bitwise reproducible dQ.  fa_bwd sums the dQ contributions
+ * of the key/value tiles with atomic adds, whose order varies from run to run
+ * (the pages use atomic adds here and do not discuss the non-determinism:
+ * "FlashAttention-2: Faster Attention with Better Parallelism and Work
+ * Partitioning", paper digest, section 7).  This entry point instead computes
+ * dQ in a query-outer kernel that owns each query tile and walks the key
+ * tiles in a fixed order (two extra products per tile: S and dP are formed
+ * again); dK and dV come from the same key-outer kernel as in fa_bwd, in a
+ * mode without dQ.  Same arguments, layouts and workspace as fa_bwd; every
+ * output is the same bits on every run.
+ */
+int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                         int H, int Hkv, int N, int d, int causal, float scale, int dtype,
+                         void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * fa_bwd for callers that cannot allocate device memory (no counterpart in
  * the paper: it exists for the caller's memory rules, not for the method).
  * Plugins whose host interface passes only inputs and outputs, and processes
@@ -151,7 +168,8 @@ enum fa_kernel_kind {
   FA_KERNEL_BWD_PRE = 1,     /* backward preprocess: D and the zeroed dQ accumulator */
   FA_KERNEL_BWD_MAIN = 2,    /* backward main kernel: dK, dV and dQ accumulation */
   FA_KERNEL_BWD_CONVERT = 3, /* backward dQ conversion */
-  FA_NUM_KERNEL_KINDS = 4
+  FA_KERNEL_BWD_DQ = 4,      /* deterministic backward: query-outer dQ kernel */
+  FA_NUM_KERNEL_KINDS = 5
 };
 int fa_timing_enable(int capacity);
 int fa_timing_read(double *ms, int *launches);
