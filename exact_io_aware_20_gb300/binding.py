@@ -22,6 +22,9 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_E
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_fwd_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                       _i, _i, _vp, _sz, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
                     _vp, _sz, _vp]),
@@ -132,26 +135,32 @@ def fa_get_device_status(stream=None) -> int:
 
 # ---------------------------------------------------------------- tensor helpers
 def _shapes(q, k, v):
+    """(B, H, Hkv, Nq, Nk, d) of q [B,H,Nq,d], k and v [B,Hkv,Nk,d]."""
     if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
-        raise ValueError("expected q [B,H,N,d], k and v [B,Hkv,N,d]")
-    B, H, N, d = q.shape
-    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError("expected q [B,H,Nq,d], k and v [B,Hkv,Nk,d]")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[3] != d:
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)}")
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
             raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
-    return B, H, k.shape[1], N, d
+    return B, H, k.shape[1], Nq, k.shape[2], d
 
 
 def forward(q, k, v, causal: bool, scale: float, out=None, lse=None, stream=None):
-    """(o, lse) of exact attention; outputs are allocated unless given."""
-    B, H, Hkv, N, d = _shapes(q, k, v)
+    """(o, lse) of exact attention; outputs are allocated unless given.  The
+    key length may differ from the query length (causal mask bottom-right)."""
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check(fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, causal, scale, _dtype_code(q), stream),
-           "fa_fwd")
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if Nq == Nk:
+        st = fa_fwd(q, k, v, out, lse, B, H, Hkv, Nq, d, causal, scale, _dtype_code(q), stream)
+    else:
+        st = load().fa_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, Nq, Nk,
+                              d, int(causal), float(scale), _dtype_code(q), _stream_ptr(stream))
+    _check(st, "fa_fwd")
     return out, lse
 
 
@@ -159,17 +168,24 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None
              workspace=None, stream=None, deterministic: bool = False):
     """(dq, dk, dv) of sum(O o dO); outputs and scratch are allocated unless given.
     deterministic=True uses fa_bwd_deterministic (bitwise reproducible dQ)."""
-    B, H, Hkv, N, d = _shapes(q, k, v)
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = fa_bwd_workspace_size(B, H, Hkv, N, d)
+    need = fa_bwd_workspace_size(B, H, Hkv, Nq, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    fn = fa_bwd_deterministic if deterministic else fa_bwd
-    _check(fn(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale,
-              _dtype_code(q), workspace, workspace.numel() * workspace.element_size(),
-              stream), "fa_bwd_deterministic" if deterministic else "fa_bwd")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if Nq == Nk:
+        fn = fa_bwd_deterministic if deterministic else fa_bwd
+        st = fn(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, d, causal, scale,
+                _dtype_code(q), workspace, ws_bytes, stream)
+    else:
+        st = load().fa_bwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, H, Hkv, Nq, Nk, d, int(causal), float(scale),
+                              _dtype_code(q), int(bool(deterministic)), _ptr(workspace),
+                              ws_bytes, _stream_ptr(stream))
+    _check(st, "fa_bwd_deterministic" if deterministic else "fa_bwd")
     return dq, dk, dv
 
 

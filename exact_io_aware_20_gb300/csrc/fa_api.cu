@@ -79,9 +79,9 @@ int check_device(unsigned int** err) {
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-int validate(int B, int H, int Hkv, int N, int d, int causal, float scale, int dtype,
+int validate(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
              Problem* pr) {
-  if (B < 1 || H < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
   if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
@@ -90,14 +90,17 @@ int validate(int B, int H, int Hkv, int N, int d, int causal, float scale, int d
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   // Every tensor-map dimension and every flat index must fit the kernels'
   // 32-bit coordinates.
-  const long long rows = static_cast<long long>(B) * H * N;
-  if (static_cast<long long>(B) * H > INT32_MAX || rows > (1ll << 31) - 1 ||
-      static_cast<long long>(N) * d > INT32_MAX)
+  const long long rows_q = static_cast<long long>(B) * H * Nq;
+  const long long rows_k = static_cast<long long>(B) * Hkv * Nk;
+  if (static_cast<long long>(B) * H > INT32_MAX || rows_q > (1ll << 31) - 1 ||
+      rows_k > (1ll << 31) - 1 || static_cast<long long>(Nq) * d > INT32_MAX ||
+      static_cast<long long>(Nk) * d > INT32_MAX)
     return FA_ERR_INVALID_ARG;
   pr->B = B;
   pr->H = H;
   pr->Hkv = Hkv;
-  pr->N = N;
+  pr->Nq = Nq;
+  pr->Nk = Nk;
   pr->d = d;
   pr->causal = causal;
   pr->bf16 = dtype == FA_BF16 ? 1 : 0;
@@ -179,35 +182,51 @@ size_t bwd_workspace_bytes(int B, int H, int N, int d) {
 
 using fa::Problem;
 
+namespace fa {
+namespace {
+int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+               fa_stream_t stream) {
+  Problem pr;
+  int st = validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  if ((st = check_device(&pr.err)) != FA_OK) return st;
+  FwdArgs a{q, k, v, o, lse};
+  cudaError_t e = launch_fwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+  return FA_OK;
+}
+}  // namespace
+}  // namespace fa
+
 extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int H, int Hkv, int N, int d, int causal, float scale, int dtype,
                       fa_stream_t stream) {
-  Problem pr;
-  int st = fa::validate(B, H, Hkv, N, d, causal, scale, dtype, &pr);
-  if (st != FA_OK) return st;
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!fa::aligned(q, 16) || !fa::aligned(k, 16) || !fa::aligned(v, 16) || !fa::aligned(o, 16) ||
-      !fa::aligned(lse, 4))
-    return FA_ERR_INVALID_ARG;
-  if ((st = fa::check_device(&pr.err)) != FA_OK) return st;
-  fa::FwdArgs a{q, k, v, o, lse};
-  cudaError_t e = fa::launch_fwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fa::cuda_fail(e, "fa_fwd launch");
-  return FA_OK;
+  return fa::fwd_common(q, k, v, o, lse, B, H, Hkv, N, N, d, causal, scale, dtype, stream);
+}
+
+extern "C" int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                         fa_stream_t stream) {
+  return fa::fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream);
 }
 
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   Problem pr;
-  if (fa::validate(B, H, Hkv, N, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
+  if (fa::validate(B, H, Hkv, N, N, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
   return fa::bwd_workspace_bytes(B, H, N, d);
 }
 
 namespace fa {
 namespace {
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
-               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
-               int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
-               fa_stream_t stream, int deterministic);
+               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+               int Nk, int d, int causal, float scale, int dtype, void* workspace,
+               size_t workspace_bytes, fa_stream_t stream, int deterministic);
 }  // namespace
 }  // namespace fa
 
@@ -215,8 +234,8 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                       int H, int Hkv, int N, int d, int causal, float scale, int dtype,
                       void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
-                        workspace, workspace_bytes, stream, 0);
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, N, d, causal, scale,
+                        dtype, workspace, workspace_bytes, stream, 0);
 }
 
 extern "C" int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
@@ -224,29 +243,39 @@ extern "C" int fa_bwd_deterministic(const void* q, const void* k, const void* v,
                                     void* dv, int B, int H, int Hkv, int N, int d, int causal,
                                     float scale, int dtype, void* workspace,
                                     size_t workspace_bytes, fa_stream_t stream) {
-  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype,
-                        workspace, workspace_bytes, stream, 1);
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, N, d, causal, scale,
+                        dtype, workspace, workspace_bytes, stream, 1);
+}
+
+extern "C" int fa_bwd_qk(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                         int deterministic, void* workspace, size_t workspace_bytes,
+                         fa_stream_t stream) {
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale,
+                        dtype, workspace, workspace_bytes, stream, deterministic);
 }
 
 namespace fa {
 namespace {
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
-               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
-               int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
-               fa_stream_t stream, int deterministic) {
+               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+               int Nk, int d, int causal, float scale, int dtype, void* workspace,
+               size_t workspace_bytes, fa_stream_t stream, int deterministic) {
   Problem pr;
-  int st = fa::validate(B, H, Hkv, N, d, causal, scale, dtype, &pr);
+  int st = fa::validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!fa::aligned(q, 16) || !fa::aligned(k, 16) || !fa::aligned(v, 16) || !fa::aligned(o, 16) ||
       !fa::aligned(dout, 16) || !fa::aligned(dq, 16) || !fa::aligned(dk, 16) ||
       !fa::aligned(dv, 16) || !fa::aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
-  const size_t need = fa::bwd_workspace_bytes(B, H, N, d);
+  const size_t need = fa::bwd_workspace_bytes(B, H, Nq, d);
   if (!workspace || workspace_bytes < need || !fa::aligned(workspace, 256))
     return FA_ERR_WORKSPACE;
   if ((st = fa::check_device(&pr.err)) != FA_OK) return st;
-  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
   float* delta = static_cast<float*>(workspace);
   float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);

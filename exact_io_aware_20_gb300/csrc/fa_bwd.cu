@@ -96,7 +96,9 @@ struct BwdParams {
   float* dq_acc;
   uint16_t* dk;
   uint16_t* dv;
-  int H, Hkv, N, G;
+  int H, Hkv, G;
+  int Nq, Nk;         // query / key lengths
+  int off;            // Nk - Nq: under the mask query i sees keys k <= i + off
   int n_q_tiles;
   float scale, scale_log2;
   int heavy_first;   // dispatch order, see bwd_kernel
@@ -139,7 +141,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     b = blockIdx.z;
   }
   const int kv0 = jt * kBC;
-  const int i0 = CAUSAL ? kv0 / BR : 0;        // first query tile with a row >= kv0
+  // first query tile with a row that sees key kv0 (i + off >= kv0)
+  const int i0 = CAUSAL ? max(0, kv0 - p.off) / BR : 0;
   const int n_i = p.n_q_tiles - i0;
   const int n_steps = p.G * n_i;
 
@@ -336,12 +339,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     float rl[kPer], rd[kPer];
     auto load_ld = [&](int t) {
       const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
-      const size_t base = (static_cast<size_t>(b) * p.H + h) * p.N;
+      const size_t base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
       #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int q = q0 + lane + 32 * u;
-        rl[u] = q < p.N ? -p.lse[base + q] * kLog2e : -INFINITY;
-        rd[u] = q < p.N ? -p.delta[base + q] : 0.f;
+        rl[u] = q < p.Nq ? -p.lse[base + q] * kLog2e : -INFINITY;
+        rd[u] = q < p.Nq ? -p.delta[base + q] : 0.f;
       }
     };
     auto store_ld = [&](int t) {
@@ -367,8 +370,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       // P^T = exp(S^T * scale - L), masked
       if (!wait_uniform(bar(L::kSFull + t % L::kSBuf), (t / L::kSBuf) & 1, abort)) { ok = false; break; }
       tc_fence_after();
-      const bool kv_out = kv >= p.N;
-      const bool diag = CAUSAL && (q0 < kv0 + kBC);   // tile crosses the diagonal
+      const bool kv_out = kv >= p.Nk;
+      const bool diag = CAUSAL && (q0 + p.off < kv0 + kBC);   // tile crosses the diagonal
       const bool masked = __any_sync(0xffffffffu, kv_out || diag);
       const f2 cs = {p.scale_log2, p.scale_log2};
       float P[BR];
@@ -388,7 +391,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         if (masked) {
           #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (kv_out || (diag && kv > q0 + c0 + c)) P[c0 + c] = 0.f;
+            if (kv_out || (diag && kv > q0 + c0 + c + p.off)) P[c0 + c] = 0.f;
         }
         uint32_t pk[16];
         #pragma unroll
@@ -439,8 +442,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // ------------------------------------------------------------ dK, dV epilogue
     if (ok && wait_uniform(bar(L::kFinal), 0, abort)) {
       tc_fence_after();
-      const bool in_range = kv < p.N;
-      const size_t row = (static_cast<size_t>(b) * p.Hkv + kh) * p.N + (in_range ? kv : 0);
+      const bool in_range = kv < p.Nk;
+      const size_t row = (static_cast<size_t>(b) * p.Hkv + kh) * p.Nk + (in_range ? kv : 0);
       uint4* dv_row = reinterpret_cast<uint4*>(p.dv + row * D + dh * DH);
       uint4* dk_row = reinterpret_cast<uint4*>(p.dk + row * D + dh * DH);
       #pragma unroll
@@ -485,17 +488,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       reg_fence(v);
       tc_fence_before();
       mbar_arrive(bar(L::kDQEmpty));
-      const size_t head_row = (static_cast<size_t>(b) * p.H + h) * p.N;
+      const size_t head_row = (static_cast<size_t>(b) * p.H + h) * p.Nq;
       if constexpr (L::kDqT) {
         // lane r = column r of this CTA's half of d; v[c] = dQ[q0 + c][dh*DH + r]
         float* base = p.dq_acc + (head_row + q0) * D + dh * DH + r;
-        const int n_valid = min(BR, p.N - q0);
+        const int n_valid = min(BR, p.Nq - q0);
         #pragma unroll
         for (int c = 0; c < BR; ++c)
           if (c < n_valid) atomicAdd(base + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
       } else {
         // lane r = query row q0 + r; v[c] = dQ[q0 + r][c]
-        if (q0 + r < p.N) {
+        if (q0 + r < p.Nq) {
           float4* base = reinterpret_cast<float4*>(p.dq_acc + (head_row + q0 + r) * D);
           #pragma unroll
           for (int c = 0; c < kCols / 4; ++c)
@@ -583,7 +586,7 @@ template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16>
 cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D, DH, BR, QST>;
   cudaError_t e;
-  const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.N;
+  const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
   // 1. preprocess
   int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
   bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
@@ -593,10 +596,10 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 2. main kernel
   CUtensorMap tq, tk, tv, tdo;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.N, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.N, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.N, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.N, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.Nq, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
   auto kern = bwd_kernel<D, DH, BR, QST, CAUSAL, BF16>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -613,14 +616,16 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.dv = static_cast<uint16_t*>(a.dv);
   p.H = pr.H;
   p.Hkv = pr.Hkv;
-  p.N = pr.N;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.off = pr.Nk - pr.Nq;
   p.G = pr.H / pr.Hkv;
-  p.n_q_tiles = (pr.N + BR - 1) / BR;
+  p.n_q_tiles = (pr.Nq + BR - 1) / BR;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.err = pr.err;
   p.with_dq = a.deterministic ? 0 : 1;
-  const int n_kv_tiles = (pr.N + kBC - 1) / kBC;
+  const int n_kv_tiles = (pr.Nk + kBC - 1) / kBC;
   if (g_num_sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -632,7 +637,7 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.heavy_first = 0;
   if (CAUSAL && n_kv_tiles <= 65535) {
     double total = 0.0;
-    for (int j = 0; j < n_kv_tiles; ++j) total += p.n_q_tiles - (j * kBC) / BR;
+    for (int j = 0; j < n_kv_tiles; ++j) total += p.n_q_tiles - std::max(0, j * kBC - p.off) / BR;
     total *= static_cast<double>(p.G) * (D / DH) * pr.Hkv * pr.B;
     const double longest = static_cast<double>(p.G) * p.n_q_tiles;
     p.heavy_first = longest > 0.2 * total / g_num_sms ? 1 : 0;

@@ -62,7 +62,8 @@ struct DqParams {
   const float* lse;
   const float* delta;
   uint16_t* dq;
-  int H, Hkv, N, G;
+  int H, Hkv, G;
+  int Nq, Nk, off;    // query / key lengths; off = Nk - Nq (bottom-right mask)
   int num_q_tiles;
   float scale, scale_log2;
   unsigned int* err;
@@ -87,8 +88,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         : static_cast<int>(blockIdx.x);
   const int h = blockIdx.y, b = blockIdx.z;
   const int kh = h / p.G;
-  int n_kv = (p.N + kDqBC - 1) / kDqBC;
-  if (CAUSAL) n_kv = min(n_kv, ((qt + 1) * kDqBR + kDqBC - 1) / kDqBC);
+  int n_kv = (p.Nk + kDqBC - 1) / kDqBC;
+  if (CAUSAL) {
+    const int last_key = min((qt + 1) * kDqBR, p.Nq) - 1 + p.off;
+    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / kDqBC + 1);
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQDFull), 1);
@@ -203,7 +207,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // buffer pair before this tile's dQ product.  With one stage K_{j+1}
     // can only arrive after dQ_j (K_j's last reader) has run, so the tiles
     // are processed one after the other.
-    if (ok && KST >= 2) ok = issue_sdp(0);
+    if (ok && KST >= 2 && n_kv > 0) ok = issue_sdp(0);
     for (int j = 0; ok && j < n_kv; ++j) {
       if constexpr (KST >= 2) {
         if (j + 1 < n_kv && !issue_sdp(j + 1)) break;
@@ -228,10 +232,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int quarter = warp & 3;
     const int row = qt * kDqBR + quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const size_t row_idx = (static_cast<size_t>(b) * p.H + h) * p.N + (row < p.N ? row : 0);
+    const size_t row_idx = (static_cast<size_t>(b) * p.H + h) * p.Nq + (row < p.Nq ? row : 0);
     // -L*log2(e) and -D of this thread's row (padding rows: P = 0)
-    const float nL = row < p.N ? -p.lse[row_idx] * kDqLog2e : -INFINITY;
-    const float nD = row < p.N ? -p.delta[row_idx] : 0.f;
+    const float nL = row < p.Nq ? -p.lse[row_idx] * kDqLog2e : -INFINITY;
+    const float nD = row < p.Nq ? -p.delta[row_idx] : 0.f;
     const f2 cs = {p.scale_log2, p.scale_log2}, cl = {nL, nL}, cd = {nD, nD};
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -248,15 +252,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       reg_fence(sr);
       reg_fence(dr);
       const int col0 = j * kDqBC;
-      const bool masked = (CAUSAL && col0 + kDqBC - 1 > qt * kDqBR) || (col0 + kDqBC > p.N);
+      const bool masked =
+          (CAUSAL && col0 + kDqBC - 1 > qt * kDqBR + p.off) || (col0 + kDqBC > p.Nk);
       uint32_t w[kDqBC / 2];
       #pragma unroll
       for (int c = 0; c < kDqBC; c += 2) {
         const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs, cl);
         f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
         if (masked) {
-          if (col0 + c >= p.N || (CAUSAL && col0 + c > row)) pe.x = 0.f;
-          if (col0 + c + 1 >= p.N || (CAUSAL && col0 + c + 1 > row)) pe.y = 0.f;
+          if (col0 + c >= p.Nk || (CAUSAL && col0 + c > row + p.off)) pe.x = 0.f;
+          if (col0 + c + 1 >= p.Nk || (CAUSAL && col0 + c + 1 > row + p.off)) pe.y = 0.f;
         }
         const f2 ds = fmul2(pe, fadd2(f2{__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])}, cd));
         w[c / 2] = pack2<BF16>(ds.x, ds.y);
@@ -268,7 +273,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_arrive(bar(L::kDSFull + (j & 1)));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && wait_uniform(bar(L::kDQDone), 0, abort)) {
+    if (ok && n_kv == 0) {
+      // no row of this tile sees any key: dQ = 0
+      if (row < p.Nq) {
+        uint4* out = reinterpret_cast<uint4*>(p.dq + row_idx * D);
+        #pragma unroll
+        for (int i = 0; i < D / 8; ++i) out[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else if (ok && wait_uniform(bar(L::kDQDone), 0, abort)) {
       tc_fence_after();
       uint4* out = reinterpret_cast<uint4*>(p.dq + row_idx * D);
       #pragma unroll
@@ -282,7 +294,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int i = 0; i < 16; ++i)
           o[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * p.scale,
                              __uint_as_float(v[2 * i + 1]) * p.scale);
-        if (row < p.N) {
+        if (row < p.Nq) {
           #pragma unroll
           for (int i = 0; i < 4; ++i)
             out[c0 / 8 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
@@ -306,10 +318,10 @@ cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t 
   using L = DqLayout<D, KST>;
   CUtensorMap tq, tk, tv, tdo;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.N, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.N, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.N, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.N, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.Nq, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
   auto kern = bwd_dq_kernel<D, KST, CAUSAL, BF16>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -324,9 +336,11 @@ cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t 
   p.dq = static_cast<uint16_t*>(a.dq);
   p.H = pr.H;
   p.Hkv = pr.Hkv;
-  p.N = pr.N;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.off = pr.Nk - pr.Nq;
   p.G = pr.H / pr.Hkv;
-  p.num_q_tiles = (pr.N + kDqBR - 1) / kDqBR;
+  p.num_q_tiles = (pr.Nq + kDqBR - 1) / kDqBR;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kDqLog2e;
   p.err = pr.err;

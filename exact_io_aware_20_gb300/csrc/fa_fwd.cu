@@ -81,7 +81,9 @@ struct FwdLayout {
 struct FwdParams {
   void* o;
   float* lse;
-  int H, Hkv, N, G;
+  int H, Hkv, G;
+  int Nq, Nk;         // query / key lengths
+  int off;            // Nk - Nq: under the mask query i sees keys k <= i + off
   int num_q_tiles;
   float scale_log2;   // scale * log2(e)
   unsigned int* err;
@@ -105,8 +107,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                         : static_cast<int>(blockIdx.x);
   const int h = blockIdx.y, b = blockIdx.z;
   const int kh = h / p.G;
-  int n_kv = (p.N + BC - 1) / BC;
-  if (CAUSAL) n_kv = min(n_kv, ((qt + 1) * kBR + BC - 1) / BC);
+  int n_kv = (p.Nk + BC - 1) / BC;
+  if (CAUSAL) {
+    // last key any row of this tile may see (bottom-right aligned mask);
+    // negative when every row of the tile sees none (only if Nq > Nk)
+    const int last_key = min((qt + 1) * kBR, p.Nq) - 1 + p.off;
+    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
@@ -221,7 +228,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       return true;
     };
     bool ok = wait_uniform(bar(L::kQFull), 0, abort);
-    if (ok) ok = issue_s(0);
+    if (ok && n_kv > 0) ok = issue_s(0);
     for (int j = 0; ok && j < n_kv; ++j) {
       if (j + 1 < n_kv && !issue_s(j + 1)) break;
       if (!wait_uniform(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
@@ -259,12 +266,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       reg_fence(sr);
       float* s = reinterpret_cast<float*>(sr);
       const int col0 = j * BC;
-      const bool need_mask = (CAUSAL && col0 + BC - 1 > qt * kBR) || (col0 + BC > p.N);
+      const bool need_mask = (CAUSAL && col0 + BC - 1 > qt * kBR + p.off) || (col0 + BC > p.Nk);
       if (need_mask) {
         #pragma unroll
         for (int i = 0; i < BC; ++i) {
           const int col = col0 + i;
-          if (col >= p.N || (CAUSAL && col > row)) s[i] = -INFINITY;
+          if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
         }
       }
       // Row max as a tree of three-input maxima (independent partial maxima
@@ -351,7 +358,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_arrive(bar(L::kPFull + (j & 1)));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
+    if (ok && n_kv == 0) {
+      // no row of this tile sees any key: O = 0, L = -inf
+      if (row < p.Nq) {
+        const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + r * D);
+        #pragma unroll
+        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[r] = -INFINITY;
+      }
+    } else if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
       tc_fence_after();
       if constexpr (L::kOnes) {
         uint32_t lr[16];
@@ -362,8 +378,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-      const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.N;
-      const bool in_range = row < p.N;
+      const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
+      const bool in_range = row < p.Nq;
       uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                              (row_base + (in_range ? row : 0)) * D);
       #pragma unroll
@@ -401,9 +417,9 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   using L = FwdLayout<D, BC, KST, VST>;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.N, pr.B * pr.H, 64, kBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.N, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.N, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, kBR)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
+  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
   auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -416,9 +432,11 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   p.lse = a.lse;
   p.H = pr.H;
   p.Hkv = pr.Hkv;
-  p.N = pr.N;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.off = pr.Nk - pr.Nq;
   p.G = pr.H / pr.Hkv;
-  p.num_q_tiles = (pr.N + kBR - 1) / kBR;
+  p.num_q_tiles = (pr.Nq + kBR - 1) / kBR;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.err = pr.err;
   dim3 grid(p.num_q_tiles, pr.H, pr.B);

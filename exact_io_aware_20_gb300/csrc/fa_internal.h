@@ -9,7 +9,9 @@ namespace fa {
 
 // Shapes and pointers of one call, after validation.
 struct Problem {
-  int B, H, Hkv, N, d;
+  int B, H, Hkv;
+  int Nq, Nk;     // query and key lengths (the causal mask is anchored bottom-right)
+  int d;
   int causal;
   int bf16;       // 1 = bf16, 0 = f16
   float scale;
@@ -34,8 +36,8 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* delta;    // [B, H, N] fp32 scratch
-  float* dq_acc;   // [B, H, N, d] fp32 scratch (unused when deterministic)
+  float* delta;    // [B, H, Nq] fp32 scratch
+  float* dq_acc;   // [B, H, Nq, d] fp32 scratch (unused when deterministic)
   int deterministic;   // dQ from the query-outer kernel, without atomics
 };
 

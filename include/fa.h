@@ -71,8 +71,21 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
            int Hkv, int N, int d, int causal, float scale, int dtype, fa_stream_t stream);
 
 /*
+ * Forward pass with separate query and key lengths (prefill with a cached
+ * prefix, decode, cross-attention): q, o [B][H][Nq][d], k, v [B][Hkv][Nk][d],
+ * lse [B][H][Nq].  Under the causal mask query i sees keys k <= i + Nk - Nq
+ * (the mask anchored at the bottom-right corner, so the last query sees every
+ * key; with Nq == Nk this is fa_fwd).  A query row that sees no key (only
+ * when Nq > Nk) gets O = 0 and L = -inf.  Otherwise as fa_fwd.
+ */
+int fa_fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+              int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+              fa_stream_t stream);
+
+/*
  * Bytes of device scratch fa_bwd needs for this shape: the fp32 row vector
- * D = rowsum(dO o O) [B][H][N] and an fp32 dQ accumulator [B][H][N][d].
+ * D = rowsum(dO o O) [B][H][N] and an fp32 dQ accumulator [B][H][N][d]
+ * (N = the query length).
  * Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
@@ -89,6 +102,17 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
            int causal, float scale, int dtype, void *workspace, size_t workspace_bytes,
            fa_stream_t stream);
+
+/*
+ * Backward pass of fa_fwd_qk: separate query and key lengths, the same mask.
+ * dq [B][H][Nq][d], dk, dv [B][Hkv][Nk][d].  deterministic = 1 selects the
+ * reproducible dQ path of fa_bwd_deterministic, 0 the one of fa_bwd.  The
+ * workspace is fa_bwd_workspace_size(B, H, Hkv, Nq, d) bytes.
+ */
+int fa_bwd_qk(const void *q, const void *k, const void *v, const void *o, const float *lse,
+              const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int Nq,
+              int Nk, int d, int causal, float scale, int dtype, int deterministic,
+              void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * fa_bwd with a bitwise reproducible dQ.  fa_bwd sums the dQ contributions
