@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["train", "decode"], default="train",
+                    help="train: fwd+bwd step (the headline); decode: short-query forward")
+    ap.add_argument("--decode-nq", type=int, default=1)
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (smaller profiling captures)")
     return ap.parse_args()
@@ -252,11 +255,59 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------- decode regime
+def run_decode(args):
+    """Short-query forward over a long key cache (decoding after a prefix):
+    memory-bound, so the metric is GB/s of Q, K, V read and O, L written
+    against the measured copy bandwidth.  Times fa_fwd_splitkv (key axis
+    split over CTAs, partials merged) and fa_fwd_qk (one pass)."""
+    torch.cuda.set_device(0)
+    from exact_io_aware_20_gb300 import binding
+    binding.load()
+    B, H, Hkv, Nq, Nk, d = 8, 32, 8, args.decode_nq, 8192, 128
+    w = Workload("decode", B, H, Hkv, Nq, d, "bf16", True, 1006)
+    q, k, v, _ = make_inputs(w, "cuda", Nk=Nk)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Nq, device="cuda")
+    need = int(binding.load().fa_fwd_splitkv_workspace_size(B, H, Hkv, Nq, Nk, d, 0))
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    nbytes = (q.numel() + k.numel() + v.numel() + o.numel()) * 2 + lse.numel() * 4
+    peaks, src = load_peaks()
+    res = {}
+    for name, fn in (("splitkv", lambda: binding.forward_splitkv(q, k, v, True, w.scale, 0, o, lse, ws)),
+                     ("one_pass", lambda: binding.forward(q, k, v, True, w.scale, o, lse))):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    binding.device_status()
+    print(json.dumps({
+        "metric": "decode attention forward GB/s (Q,K,V read + O,L written)", "unit": "GB/s",
+        "value": res["splitkv"]["GB/s"], "higher_is_better": True, "steps": args.steps,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode: B={B} Hq={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} bf16, "
+                               f"causal (bottom-right), inputs larger than L2 ({nbytes >> 20} MiB)"},
+        "peak": {"hbm_gbs": peaks["hbm_gbs"], "source": src},
+        "splitkv": res["splitkv"], "one_pass": res["one_pass"],
+        "splits_auto": need and int(need // (B * H * Nq * (d + 1) * 4)) or 1}), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "decode":
+        return run_decode(args)
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")

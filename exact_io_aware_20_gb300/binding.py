@@ -23,6 +23,9 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_fwd_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp,
+                            _sz, _vp]),
+    "fa_fwd_splitkv_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "fa_bwd_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                        _i, _i, _vp, _sz, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
@@ -205,3 +208,21 @@ def timing_read():
     n = (ctypes.c_int * len(KERNEL_KINDS))()
     _check(load().fa_timing_read(ms, n), "fa_timing_read")
     return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def forward_splitkv(q, k, v, causal: bool, scale: float, num_splits: int = 0, out=None, lse=None,
+                    workspace=None, stream=None):
+    """(o, lse) through fa_fwd_splitkv (key axis split, partials merged on the GPU)."""
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    need = int(load().fa_fwd_splitkv_workspace_size(B, H, Hkv, Nq, Nk, d, int(num_splits)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(load().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, Nq,
+                                 Nk, d, int(causal), float(scale), _dtype_code(q), int(num_splits),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)), "fa_fwd_splitkv")
+    return out, lse

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -184,9 +185,45 @@ using fa::Problem;
 
 namespace fa {
 namespace {
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+// Short queries of a GQA group share one query-row block (see FwdArgs::pack).
+bool pack_groups(int H, int Hkv, int Nq) { return H > Hkv && Nq <= 64; }
+
+// Split count for fa_fwd_splitkv: enough CTAs for about two waves, at least
+// two key tiles per split.
+int auto_splits(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  const int rows = pack_groups(H, Hkv, Nq) ? (H / Hkv) * Nq : Nq;
+  const long long ctas =
+      static_cast<long long>((rows + 127) / 128) * (pack_groups(H, Hkv, Nq) ? Hkv : H) * B;
+  const int n_kv = (Nk + fwd_key_tile(d) - 1) / fwd_key_tile(d);
+  const long long want = 2ll * num_sms();
+  if (ctas >= want) return 1;
+  int sp = static_cast<int>((want + ctas - 1) / ctas);
+  sp = std::min(sp, std::max(1, n_kv / 2));
+  return std::max(1, sp);
+}
+
+size_t splitkv_bytes(int B, int H, int Nq, int d, int splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  const size_t o = (static_cast<size_t>(splits) * rows * d * 4 + 255) / 256 * 256;
+  const size_t l = (static_cast<size_t>(splits) * rows * 4 + 255) / 256 * 256;
+  return o + l;
+}
+
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
-               fa_stream_t stream) {
+               fa_stream_t stream, int splits = 1, void* workspace = nullptr,
+               size_t workspace_bytes = 0) {
   Problem pr;
   int st = validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
@@ -194,8 +231,22 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
+  if (splits > 1) {
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < splitkv_bytes(B, H, Nq, d, splits))
+      return FA_ERR_WORKSPACE;
+  }
   if ((st = check_device(&pr.err)) != FA_OK) return st;
   FwdArgs a{q, k, v, o, lse};
+  a.pack = pack_groups(H, Hkv, Nq) ? 1 : 0;
+  a.splits = splits;
+  if (splits > 1) {
+    const size_t rows = static_cast<size_t>(B) * H * Nq;
+    a.o_part = static_cast<float*>(workspace);
+    a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          (static_cast<size_t>(splits) * rows * d * 4 + 255) /
+                                              256 * 256);
+  }
   cudaError_t e = launch_fwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
   return FA_OK;
@@ -213,6 +264,29 @@ extern "C" int fa_fwd_qk(const void* q, const void* k, const void* v, void* o, f
                          int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
                          fa_stream_t stream) {
   return fa::fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream);
+}
+
+extern "C" size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d,
+                                                int num_splits) {
+  Problem pr;
+  if (num_splits < 0 ||
+      fa::validate(B, H, Hkv, Nq, Nk, d, 0, 1.0f, FA_BF16, &pr) != FA_OK)
+    return 0;
+  const int sp = num_splits == 0 ? fa::auto_splits(B, H, Hkv, Nq, Nk, d) : num_splits;
+  return fa::splitkv_bytes(B, H, Nq, d, sp);
+}
+
+extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                              float scale, int dtype, int num_splits, void* workspace,
+                              size_t workspace_bytes, fa_stream_t stream) {
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  Problem pr;
+  int st = fa::validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
+  if (st != FA_OK) return st;
+  const int sp = num_splits == 0 ? fa::auto_splits(B, H, Hkv, Nq, Nk, d) : num_splits;
+  return fa::fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream, sp,
+                        workspace, workspace_bytes);
 }
 
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {

@@ -82,9 +82,15 @@ struct FwdParams {
   void* o;
   float* lse;
   int H, Hkv, G;
-  int Nq, Nk;         // query / key lengths
-  int off;            // Nk - Nq: under the mask query i sees keys k <= i + off
+  int Nq, Nk;         // query rows per head (packed rows, see mask_rows) / key length
+  int off;            // under the mask query i sees keys k <= i + off
+  int mask_rows;      // query index of a row for the mask: row % mask_rows (== Nq unless
+                      // the query heads of a KV group are packed into one row block)
   int num_q_tiles;
+  int splits;         // > 1: each CTA covers tiles_per_split key tiles and writes a
+  int tiles_per_split;  // normalised partial O (fp32) and its L to o_part / lse_part
+  float* o_part;
+  float* lse_part;
   float scale_log2;   // scale * log2(e)
   unsigned int* err;
 };
@@ -103,17 +109,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = CAUSAL ? (p.num_q_tiles - 1 - static_cast<int>(blockIdx.x))
-                        : static_cast<int>(blockIdx.x);
+  const int split = p.splits > 1 ? static_cast<int>(blockIdx.x) % p.splits : 0;
+  const int xt = p.splits > 1 ? static_cast<int>(blockIdx.x) / p.splits : static_cast<int>(blockIdx.x);
+  const int qt = CAUSAL ? (p.num_q_tiles - 1 - xt) : xt;
   const int h = blockIdx.y, b = blockIdx.z;
   const int kh = h / p.G;
+  const bool packed = p.mask_rows != p.Nq;
   int n_kv = (p.Nk + BC - 1) / BC;
   if (CAUSAL) {
     // last key any row of this tile may see (bottom-right aligned mask);
     // negative when every row of the tile sees none (only if Nq > Nk)
-    const int last_key = min((qt + 1) * kBR, p.Nq) - 1 + p.off;
+    const int max_i = packed ? p.mask_rows - 1 : min((qt + 1) * kBR, p.Nq) - 1;
+    const int last_key = max_i + p.off;
     n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
   }
+  // key tiles [j_base, j_base + n_kv) of this CTA
+  const int j_base = split * p.tiles_per_split;
+  if (p.splits > 1) n_kv = max(0, min(n_kv, j_base + p.tiles_per_split) - j_base);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
@@ -179,7 +191,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
           tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
-                      bar(L::kKFull + s), c * 64, j * BC, zkv);
+                      bar(L::kKFull + s), c * 64, (j_base + j) * BC, zkv);
       }
       __syncwarp();
       ++k_issued;
@@ -190,7 +202,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
           tma_load_3d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
-                      bar(L::kVFull + sv), c * 64, j * BC, zkv);
+                      bar(L::kVFull + sv), c * 64, (j_base + j) * BC, zkv);
       }
       __syncwarp();
       ++v_issued;
@@ -251,6 +263,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const int quarter = warp & 3;                 // TMEM lanes this warp may access
     const int r_tile = quarter * 32 + lane;
     const int row = qt * kBR + r_tile;
+    const int qi = row % p.mask_rows;             // query index of this row for the mask
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
     bool ok = true;
@@ -265,13 +278,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       tmem_ld_wait();
       reg_fence(sr);
       float* s = reinterpret_cast<float*>(sr);
-      const int col0 = j * BC;
-      const bool need_mask = (CAUSAL && col0 + BC - 1 > qt * kBR + p.off) || (col0 + BC > p.Nk);
+      const int col0 = (j_base + j) * BC;
+      const int min_i = packed ? 0 : qt * kBR;
+      const bool need_mask = (CAUSAL && col0 + BC - 1 > min_i + p.off) || (col0 + BC > p.Nk);
       if (need_mask) {
         #pragma unroll
         for (int i = 0; i < BC; ++i) {
           const int col = col0 + i;
-          if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
+          if (col >= p.Nk || (CAUSAL && col > qi + p.off)) s[i] = -INFINITY;
         }
       }
       // Row max as a tree of three-input maxima (independent partial maxima
@@ -358,7 +372,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_arrive(bar(L::kPFull + (j & 1)));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && n_kv == 0) {
+    if (ok && p.splits > 1 && n_kv == 0) {
+      // this split holds no key of these rows: partial O = 0, L = -inf
+      if (row < p.Nq) {
+        const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
+        const size_t rows_total = static_cast<size_t>(gridDim.z) * p.H * p.Nq;
+        float4* orow = reinterpret_cast<float4*>(p.o_part + (split * rows_total + r) * D);
+        #pragma unroll
+        for (int i = 0; i < D / 4; ++i) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.lse_part[split * rows_total + r] = -INFINITY;
+      }
+    } else if (ok && n_kv == 0) {
       // no row of this tile sees any key: O = 0, L = -inf
       if (row < p.Nq) {
         const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
@@ -380,6 +404,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
       const bool in_range = row < p.Nq;
+      if (p.splits > 1) {
+        // partial result of this key range, combined by fwd_combine_splits
+        const size_t rows_total = static_cast<size_t>(gridDim.z) * p.H * p.Nq;
+        const size_t r = split * rows_total + row_base + (in_range ? row : 0);
+        float4* orow = reinterpret_cast<float4*>(p.o_part + r * D);
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o1[32];
+          tmem_ld32(tO + lane_off + 32 * c, o1);
+          tmem_ld_wait();
+          reg_fence(o1);
+          if (in_range) {
+            #pragma unroll
+            for (int i = 0; i < 8; ++i)
+              orow[c * 8 + i] = make_float4(
+                  __uint_as_float(o1[4 * i]) * inv_l, __uint_as_float(o1[4 * i + 1]) * inv_l,
+                  __uint_as_float(o1[4 * i + 2]) * inv_l, __uint_as_float(o1[4 * i + 3]) * inv_l);
+          }
+        }
+        if (in_range) p.lse_part[r] = lse;
+      } else {
       uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                              (row_base + (in_range ? row : 0)) * D);
       #pragma unroll
@@ -399,6 +444,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
       }
       if (in_range) p.lse[row_base + row] = lse;
+      }
     }
   }
 
@@ -412,12 +458,51 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
 }
 
+// Merge the per-split partial results of one query row: with L_s the split
+// logsumexps, L = ln sum_s exp(L_s) and O = sum_s exp(L_s - L) O_s.  One warp
+// per row.  A row no split has a key for gets O = 0, L = -inf.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+fwd_combine_splits(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                   uint16_t* __restrict__ o, float* __restrict__ lse, size_t rows, int splits) {
+  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int kPer = D / 32;
+  float m = -INFINITY;
+  for (int sp = 0; sp < splits; ++sp) m = fmaxf(m, lse_part[sp * rows + row]);
+  uint16_t* orow = o + row * D + lane * kPer;
+  if (m == -INFINITY) {
+    #pragma unroll
+    for (int i = 0; i < kPer; i += 2) *reinterpret_cast<uint32_t*>(orow + i) = 0u;
+    if (lane == 0) lse[row] = -INFINITY;
+    return;
+  }
+  float acc[kPer];
+  #pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float sum = 0.f;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float ls = lse_part[sp * rows + row];
+    if (ls == -INFINITY) continue;
+    const float w = expf(ls - m);
+    sum += w;
+    const float* src = o_part + (sp * rows + row) * D + lane * kPer;
+    #pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = fmaf(w, src[i], acc[i]);
+  }
+  const float inv = 1.f / sum;
+  #pragma unroll
+  for (int i = 0; i < kPer; i += 2)
+    *reinterpret_cast<uint32_t*>(orow + i) = pack2<BF16>(acc[i] * inv, acc[i + 1] * inv);
+  if (lane == 0) lse[row] = m + logf(sum);
+}
+
 template <int D, int BC, bool CAUSAL, bool BF16, int KST, int VST>
 cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D, BC, KST, VST>;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, kBR)) != cudaSuccess) return e;
   if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
   if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
   auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST>;
@@ -427,23 +512,44 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  const int G = pr.H / pr.Hkv;
   FwdParams p;
   p.o = a.o;
   p.lse = a.lse;
-  p.H = pr.H;
+  // Packed: the G heads of a group are G * Nq consecutive rows of q, o and
+  // lse, so the group runs as one "head" of G * Nq query rows.
+  p.H = a.pack ? pr.Hkv : pr.H;
   p.Hkv = pr.Hkv;
-  p.Nq = pr.Nq;
+  p.G = a.pack ? 1 : G;
+  p.Nq = a.pack ? G * pr.Nq : pr.Nq;
   p.Nk = pr.Nk;
   p.off = pr.Nk - pr.Nq;
-  p.G = pr.H / pr.Hkv;
-  p.num_q_tiles = (pr.Nq + kBR - 1) / kBR;
+  p.mask_rows = pr.Nq;
+  p.num_q_tiles = (p.Nq + kBR - 1) / kBR;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.err = pr.err;
-  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  const int n_kv_tiles = (pr.Nk + BC - 1) / BC;
+  p.splits = 1;
+  p.tiles_per_split = n_kv_tiles;
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  if (a.splits > 1) {
+    p.tiles_per_split = (n_kv_tiles + a.splits - 1) / a.splits;
+    p.splits = (n_kv_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  }
+  if ((e = make_tmap_3d(&tq, a.q, D, p.Nq, pr.B * p.H, 64, kBR)) != cudaSuccess) return e;
+  dim3 grid(p.num_q_tiles * p.splits, p.H, pr.B);
   const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
   timing_end(slot, stream);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.splits > 1) {
+    const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
+    fwd_combine_splits<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        a.o_part, a.lse_part, static_cast<uint16_t*>(a.o), a.lse, rows, p.splits);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 template <int D, int BC, int KST, int VST>
@@ -457,6 +563,8 @@ cudaError_t dispatch_flags(const Problem& pr, const FwdArgs& a, cudaStream_t s) 
 }
 
 }  // namespace
+
+int fwd_key_tile(int d) { return d == 256 ? 64 : 128; }
 
 cudaError_t launch_fwd(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
   switch (pr.d) {

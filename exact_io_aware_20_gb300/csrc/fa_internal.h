@@ -24,7 +24,14 @@ struct FwdArgs {
   const void* v;
   void* o;
   float* lse;
+  int pack = 0;              // 1: the G query heads of a KV group form one row block
+  int splits = 1;            // > 1: split the key range, partials in o_part / lse_part
+  float* o_part = nullptr;   // [splits][B*H*Nq][d] fp32
+  float* lse_part = nullptr; // [splits][B*H*Nq] fp32
 };
+
+// Key tiles of the forward kernel (for choosing a split count).
+int fwd_key_tile(int d);
 
 struct BwdArgs {
   const void* q;

@@ -81,6 +81,30 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 int fa_fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
               int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
               fa_stream_t stream);
+/* (For Nq <= 64 and H > Hkv the G = H / Hkv query heads of a key/value head,
+ * G * Nq consecutive rows of q in memory, are processed as one row block.) */
+
+/*
+ * Forward pass split over the key axis, for short queries and long keys
+ * (decoding): each CTA covers one contiguous range of key tiles and writes a
+ * normalised partial output O_s and its logsumexp L_s (fp32) to `workspace`;
+ * a second kernel merges them exactly, L = ln sum_s exp(L_s) and
+ * O = sum_s exp(L_s - L) O_s, so the result equals fa_fwd_qk's up to
+ * rounding.  More CTAs stream K and V at once, which is what a few query rows
+ * over many keys need to reach memory bandwidth.  num_splits >= 1 fixes the
+ * split count (1 = no split, workspace may be NULL), 0 picks one from the
+ * device's SM count.  workspace: device memory of at least
+ * fa_fwd_splitkv_workspace_size(...) bytes for the same num_splits, 256-byte
+ * aligned.  Otherwise as fa_fwd_qk.
+ */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                   int num_splits, void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Bytes of workspace fa_fwd_splitkv needs (0 when it does not split); 0 for
+ * invalid sizes as well. */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d,
+                                     int num_splits);
 
 /*
  * Bytes of device scratch fa_bwd needs for this shape: the fp32 row vector

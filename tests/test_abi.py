@@ -96,3 +96,17 @@ def test_bwd_rejects(lib, case, expect):
                     a["dv"], a["B"], a["H"], a["Hkv"], a["N"], a["d"], a["causal"], a["scale"],
                     a["dtype"], a["ws"], a["ws_bytes"], None)
     assert st == expect
+
+
+def test_splitkv_workspace_checks(lib):
+    B, H, Hkv, Nq, Nk, d = 2, 8, 2, 1, 4096, 128
+    need = binding.load().fa_fwd_splitkv_workspace_size(B, H, Hkv, Nq, Nk, d, 4)
+    assert need == 4 * B * H * Nq * d * 4 + 256   # partial O + (padded) partial L
+    assert binding.load().fa_fwd_splitkv_workspace_size(B, H, Hkv, Nq, Nk, d, 1) == 0
+    assert binding.load().fa_fwd_splitkv_workspace_size(B, H, 3, Nq, Nk, d, 4) == 0
+    st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv, Nq, Nk, d, 1, 0.088,
+                            binding.FA_BF16, 4, FAKE, 16, None)
+    assert st == binding.FA_ERR_WORKSPACE
+    st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv, Nq, Nk, d, 1, 0.088,
+                            binding.FA_BF16, -1, FAKE, 1 << 30, None)
+    assert st == binding.FA_ERR_INVALID_ARG
