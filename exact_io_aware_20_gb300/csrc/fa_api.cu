@@ -198,18 +198,31 @@ int num_sms() {
 // Short queries of a GQA group share one query-row block (see FwdArgs::pack).
 bool pack_groups(int H, int Hkv, int Nq) { return H > Hkv && Nq <= 64; }
 
-// Split count for fa_fwd_splitkv: enough CTAs for about two waves, at least
-// two key tiles per split.
+// Split count for fa_fwd_splitkv: among the counts that keep at least four
+// key tiles per split and give at least two waves of CTAs, the one whose
+// last wave is fullest (fewest idle SMs); 1 when there are enough CTAs.
 int auto_splits(int B, int H, int Hkv, int Nq, int Nk, int d) {
   const int rows = pack_groups(H, Hkv, Nq) ? (H / Hkv) * Nq : Nq;
   const long long ctas =
       static_cast<long long>((rows + 127) / 128) * (pack_groups(H, Hkv, Nq) ? Hkv : H) * B;
   const int n_kv = (Nk + fwd_key_tile(d) - 1) / fwd_key_tile(d);
-  const long long want = 2ll * num_sms();
-  if (ctas >= want) return 1;
-  int sp = static_cast<int>((want + ctas - 1) / ctas);
-  sp = std::min(sp, std::max(1, n_kv / 2));
-  return std::max(1, sp);
+  const long long sms = num_sms();
+  if (ctas >= 2 * sms) return 1;
+  const int max_sp = std::max(1, n_kv / 4);
+  int best = 1;
+  double best_eff = -1.0;
+  for (int sp = 1; sp <= max_sp; ++sp) {
+    const long long total = ctas * sp;
+    if (total < 2 * sms && sp < max_sp) continue;
+    const double waves = static_cast<double>(total) / sms;
+    const double eff = waves / std::ceil(waves);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = sp;
+    }
+    if (total >= 8 * sms) break;
+  }
+  return best;
 }
 
 size_t splitkv_bytes(int B, int H, int Nq, int d, int splits) {

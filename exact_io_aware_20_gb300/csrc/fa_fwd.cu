@@ -267,10 +267,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
     bool ok = true;
+    // A warp whose 32 rows all lie past the last query row (short or packed
+    // queries) only keeps the barrier protocol: its Q rows are zero-filled,
+    // so its scores are 0 and the P it leaves in TMEM is 0, and its rows are
+    // never stored.
+    const bool idle = qt * kBR + quarter * 32 >= p.Nq;
     for (int j = 0; j < n_kv; ++j) {
       const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
       if (!wait_uniform(bar(L::kSFull + (j & 1)), (j >> 1) & 1, abort)) { ok = false; break; }
       tc_fence_after();
+      if (idle) {
+        if (j > 0 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
+        tc_fence_before();
+        mbar_arrive(bar(L::kPFull + (j & 1)));
+        continue;
+      }
       uint32_t sr[BC];
       #pragma unroll
       for (int c = 0; c < BC / 32; ++c)
