@@ -76,6 +76,17 @@ def load(path: str | None = None):
                                     ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
                                     ctypes.c_long, ctypes.c_long, _dp, _dp, _dp]
     lib.oracle_bwd_rows.restype = None
+    _bp = ctypes.POINTER(ctypes.c_ubyte)
+    lib.oracle_fwd_group_blockmask.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                               ctypes.c_long, ctypes.c_long, ctypes.c_int, _bp,
+                                               ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                               ctypes.c_double, _dp, _dp]
+    lib.oracle_fwd_group_blockmask.restype = None
+    lib.oracle_bwd_group_blockmask.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                               ctypes.c_long, ctypes.c_long, ctypes.c_int, _bp,
+                                               ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                               ctypes.c_double, _dp, _dp, _dp]
+    lib.oracle_bwd_group_blockmask.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     if path is None:
@@ -217,4 +228,81 @@ def backward_rows(q_group, k_head, v_head, dout_group, r0: int, r1: int, causal:
     assert dv.dtype == np.float64 and dv.flags.c_contiguous and dv.shape == (Nk, d)
     lib.oracle_bwd_rows(_ptr(qg), _ptr(kh), _ptr(vh), _ptr(dg), G, Nq, Nk, d, int(bool(causal)),
                         float(scale), int(r0), int(r1), _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
+
+
+def _block_mask(block_mask, H: int, Nq: int, Nk: int, bs: int) -> np.ndarray:
+    """Check a block mask [mask_heads, ceil(Nq/bs), ceil(Nk/bs)] (mask_heads 1 or H)
+    and return it as contiguous uint8 (nonzero = the block is kept)."""
+    m = np.ascontiguousarray(np.asarray(block_mask) != 0, dtype=np.uint8)
+    nbr, nbc = -(-Nq // bs), -(-Nk // bs)
+    if m.ndim != 3 or m.shape[0] not in (1, H) or m.shape[1:] != (nbr, nbc):
+        raise ValueError(f"block mask shape {m.shape} does not fit H={H} "
+                         f"[{nbr}, {nbc}] blocks of {bs}")
+    return m
+
+
+def forward_blocksparse(q, k, v, block_mask, causal: bool, scale: float, bs: int = 128,
+                        lib=None):
+    """Exact attention restricted to a block pattern: key k is visible to query i
+    of head h only where block_mask[h or 0, i // bs, k // bs] != 0 (and, if
+    causal, k <= i + Nk - Nq).  Returns O [B,H,Nq,d], L [B,H,Nq] in fp64."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k)
+    G = H // Hkv
+    m = _block_mask(block_mask, H, Nq, Nk, bs)
+    per_head = m.shape[0] == H
+    nbc = m.shape[2]
+    hstride = m.shape[1] * nbc if per_head else 0
+    o = np.zeros((B, H, Nq, d))
+    lse = np.zeros((B, H, Nq))
+    for b in range(B):
+        for kh in range(Hkv):
+            sl = slice(kh * G, (kh + 1) * G)
+            qs = np.ascontiguousarray(q[b, sl])
+            mg = np.ascontiguousarray(m[sl] if per_head else m[0:1])
+            og = np.zeros((G, Nq, d))
+            lg = np.zeros((G, Nq))
+            lib.oracle_fwd_group_blockmask(
+                _ptr(qs), _ptr(np.ascontiguousarray(k[b, kh])),
+                _ptr(np.ascontiguousarray(v[b, kh])), G, Nq, Nk, d, int(bool(causal)),
+                mg.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)), bs, nbc, hstride,
+                float(scale), _ptr(og), _ptr(lg))
+            o[b, sl] = og
+            lse[b, sl] = lg
+    return o, lse
+
+
+def backward_blocksparse(q, k, v, dout, block_mask, causal: bool, scale: float,
+                         bs: int = 128, lib=None):
+    """Gradients of sum(O o dO) for the block-restricted attention of
+    forward_blocksparse: dQ [B,H,Nq,d], dK/dV [B,Hkv,Nk,d] in fp64."""
+    lib = lib or load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k)
+    G = H // Hkv
+    m = _block_mask(block_mask, H, Nq, Nk, bs)
+    per_head = m.shape[0] == H
+    nbc = m.shape[2]
+    hstride = m.shape[1] * nbc if per_head else 0
+    dq = np.zeros((B, H, Nq, d))
+    dk = np.zeros((B, Hkv, Nk, d))
+    dv = np.zeros((B, Hkv, Nk, d))
+    for b in range(B):
+        for kh in range(Hkv):
+            sl = slice(kh * G, (kh + 1) * G)
+            mg = np.ascontiguousarray(m[sl] if per_head else m[0:1])
+            g_dq = np.zeros((G, Nq, d))
+            g_dk = np.zeros((Nk, d))
+            g_dv = np.zeros((Nk, d))
+            lib.oracle_bwd_group_blockmask(
+                _ptr(np.ascontiguousarray(q[b, sl])), _ptr(np.ascontiguousarray(k[b, kh])),
+                _ptr(np.ascontiguousarray(v[b, kh])), _ptr(np.ascontiguousarray(dout[b, sl])),
+                G, Nq, Nk, d, int(bool(causal)),
+                mg.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)), bs, nbc, hstride,
+                float(scale), _ptr(g_dq), _ptr(g_dk), _ptr(g_dv))
+            dq[b, sl] = g_dq
+            dk[b, kh] = g_dk
+            dv[b, kh] = g_dv
     return dq, dk, dv

@@ -32,7 +32,12 @@
  *  - L is the natural logarithm, of the scaled scores;
  *  - a query row with no allowed key (only possible when Nq > Nk under the
  *    mask) has O = 0, L = -inf and zero gradients;
- *  - query head h reads key/value head h / G, G = H / Hkv.
+ *  - query head h reads key/value head h / G, G = H / Hkv;
+ *  - block-sparse attention ("FlashAttention: Fast and Memory-Efficient
+ *    Exact Attention with IO-Awareness", abstract and "Key contributions") is
+ *    exact attention restricted to the kept blocks of a given pattern: the
+ *    block mask and the causal mask both apply, and a row they empty is
+ *    treated as above.
  *
  * Layout: every array is row-major.  One call works on one "group": the G
  * query heads that share one key/value head.
@@ -47,10 +52,26 @@
 #include <omp.h>
 #endif
 
-/* Whether query row i may attend to key k. */
-static int allowed(long i, long k, long Nq, long Nk, int causal)
+/*
+ * Which keys a query row may see.  causal: key k for query i when
+ * k <= i + (Nk - Nq).  block (optional): query block i / bs sees key block
+ * k / bs only where block[g * head_stride + (i / bs) * nbc + k / bs] != 0, g
+ * the query head within the group ("FlashAttention: Fast and Memory-Efficient
+ * Exact Attention with IO-Awareness", abstract and "Key contributions": block-sparse
+ * FlashAttention skips the zero blocks of a given block pattern; here it is
+ * exact attention restricted to that pattern).
+ */
+struct mask_spec {
+    int causal;
+    const unsigned char *block; /* NULL: no block mask */
+    long bs, nbc, head_stride;
+};
+
+static int allowed(const struct mask_spec *m, long g, long i, long k, long Nq, long Nk)
 {
-    if (!causal)
+    if (m->block && !m->block[g * m->head_stride + (i / m->bs) * m->nbc + k / m->bs])
+        return 0;
+    if (!m->causal)
         return 1;
     return k <= i + (Nk - Nq);
 }
@@ -68,12 +89,12 @@ static double dot(const double *x, const double *y, long d)
  * -inf elsewhere.  Returns the row logsumexp L = m + ln(sum_k exp(s_k - m))
  * (two passes: max, then the shifted sum), or -inf for an empty row.
  */
-static double score_row(const double *qi, const double *k, long i, long Nq,
-                        long Nk, long d, int causal, double scale, double *s)
+static double score_row(const double *qi, const double *k, long g, long i, long Nq,
+                        long Nk, long d, const struct mask_spec *ms, double scale, double *s)
 {
     double m = -INFINITY;
     for (long kk = 0; kk < Nk; ++kk) {
-        if (allowed(i, kk, Nq, Nk, causal)) {
+        if (allowed(ms, g, i, kk, Nq, Nk)) {
             s[kk] = scale * dot(qi, k + kk * d, d);
             if (s[kk] > m)
                 m = s[kk];
@@ -85,7 +106,7 @@ static double score_row(const double *qi, const double *k, long i, long Nq,
         return -INFINITY;
     double l = 0.0;
     for (long kk = 0; kk < Nk; ++kk)
-        if (allowed(i, kk, Nq, Nk, causal))
+        if (allowed(ms, g, i, kk, Nq, Nk))
             l += exp(s[kk] - m);
     return m + log(l);
 }
@@ -100,10 +121,11 @@ static double weight(double s, double lse)
 
 /* One query row of the forward pass: O_i = sum_k P_ik V_k, and L_i. */
 static void forward_row(const double *qi, const double *k, const double *v,
-                        long i, long Nq, long Nk, long d, int causal,
-                        double scale, double *s, double *oi, double *lse_i)
+                        long g, long i, long Nq, long Nk, long d,
+                        const struct mask_spec *ms, double scale, double *s,
+                        double *oi, double *lse_i)
 {
-    double L = score_row(qi, k, i, Nq, Nk, d, causal, scale, s);
+    double L = score_row(qi, k, g, i, Nq, Nk, d, ms, scale, s);
     for (long c = 0; c < d; ++c)
         oi[c] = 0.0;
     for (long kk = 0; kk < Nk; ++kk) {
@@ -120,9 +142,9 @@ static void forward_row(const double *qi, const double *k, const double *v,
  * Forward pass for one group of G query heads.
  * q [G][Nq][d], k/v [Nk][d] -> o [G][Nq][d], lse [G][Nq].
  */
-void oracle_fwd_group(const double *q, const double *k, const double *v,
-                      long G, long Nq, long Nk, long d, int causal,
-                      double scale, double *o, double *lse)
+static void fwd_group(const double *q, const double *k, const double *v, long G, long Nq,
+                      long Nk, long d, const struct mask_spec *ms, double scale, double *o,
+                      double *lse)
 {
     long rows = G * Nq;
 #pragma omp parallel
@@ -130,12 +152,34 @@ void oracle_fwd_group(const double *q, const double *k, const double *v,
         double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
 #pragma omp for schedule(dynamic, 4)
         for (long r = 0; r < rows; ++r) {
-            long i = r % Nq;
-            forward_row(q + r * d, k, v, i, Nq, Nk, d, causal, scale, s,
-                        o + r * d, lse + r);
+            long g = r / Nq, i = r % Nq;
+            forward_row(q + r * d, k, v, g, i, Nq, Nk, d, ms, scale, s, o + r * d,
+                        lse + r);
         }
         free(s);
     }
+}
+
+void oracle_fwd_group(const double *q, const double *k, const double *v,
+                      long G, long Nq, long Nk, long d, int causal,
+                      double scale, double *o, double *lse)
+{
+    struct mask_spec ms = {causal, NULL, 1, 1, 0};
+    fwd_group(q, k, v, G, Nq, Nk, d, &ms, scale, o, lse);
+}
+
+/*
+ * As oracle_fwd_group with a block mask: block [G or 1][ceil(Nq/bs)][nbc]
+ * bytes, head_stride = bytes between the heads' masks (0: one mask shared by
+ * the group's heads).
+ */
+void oracle_fwd_group_blockmask(const double *q, const double *k, const double *v, long G,
+                                long Nq, long Nk, long d, int causal,
+                                const unsigned char *block, long bs, long nbc,
+                                long head_stride, double scale, double *o, double *lse)
+{
+    struct mask_spec ms = {causal, block, bs, nbc, head_stride};
+    fwd_group(q, k, v, G, Nq, Nk, d, &ms, scale, o, lse);
 }
 
 /*
@@ -149,14 +193,15 @@ void oracle_fwd_rows(const double *q, const double *k, const double *v,
                      double *lse)
 {
     (void)G;
+    struct mask_spec ms = {causal, NULL, 1, 1, 0};
 #pragma omp parallel
     {
         double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
 #pragma omp for schedule(dynamic, 1)
         for (long t = 0; t < n; ++t) {
             long g = rows[2 * t], i = rows[2 * t + 1];
-            forward_row(q + (g * Nq + i) * d, k, v, i, Nq, Nk, d, causal,
-                        scale, s, o + t * d, lse + t);
+            forward_row(q + (g * Nq + i) * d, k, v, g, i, Nq, Nk, d, &ms, scale, s,
+                        o + t * d, lse + t);
         }
         free(s);
     }
@@ -172,9 +217,9 @@ void oracle_fwd_rows(const double *q, const double *k, const double *v,
  * Optional outputs o_out / lse_out / delta_out receive O, L and D (may be
  * NULL).
  */
-void oracle_bwd_group(const double *q, const double *k, const double *v,
+static void bwd_group(const double *q, const double *k, const double *v,
                       const double *dout, long G, long Nq, long Nk, long d,
-                      int causal, double scale, double *dq, double *dk,
+                      const struct mask_spec *ms, double scale, double *dq, double *dk,
                       double *dv, double *o_out, double *lse_out,
                       double *delta_out)
 {
@@ -189,8 +234,8 @@ void oracle_bwd_group(const double *q, const double *k, const double *v,
         double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
 #pragma omp for schedule(dynamic, 4)
         for (long r = 0; r < rows; ++r) {
-            long i = r % Nq;
-            forward_row(q + r * d, k, v, i, Nq, Nk, d, causal, scale, s,
+            long g = r / Nq, i = r % Nq;
+            forward_row(q + r * d, k, v, g, i, Nq, Nk, d, ms, scale, s,
                         o + r * d, L + r);
             D[r] = dot(dout + r * d, o + r * d, d);
         }
@@ -200,13 +245,13 @@ void oracle_bwd_group(const double *q, const double *k, const double *v,
     /* Pass 2: dQ_i = scale * sum_k P_ik (dP_ik - D_i) K_k, row by row. */
 #pragma omp parallel for schedule(dynamic, 4)
     for (long r = 0; r < rows; ++r) {
-        long i = r % Nq;
+        long g = r / Nq, i = r % Nq;
         const double *qi = q + r * d, *doi = dout + r * d;
         double *dqi = dq + r * d;
         for (long c = 0; c < d; ++c)
             dqi[c] = 0.0;
         for (long kk = 0; kk < Nk; ++kk) {
-            if (!allowed(i, kk, Nq, Nk, causal))
+            if (!allowed(ms, g, i, kk, Nq, Nk))
                 continue;
             double sik = scale * dot(qi, k + kk * d, d);
             double p = weight(sik, L[r]);
@@ -226,8 +271,8 @@ void oracle_bwd_group(const double *q, const double *k, const double *v,
             dvk[c] = 0.0;
         }
         for (long r = 0; r < rows; ++r) {
-            long i = r % Nq;
-            if (!allowed(i, kk, Nq, Nk, causal))
+            long g = r / Nq, i = r % Nq;
+            if (!allowed(ms, g, i, kk, Nq, Nk))
                 continue;
             const double *qi = q + r * d, *doi = dout + r * d;
             double sik = scale * dot(qi, k + kk * d, d);
@@ -252,6 +297,29 @@ void oracle_bwd_group(const double *q, const double *k, const double *v,
     free(D);
 }
 
+/* Backward pass for one group (see bwd_group); causal or dense mask. */
+void oracle_bwd_group(const double *q, const double *k, const double *v,
+                      const double *dout, long G, long Nq, long Nk, long d,
+                      int causal, double scale, double *dq, double *dk,
+                      double *dv, double *o_out, double *lse_out,
+                      double *delta_out)
+{
+    struct mask_spec ms = {causal, NULL, 1, 1, 0};
+    bwd_group(q, k, v, dout, G, Nq, Nk, d, &ms, scale, dq, dk, dv, o_out, lse_out,
+              delta_out);
+}
+
+/* As oracle_bwd_group with the block mask of oracle_fwd_group_blockmask. */
+void oracle_bwd_group_blockmask(const double *q, const double *k, const double *v,
+                                const double *dout, long G, long Nq, long Nk, long d,
+                                int causal, const unsigned char *block, long bs, long nbc,
+                                long head_stride, double scale, double *dq, double *dk,
+                                double *dv)
+{
+    struct mask_spec ms = {causal, block, bs, nbc, head_stride};
+    bwd_group(q, k, v, dout, G, Nq, Nk, d, &ms, scale, dq, dk, dv, NULL, NULL, NULL);
+}
+
 /*
  * The backward sums run over query rows, so they split by rows.  For the
  * flattened rows r = g * Nq + i in [r0, r1) of one group, this writes dQ of
@@ -266,6 +334,7 @@ void oracle_bwd_rows(const double *q, const double *k, const double *v,
                      double *dk, double *dv)
 {
     (void)G;
+    struct mask_spec ms = {causal, NULL, 1, 1, 0};
     long n = r1 - r0;
     if (n <= 0)
         return;
@@ -278,8 +347,8 @@ void oracle_bwd_rows(const double *q, const double *k, const double *v,
         double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
 #pragma omp for schedule(dynamic, 4)
         for (long t = 0; t < n; ++t) {
-            long r = r0 + t, i = r % Nq;
-            forward_row(q + r * d, k, v, i, Nq, Nk, d, causal, scale, s,
+            long r = r0 + t, g = r / Nq, i = r % Nq;
+            forward_row(q + r * d, k, v, g, i, Nq, Nk, d, &ms, scale, s,
                         o + t * d, L + t);
             D[t] = dot(dout + r * d, o + t * d, d);
         }
@@ -288,13 +357,13 @@ void oracle_bwd_rows(const double *q, const double *k, const double *v,
 
 #pragma omp parallel for schedule(dynamic, 4)
     for (long t = 0; t < n; ++t) {
-        long r = r0 + t, i = r % Nq;
+        long r = r0 + t, g = r / Nq, i = r % Nq;
         const double *qi = q + r * d, *doi = dout + r * d;
         double *dqi = dq + t * d;
         for (long c = 0; c < d; ++c)
             dqi[c] = 0.0;
         for (long kk = 0; kk < Nk; ++kk) {
-            if (!allowed(i, kk, Nq, Nk, causal))
+            if (!allowed(&ms, g, i, kk, Nq, Nk))
                 continue;
             double sik = scale * dot(qi, k + kk * d, d);
             double p = weight(sik, L[t]);
@@ -309,8 +378,8 @@ void oracle_bwd_rows(const double *q, const double *k, const double *v,
     for (long kk = 0; kk < Nk; ++kk) {
         double *dkk = dk + kk * d, *dvk = dv + kk * d;
         for (long t = 0; t < n; ++t) {
-            long r = r0 + t, i = r % Nq;
-            if (!allowed(i, kk, Nq, Nk, causal))
+            long r = r0 + t, g = r / Nq, i = r % Nq;
+            if (!allowed(&ms, g, i, kk, Nq, Nk))
                 continue;
             const double *qi = q + r * d, *doi = dout + r * d;
             double sik = scale * dot(qi, k + kk * d, d);

@@ -15,6 +15,15 @@ What pins what:
   derivatives       central finite differences of sum(O o dO)
   library routines  torch fp64 softmax/matmul and torch.autograd gradients
   bottom-right mask Nq != Nk rows, including rows with no allowed key
+  block mask        an all-ones mask is the dense result bit for bit; a query
+                    block that keeps one key block is dense attention over
+                    that key slice; torch fp64 with the block mask expanded
+                    to an element mask (shared and per-head masks, GQA,
+                    causal, ragged edges, fully masked rows)
+
+Block-sparse attention ("FlashAttention: Fast and Memory-Efficient Exact
+Attention with IO-Awareness", abstract and "Key contributions") is read as
+exact attention restricted to the kept blocks of a given pattern.
 
 The attention definition these follow: "FlashAttention-2: Faster Attention
 with Better Parallelism and Work Partitioning" (paper digest), section 3
@@ -282,8 +291,10 @@ def pin_finite_differences(lib):
         _fd_check(lib, G, Nq, Nk, d, causal, seed)
 
 
-def _torch_reference(q, k, v, do, causal, scale):
-    """torch fp64: explicit matmul + torch.softmax, autograd for the gradients."""
+def _torch_reference(q, k, v, do, causal, scale, keep=None):
+    """torch fp64: explicit matmul + torch.softmax, autograd for the gradients.
+    keep (optional, bool [H or 1, Nq, Nk]): element mask; rows it empties get
+    O = 0, L = -inf and zero gradients."""
     q = torch.tensor(q, dtype=torch.float64, requires_grad=True)
     k = torch.tensor(k, dtype=torch.float64, requires_grad=True)
     v = torch.tensor(v, dtype=torch.float64, requires_grad=True)
@@ -296,7 +307,10 @@ def _torch_reference(q, k, v, do, causal, scale):
         i = torch.arange(Nq).view(-1, 1)
         kk = torch.arange(Nk).view(1, -1)
         s = s.masked_fill(kk > i + (Nk - Nq), float("-inf"))
-    p = torch.softmax(s, dim=-1)
+    if keep is not None:
+        s = s.masked_fill(~torch.as_tensor(keep), float("-inf"))
+    empty = torch.isneginf(s).all(dim=-1, keepdim=True)
+    p = torch.softmax(s.masked_fill(empty, 0.0), dim=-1).masked_fill(empty, 0.0)
     lse = torch.logsumexp(s, dim=-1)
     o = torch.matmul(p, vr)
     (o * torch.tensor(do)).sum().backward()
@@ -372,8 +386,82 @@ def pin_row_slabs_sum_to_group(lib):
         np.testing.assert_allclose(dv_s, dv, rtol=0, atol=1e-12)
 
 
+def _expand_blocks(mask, Nq, Nk, bs):
+    """Element mask [h, Nq, Nk] from a block mask [h, ceil(Nq/bs), ceil(Nk/bs)]."""
+    m = np.asarray(mask, dtype=bool)
+    return np.repeat(np.repeat(m, bs, axis=1), bs, axis=2)[:, :Nq, :Nk]
+
+
+def pin_blockmask_all_ones_is_dense(lib):
+    """An all-ones block mask changes nothing: outputs equal the dense ones bit for bit."""
+    rng = _rng(30)
+    B, H, Hkv, Nq, Nk, d, bs = 1, 4, 2, 21, 26, 8, 4
+    q, k, v = _rand(rng, B, H, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+    do = _rand(rng, B, H, Nq, d)
+    for causal in (False, True):
+        o, lse = oracle.forward(q, k, v, causal, 0.4, lib)
+        dq, dk, dv = oracle.backward(q, k, v, do, causal, 0.4, lib)
+        for heads in (1, H):
+            ones = np.ones((heads, -(-Nq // bs), -(-Nk // bs)), dtype=np.uint8)
+            ob, lb = oracle.forward_blocksparse(q, k, v, ones, causal, 0.4, bs, lib)
+            gb = oracle.backward_blocksparse(q, k, v, do, ones, causal, 0.4, bs, lib)
+            assert np.array_equal(ob, o) and np.array_equal(lb, lse)
+            for a, b in zip(gb, (dq, dk, dv)):
+                assert np.array_equal(a, b)
+
+
+def pin_blockmask_single_block(lib):
+    """A query block that keeps only key block j is dense attention of those
+    queries over keys [j*bs, (j+1)*bs); a query block that keeps none has
+    O = 0, L = -inf and zero dQ."""
+    rng = _rng(31)
+    H, N, d, bs = 2, 24, 4, 6
+    q, k, v = _rand(rng, 1, H, N, d), _rand(rng, 1, 1, N, d), _rand(rng, 1, 1, N, d)
+    do = _rand(rng, 1, H, N, d)
+    nb = N // bs
+    mask = np.zeros((H, nb, nb), dtype=np.uint8)
+    mask[0, 1, 3] = 1     # head 0: query block 1 sees key block 3 only
+    mask[1, 2, 0] = 1     # head 1: query block 2 sees key block 0 only
+    mask[1, 0, 2] = 1
+    o, lse = oracle.forward_blocksparse(q, k, v, mask, False, 0.7, bs, lib)
+    for h, qb, kb in ((0, 1, 3), (1, 2, 0), (1, 0, 2)):
+        qs = q[0, h, qb * bs:(qb + 1) * bs][None]
+        ks, vs = k[0, 0, kb * bs:(kb + 1) * bs], v[0, 0, kb * bs:(kb + 1) * bs]
+        od, ld = oracle.forward_group(qs, ks, vs, False, 0.7, lib)
+        np.testing.assert_allclose(o[0, h, qb * bs:(qb + 1) * bs], od[0], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[0, h, qb * bs:(qb + 1) * bs], ld[0], rtol=0, atol=1e-14)
+    assert np.all(o[0, 0, :bs] == 0.0) and np.all(np.isneginf(lse[0, 0, :bs]))
+    dq, dk, dv = oracle.backward_blocksparse(q, k, v, do, mask, False, 0.7, bs, lib)
+    assert np.all(dq[0, 0, :bs] == 0.0) and np.all(dq[0, 1, bs:2 * bs] == 0.0)
+    # key block 1 is kept by no query block of either head
+    assert np.all(dk[0, 0, bs:2 * bs] == 0.0) and np.all(dv[0, 0, bs:2 * bs] == 0.0)
+
+
+def pin_blockmask_torch(lib):
+    """Agreement with torch fp64 under the element mask a block mask expands to."""
+    rng = _rng(32)
+    for (B, H, Hkv, Nq, Nk, d, bs, heads, causal) in (
+            (1, 2, 2, 17, 23, 8, 4, 2, False), (2, 4, 2, 20, 20, 4, 4, 4, True),
+            (1, 4, 1, 13, 30, 8, 8, 1, True), (1, 3, 3, 30, 11, 4, 5, 3, True),
+            (1, 2, 1, 300, 260, 16, 128, 2, False)):
+        q, k, v = _rand(rng, B, H, Nq, d), _rand(rng, B, Hkv, Nk, d), _rand(rng, B, Hkv, Nk, d)
+        do = _rand(rng, B, H, Nq, d)
+        mask = (rng.random((heads, -(-Nq // bs), -(-Nk // bs))) < 0.5).astype(np.uint8)
+        mask[0, 0, :] = 0  # one query block with no key at all
+        keep = _expand_blocks(mask, Nq, Nk, bs)
+        o_t, l_t, dq_t, dk_t, dv_t = _torch_reference(q, k, v, do, causal, 0.35, keep)
+        o, lse = oracle.forward_blocksparse(q, k, v, mask, causal, 0.35, bs, lib)
+        dq, dk, dv = oracle.backward_blocksparse(q, k, v, do, mask, causal, 0.35, bs, lib)
+        np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(l_t))
+        fin = np.isfinite(l_t)
+        np.testing.assert_allclose(lse[fin], l_t[fin], rtol=0, atol=1e-12)
+        for a, b in ((o, o_t), (dq, dq_t), (dk, dk_t), (dv, dv_t)):
+            np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [pin_identical_keys, pin_zero_queries, pin_dominant_score, pin_causal_first_row,
             pin_two_keys_forward, pin_two_keys_backward, pin_rows_are_probabilities,
             pin_permutation_and_shift, pin_gqa_equals_repeated_mha, pin_delta_and_extras,
             pin_finite_differences, pin_torch_fp64, pin_bottom_right_mask, pin_rows_match_group,
-            pin_row_slabs_sum_to_group]
+            pin_row_slabs_sum_to_group, pin_blockmask_all_ones_is_dense,
+            pin_blockmask_single_block, pin_blockmask_torch]

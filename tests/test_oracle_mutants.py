@@ -18,6 +18,10 @@ MUTANTS = {
     "scale_dropped": ("s[kk] = scale * dot(qi, k + kk * d, d);", "s[kk] = dot(qi, k + kk * d, d);"),
     "mask_strict": ("return k <= i + (Nk - Nq);", "return k < i + (Nk - Nq);"),
     "mask_top_left": ("return k <= i + (Nk - Nq);", "return k <= i;"),
+    "block_transposed": ("(i / m->bs) * m->nbc + k / m->bs]", "(k / m->bs) * m->nbc + i / m->bs]"),
+    "block_head_ignored": ("m->block[g * m->head_stride +", "m->block[0 * m->head_stride +"),
+    "block_ignored": ("if (m->block && !m->block[", "if (0 && m->block && !m->block["),
+    "block_overrides_causal": ("        return 0;\n    if (!m->causal)", "        return 0;\n    if (m->block || !m->causal)"),
     "lse_log2": ("return m + log(l);", "return m + log2(l);"),
     "lse_no_max": ("return m + log(l);", "return log(l);"),
     "pv_wrong_operand": ("oi[c] += p * v[kk * d + c];", "oi[c] += p * k[kk * d + c];"),
