@@ -35,6 +35,10 @@ SIGNATURES = {
                                   _i, _f, _i, _vp, _sz, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
                             _i, _vp]),
+    "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
+                                _i, _vp]),
+    "fa_bwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                _i, _f, _i, _vp, _i, _i, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_selftest_expired_wait": (_i, [_i, _vp]),
@@ -226,3 +230,55 @@ def forward_splitkv(q, k, v, causal: bool, scale: float, num_splits: int = 0, ou
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream)), "fa_fwd_splitkv")
     return out, lse
+
+
+def _check_mask(block_mask, H, Nq, Nk, device):
+    """A block mask [1 or H, ceil(Nq/128), ceil(Nk/128)] as a contiguous uint8
+    CUDA tensor (nonzero = computed); returns (mask, mask_heads)."""
+    nbr, nbc = -(-Nq // 128), -(-Nk // 128)
+    if (block_mask.dim() != 3 or block_mask.shape[0] not in (1, H)
+            or tuple(block_mask.shape[1:]) != (nbr, nbc)):
+        raise ValueError(f"block mask must be [1 or {H}, {nbr}, {nbc}], got "
+                         f"{tuple(block_mask.shape)}")
+    if block_mask.dtype not in (torch.uint8, torch.bool):
+        raise TypeError("block mask must be uint8 or bool")
+    if not block_mask.is_cuda or block_mask.device != device or not block_mask.is_contiguous():
+        raise ValueError("block mask must be a contiguous tensor on the inputs' device")
+    return block_mask, int(block_mask.shape[0])
+
+
+def forward_blocksparse(q, k, v, block_mask, causal: bool, scale: float, out=None, lse=None,
+                        stream=None):
+    """(o, lse) of exact attention restricted to the kept 128 x 128 blocks of
+    block_mask [1 or H, ceil(Nq/128), ceil(Nk/128)] (fa_fwd_blocksparse)."""
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v)
+    mask, mh = _check_mask(block_mask, H, Nq, Nk, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check(load().fa_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv,
+                                     Nq, Nk, d, int(causal), float(scale), _dtype_code(q),
+                                     _ptr(mask), mh, _stream_ptr(stream)), "fa_fwd_blocksparse")
+    return out, lse
+
+
+def backward_blocksparse(q, k, v, o, lse, dout, block_mask, causal: bool, scale: float, dq=None,
+                         dk=None, dv=None, workspace=None, stream=None,
+                         deterministic: bool = False):
+    """(dq, dk, dv) of the block-sparse forward above (fa_bwd_blocksparse)."""
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v)
+    mask, mh = _check_mask(block_mask, H, Nq, Nk, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, H, Hkv, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(load().fa_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, Nq, Nk, d,
+                                     int(causal), float(scale), _dtype_code(q), _ptr(mask), mh,
+                                     int(bool(deterministic)), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_ptr(stream)), "fa_bwd_blocksparse")
+    return dq, dk, dv

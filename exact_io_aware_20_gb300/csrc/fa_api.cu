@@ -236,7 +236,7 @@ size_t splitkv_bytes(int B, int H, int Nq, int d, int splits) {
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
                fa_stream_t stream, int splits = 1, void* workspace = nullptr,
-               size_t workspace_bytes = 0) {
+               size_t workspace_bytes = 0, const BlockMask* mask = nullptr) {
   Problem pr;
   int st = validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
@@ -251,7 +251,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   }
   if ((st = check_device(&pr.err)) != FA_OK) return st;
   FwdArgs a{q, k, v, o, lse};
-  a.pack = pack_groups(H, Hkv, Nq) ? 1 : 0;
+  a.pack = pack_groups(H, Hkv, Nq) && mask == nullptr ? 1 : 0;
+  if (mask != nullptr) a.mask = *mask;
   a.splits = splits;
   if (splits > 1) {
     const size_t rows = static_cast<size_t>(B) * H * Nq;
@@ -302,6 +303,38 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
                         workspace, workspace_bytes);
 }
 
+namespace fa {
+namespace {
+// Checks a block mask's arguments and the step-list capacities for the
+// shape (pr already validated); fills *m.
+int mask_args(const Problem& pr, const unsigned char* block_mask, int mask_heads, BlockMask* m) {
+  if (block_mask == nullptr) return FA_ERR_INVALID_ARG;
+  if (mask_heads != 1 && mask_heads != pr.H) return FA_ERR_INVALID_ARG;
+  m->ptr = block_mask;
+  m->heads = mask_heads;
+  m->nbr = (pr.Nq + kMaskBlock - 1) / kMaskBlock;
+  m->nbc = (pr.Nk + kMaskBlock - 1) / kMaskBlock;
+  return FA_OK;
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                  int causal, float scale, int dtype,
+                                  const unsigned char* block_mask, int mask_heads,
+                                  fa_stream_t stream) {
+  Problem pr;
+  int st = fa::validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
+  if (st != FA_OK) return st;
+  fa::BlockMask m;
+  if ((st = fa::mask_args(pr, block_mask, mask_heads, &m)) != FA_OK) return st;
+  if ((Nk + fa::fwd_key_tile(d) - 1) / fa::fwd_key_tile(d) > fa::kFwdListCap)
+    return FA_ERR_INVALID_ARG;
+  return fa::fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream, 1,
+                        nullptr, 0, &m);
+}
+
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   Problem pr;
   if (fa::validate(B, H, Hkv, N, N, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
@@ -313,7 +346,8 @@ namespace {
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
                int Nk, int d, int causal, float scale, int dtype, void* workspace,
-               size_t workspace_bytes, fa_stream_t stream, int deterministic);
+               size_t workspace_bytes, fa_stream_t stream, int deterministic,
+               const BlockMask* mask = nullptr);
 }  // namespace
 }  // namespace fa
 
@@ -344,12 +378,35 @@ extern "C" int fa_bwd_qk(const void* q, const void* k, const void* v, const void
                         dtype, workspace, workspace_bytes, stream, deterministic);
 }
 
+extern "C" int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, void* dq, void* dk,
+                                  void* dv, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                  int causal, float scale, int dtype,
+                                  const unsigned char* block_mask, int mask_heads,
+                                  int deterministic, void* workspace, size_t workspace_bytes,
+                                  fa_stream_t stream) {
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+  Problem pr;
+  int st = fa::validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
+  if (st != FA_OK) return st;
+  fa::BlockMask m;
+  if ((st = fa::mask_args(pr, block_mask, mask_heads, &m)) != FA_OK) return st;
+  const int bq = fa::bwd_query_tile(d);
+  if (static_cast<long long>(H / Hkv) * ((Nq + bq - 1) / bq) > fa::bwd_list_cap(d))
+    return FA_ERR_INVALID_ARG;
+  if (deterministic && (Nk + fa::kDqKeyTile - 1) / fa::kDqKeyTile > fa::kDqListCap)
+    return FA_ERR_INVALID_ARG;
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale,
+                        dtype, workspace, workspace_bytes, stream, deterministic, &m);
+}
+
 namespace fa {
 namespace {
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
                int Nk, int d, int causal, float scale, int dtype, void* workspace,
-               size_t workspace_bytes, fa_stream_t stream, int deterministic) {
+               size_t workspace_bytes, fa_stream_t stream, int deterministic,
+               const BlockMask* mask) {
   Problem pr;
   int st = fa::validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
@@ -367,6 +424,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
   float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);
   fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};
+  if (mask != nullptr) a.mask = *mask;
   cudaError_t e = fa::launch_bwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fa::cuda_fail(e, "fa_bwd launch");
   return FA_OK;

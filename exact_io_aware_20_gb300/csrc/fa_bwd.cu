@@ -1,683 +1,21 @@
-// Backward pass of exact attention on sm_103a: dQ, dK, dV of sum(O o dO).
-//
-// Method ("FlashAttention-2: Faster Attention with Better Parallelism and
-// Work Partitioning", paper digest):
-//  - section 2 Q2, improvement 2 (backward): the outer loop runs over
-//    key/value tiles; dK and dV stay on chip for the whole loop, and dQ is
-//    accumulated across key/value tiles with atomic adds;
-//  - section 4 "logsumexp fusion": the softmax weights are rebuilt from the
-//    saved L as P = exp(S - L), so S and P are never stored;
-//  - section 4 notation table: D = rowsum(dO o O), computed once up front;
-//  - section 3 "FLOPs": five products per tile, S = Q K^T, dP = dO V^T,
-//    dV += P^T dO, dK += dS^T Q, dQ += dS K with dS = P o (dP - D);
-//  - section 4 "six checks", GQA/MQA: dK and dV sum over the query heads
-//    sharing a key/value head; here one CTA loops over all of them, so that
-//    sum needs no atomics.
-//
-// Three kernels: preprocess (D and a zeroed fp32 dQ accumulator), the main
-// kernel below, and a conversion of the accumulator to the output dtype
-// (with the softmax scale applied).
-//
-// Main kernel, one CTA per (batch, key/value head, 128-key tile[, half of
-// d when d = 256]); 10 warps:
-//   warp 0      TMA producer: K and V once, then (Q_i, dO_i) tiles;
-//   warp 1      MMA issuer (tcgen05, fp32 accumulators in TMEM);
-//   warps 2..5  one key row per thread: P^T = exp(S^T - L) with the masks,
-//               written to TMEM (16-bit) as the A operand of dV += P^T dO;
-//               dS^T = P^T o (dP^T - D) written to shared memory (128-byte
-//               swizzle) as the operand of dK += dS^T Q and of dQ;
-//               epilogue for dK (times scale) and dV;
-//   warps 6..9  read the dQ tile out of TMEM and add it to the fp32
-//               accumulator in global memory (red.global.add).
-// S^T and dP^T are computed with keys on the TMEM lanes (M = 128) so the
-// dK/dV accumulators and the score tiles share one layout.  Two tile shapes:
-//   d = 64:       128 query rows per step; dQ = dS K (query rows on lanes).
-//   d = 128, 256: 64 query rows per step; dQ^T = K^T dS^T (d on lanes).
-//   d = 256 is split over two CTAs by output half of d (S^T and dP^T are
-//   computed by both), because dK + dV for all 256 columns would fill TMEM.
-#include "fa.h"
-#include "fa_internal.h"
-#include "sm103_ptx.cuh"
+// Backward pass, dense; the kernels are in fa_bwd_kernel.cuh.
+#include "fa_bwd_kernel.cuh"
 
 namespace fa {
 
-namespace {
+int bwd_query_tile(int d) { return d == 64 ? 128 : 64; }
 
-constexpr int kBC = 128;        // key rows per CTA
-constexpr int kBwdThreads = 320;
-constexpr float kLog2e = 1.4426950408889634f;
-
-template <int D, int DH, int BR, int QST>
-struct BwdLayout {
-  static constexpr bool kDqT = (BR == 64);
-  static constexpr int kNch = D / 64;
-  static constexpr int kKBytes = kBC * D * 2;
-  static constexpr int kQBytes = BR * D * 2;
-  static constexpr int kDSBytes = kBC * BR * 2;
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKOff + kKBytes;
-  static constexpr int kQOff = kVOff + kKBytes;
-  static constexpr int kDOOff = kQOff + QST * kQBytes;
-  static constexpr int kDSOff = kDOOff + QST * kQBytes;
-  // Two score buffers in TMEM when there is room for them and the Q/dO ring
-  // can hold the next tile while the current one is still in use.
-  static constexpr int kSBuf = (kDqT && QST >= 2) ? 2 : 1;
-  static constexpr int kLDOff = kDSOff + kDSBytes;   // 4 warps x 2 bufs x {-L*log2e, -D} [BR]
-  static constexpr int kBarOff = kLDOff + 4 * 2 * 2 * BR * 4;
-  static constexpr int kKVFull = 0;
-  static constexpr int kQDFull = 1;
-  static constexpr int kQDEmpty = kQDFull + QST;
-  static constexpr int kSFull = kQDEmpty + QST;     // one per score buffer
-  static constexpr int kDPFull = kSFull + 2;
-  static constexpr int kPFull = kDPFull + 1;
-  static constexpr int kDSFull = kPFull + 1;
-  static constexpr int kDSEmpty = kDSFull + 1;
-  static constexpr int kDQFull = kDSEmpty + 1;
-  static constexpr int kDQEmpty = kDQFull + 1;
-  static constexpr int kFinal = kDQEmpty + 1;
-  static constexpr int kDrain = kFinal + 1;
-  static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;
-  // TMEM columns
-  static constexpr uint32_t kTdV = 0, kTdK = DH, kTS = 2 * DH, kTdP = 2 * DH + kSBuf * BR,
-                            kTdQ = 2 * DH + (kSBuf + 1) * BR;
-  static constexpr uint32_t kDqCols = kDqT ? BR : D;
-  static constexpr uint32_t kTmemCols = 512;
-  static_assert(kTdQ + kDqCols <= kTmemCols, "TMEM budget");
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kDqT ? (DH == 128) : (BR == 128 && D == DH), "tile shapes");
-};
-
-struct BwdParams {
-  const float* lse;
-  const float* delta;
-  float* dq_acc;
-  uint16_t* dk;
-  uint16_t* dv;
-  int H, Hkv, G;
-  int Nq, Nk;         // query / key lengths
-  int off;            // Nk - Nq: under the mask query i sees keys k <= i + off
-  int n_q_tiles;
-  float scale, scale_log2;
-  int heavy_first;   // dispatch order, see bwd_kernel
-  int with_dq;       // 0: dK and dV only (dQ comes from the query-outer kernel)
-  unsigned int* err;
-};
-
-template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-           const BwdParams p) {
-  using L = BwdLayout<D, DH, BR, QST>;
-  constexpr int kNSplit = D / DH;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sbase - raw);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Two dispatch orders (chosen on the host):
-  //  - key tiles vary fastest, so the CTAs of one (batch, kv head) group run
-  //    together and share its Q / dO tiles in L2;
-  //  - heavy first: under the mask the work of a CTA falls with its key tile,
-  //    so when single CTAs are long, every group's heaviest tiles go first and
-  //    the last wave holds only short CTAs.
-  int jt, dh, kh, b;
-  if (p.heavy_first) {
-    jt = blockIdx.y;
-    dh = blockIdx.x % kNSplit;
-    kh = (blockIdx.x / kNSplit) % p.Hkv;
-    b = blockIdx.x / (kNSplit * p.Hkv);
-  } else {
-    jt = blockIdx.x / kNSplit;
-    dh = blockIdx.x % kNSplit;
-    kh = blockIdx.y;
-    b = blockIdx.z;
-  }
-  const int kv0 = jt * kBC;
-  // first query tile with a row that sees key kv0 (i + off >= kv0)
-  const int i0 = CAUSAL ? max(0, kv0 - p.off) / BR : 0;
-  const int n_i = p.n_q_tiles - i0;
-  const int n_steps = p.G * n_i;
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(L::kKVFull), 1);
-    for (int s = 0; s < QST; ++s) {
-      mbar_init(bar(L::kQDFull + s), 1);
-      mbar_init(bar(L::kQDEmpty + s), 1);
-    }
-    mbar_init(bar(L::kSFull), 1);
-    mbar_init(bar(L::kSFull + 1), 1);
-    mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kPFull), 128);
-    mbar_init(bar(L::kDSFull), 128);
-    mbar_init(bar(L::kDSEmpty), 1);
-    mbar_init(bar(L::kDQFull), 1);
-    mbar_init(bar(L::kDQEmpty), 128);
-    mbar_init(bar(L::kFinal), 1);
-    mbar_init(bar(L::kDrain), 1);
-    *abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  const uint32_t tdV = tmem + L::kTdV, tdK = tmem + L::kTdK, tS0 = tmem + L::kTS,
-                 tdP = tmem + L::kTdP, tdQ = tmem + L::kTdQ;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop; one elected lane issues the copies.
-    const int zkv = b * p.Hkv + kh;
-    if (elect_one()) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kKBytes);
-      #pragma unroll
-      for (int c = 0; c < L::kNch; ++c) {
-        tma_load_3d(sbase + L::kKOff + c * (kBC * 128), &tm_k, bar(L::kKVFull), c * 64, kv0, zkv);
-        tma_load_3d(sbase + L::kVOff + c * (kBC * 128), &tm_v, bar(L::kKVFull), c * 64, kv0, zkv);
-      }
-    }
-    __syncwarp();
-    int issued = 0;
-    for (int t = 0; t < n_steps; ++t) {
-      const int st = t % QST;
-      if (t >= QST && !wait_uniform(bar(L::kQDEmpty + st), ((t / QST) + 1) & 1, abort)) break;
-      const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
-      const int zq = b * p.H + h;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kQDFull + st), 2 * L::kQBytes);
-        #pragma unroll
-        for (int c = 0; c < L::kNch; ++c) {
-          tma_load_3d(sbase + L::kQOff + st * L::kQBytes + c * (BR * 128), &tm_q,
-                      bar(L::kQDFull + st), c * 64, q0, zq);
-          tma_load_3d(sbase + L::kDOOff + st * L::kQBytes + c * (BR * 128), &tm_do,
-                      bar(L::kQDFull + st), c * 64, q0, zq);
-        }
-      }
-      __syncwarp();
-      ++issued;
-    }
-    drain_wait(bar(L::kKVFull), 0);
-    for (int t = max(0, issued - QST); t < issued; ++t)
-      drain_wait(bar(L::kQDFull + t % QST), (t / QST) & 1);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Warp-wide; each tcgen05 instruction is issued by one elected lane.
-    // Descriptors are built once and advanced by constant offsets.
-    {
-      constexpr uint32_t kIdS = idesc_f16(kBC, BR, BF16 ? 1 : 0, 0, 0);
-      constexpr uint32_t kIdKV = idesc_f16(kBC, DH, BF16 ? 1 : 0, 0, 1);
-      constexpr uint32_t kIdQ = L::kDqT ? idesc_f16(DH, BR, BF16 ? 1 : 0, 1, 1)
-                                        : idesc_f16(BR, D, BF16 ? 1 : 0, 1, 1);
-      const uint32_t dh_chunk = static_cast<uint32_t>(dh * (DH / 64));
-      // K-major views (LBO unused): K, V, Q stages, dO stages, dS^T.
-      const uint64_t k_kmaj = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
-      const uint64_t v_kmaj = smem_desc_sw128(sbase + L::kVOff, 16, 1024);
-      const uint64_t q_kmaj = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t do_kmaj = smem_desc_sw128(sbase + L::kDOOff, 16, 1024);
-      const uint64_t ds_kmaj = smem_desc_sw128(sbase + L::kDSOff, 16, 1024);
-      // MN-major views: LBO = distance between 64-column chunks.
-      const uint64_t q_mn = smem_desc_sw128(sbase + L::kQOff, BR * 128, 1024);
-      const uint64_t do_mn = smem_desc_sw128(sbase + L::kDOOff, BR * 128, 1024);
-      const uint64_t k_mn = smem_desc_sw128(sbase + L::kKOff, kBC * 128, 1024);
-      const uint64_t ds_mn = smem_desc_sw128(sbase + L::kDSOff, kBC * 128, 1024);
-      auto s_tmem = [&](int t) { return tS0 + (t % L::kSBuf) * BR; };
-      // S^T_t = K Q_t^T (waits for the (Q_t, dO_t) tile).
-      auto issue_s = [&](int t) -> bool {
-        if (!wait_uniform(bar(L::kQDFull + t % QST), (t / QST) & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t qs = (t % QST) * L::kQBytes;
-        #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t c = kk >> 2, w = kk & 3;
-          mma_ss(s_tmem(t), desc_add(k_kmaj, c * (kBC * 128) + w * 32),
-                 desc_add(q_kmaj, qs + c * (BR * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kSFull + t % L::kSBuf));
-        return true;
-      };
-      // dP^T_t = V dO_t^T (the tile is known to be loaded).
-      auto issue_dp = [&](int t) {
-        const uint32_t qs = (t % QST) * L::kQBytes;
-        #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t c = kk >> 2, w = kk & 3;
-          mma_ss(tdP, desc_add(v_kmaj, c * (kBC * 128) + w * 32),
-                 desc_add(do_kmaj, qs + c * (BR * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kDPFull));
-      };
-      bool ok = wait_uniform(bar(L::kKVFull), 0, abort);
-      if (ok && L::kSBuf == 2 && n_steps > 0) {
-        ok = issue_s(0);
-        if (ok) issue_dp(0);
-      }
-      for (int t = 0; ok && t < n_steps; ++t) {
-        const int st = t % QST;
-        const uint32_t qs = st * L::kQBytes;
-        if constexpr (L::kSBuf == 2) {
-          // The next scores go to the other buffer now, so the P / dS warps
-          // can start on them while this step's products run.
-          if (t + 1 < n_steps && !issue_s(t + 1)) break;
-        } else {
-          if (!issue_s(t)) break;
-          issue_dp(t);
-        }
-        // dV += P^T dO (P^T from TMEM, dO MN-major)
-        if (!wait_uniform(bar(L::kPFull), t & 1, abort)) break;
-        tc_fence_after();
-        #pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ts(tdV, s_tmem(t) + kk * 8, desc_add(do_mn, qs + dh_chunk * (BR * 128) + kk * 2048),
-                 kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q (dS^T K-major in shared memory, Q MN-major)
-        if (!wait_uniform(bar(L::kDSFull), t & 1, abort)) break;
-        tc_fence_after();
-        #pragma unroll
-        for (int kk = 0; kk < BR / 16; ++kk)
-          mma_ss(tdK, desc_add(ds_kmaj, (kk >> 2) * (kBC * 128) + (kk & 3) * 32),
-                 desc_add(q_mn, qs + dh_chunk * (BR * 128) + kk * 2048), kIdKV,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        // dK was the last reader of Q_t and dO_t: the stage can be refilled.
-        mma_commit(bar(L::kQDEmpty + st));
-        // dQ contribution of this key tile
-        if (p.with_dq) {
-        if (t > 0 && !wait_uniform(bar(L::kDQEmpty), (t - 1) & 1, abort)) break;
-        tc_fence_after();
-        #pragma unroll
-        for (int kk = 0; kk < kBC / 16; ++kk) {
-          if constexpr (L::kDqT) {
-            // dQ^T = K^T dS^T: A = K^T (d x keys, MN-major), B = dS^T (keys x q, MN-major)
-            mma_ss(tdQ, desc_add(k_mn, dh_chunk * (kBC * 128) + kk * 2048),
-                   desc_add(ds_mn, kk * 2048), kIdQ, kk > 0 ? 1u : 0u);
-          } else {
-            // dQ = dS K: A = dS (q x keys, MN-major), B = K (keys x d, MN-major)
-            mma_ss(tdQ, desc_add(ds_mn, kk * 2048), desc_add(k_mn, kk * 2048), kIdQ,
-                   kk > 0 ? 1u : 0u);
-          }
-        }
-        mma_commit(bar(L::kDQFull));
-        }
-        mma_commit(bar(L::kDSEmpty));
-        // The P / dS warps are done with dP^T_t (they signalled dS_t), so the
-        // next dP^T can overwrite it.
-        if constexpr (L::kSBuf == 2) {
-          if (t + 1 < n_steps) issue_dp(t + 1);
-        }
-      }
-      mma_commit(bar(L::kFinal));
-      mma_commit(bar(L::kDrain));
-      drain_wait(bar(L::kDrain), 0);
-    }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ P / dS warps
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;           // key row within the tile
-    const int kv = kv0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // Each warp stages -L*log2(e) and -D of a query tile in its own
-    // shared-memory slice (two buffers), loading the next tile's values into
-    // registers while the current tile is processed; only __syncwarp is
-    // needed.
-    float* ld_base = reinterpret_cast<float*>(smem + L::kLDOff) + (warp - 2) * 2 * 2 * BR;
-    constexpr int kPer = BR / 32;
-    float rl[kPer], rd[kPer];
-    auto load_ld = [&](int t) {
-      const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
-      const size_t base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
-      #pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        const int q = q0 + lane + 32 * u;
-        rl[u] = q < p.Nq ? -p.lse[base + q] * kLog2e : -INFINITY;
-        rd[u] = q < p.Nq ? -p.delta[base + q] : 0.f;
-      }
-    };
-    auto store_ld = [&](int t) {
-      float* dst = ld_base + (t & 1) * 2 * BR;
-      #pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        dst[lane + 32 * u] = rl[u];
-        dst[BR + lane + 32 * u] = rd[u];
-      }
-    };
-    if (n_steps > 0) {
-      load_ld(0);
-      store_ld(0);
-    }
-    __syncwarp();
-    bool ok = true;
-    for (int t = 0; t < n_steps; ++t) {
-      const int q0 = (i0 + t % n_i) * BR;
-      const float* sL = ld_base + (t & 1) * 2 * BR;   // -L * log2(e)
-      const float* sD = sL + BR;                       // -D
-      if (t + 1 < n_steps) load_ld(t + 1);             // in flight during this step
-      const uint32_t tS = tS0 + (t % L::kSBuf) * BR;
-      // P^T = exp(S^T * scale - L), masked
-      if (!wait_uniform(bar(L::kSFull + t % L::kSBuf), (t / L::kSBuf) & 1, abort)) { ok = false; break; }
-      tc_fence_after();
-      const bool kv_out = kv >= p.Nk;
-      const bool diag = CAUSAL && (q0 + p.off < kv0 + kBC);   // tile crosses the diagonal
-      const bool masked = __any_sync(0xffffffffu, kv_out || diag);
-      const f2 cs = {p.scale_log2, p.scale_log2};
-      float P[BR];
-      #pragma unroll
-      for (int c0 = 0; c0 < BR; c0 += 32) {
-        uint32_t sr[32];
-        tmem_ld32(tS + lane_off + c0, sr);
-        tmem_ld_wait();
-        reg_fence(sr);
-        #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs,
-                               f2{sL[c0 + c], sL[c0 + c + 1]});
-          P[c0 + c] = ex2_approx(arg.x);
-          P[c0 + c + 1] = ex2_approx(arg.y);
-        }
-        if (masked) {
-          #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (kv_out || (diag && kv > q0 + c0 + c + p.off)) P[c0 + c] = 0.f;
-        }
-        uint32_t pk[16];
-        #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(P[c0 + 2 * c], P[c0 + 2 * c + 1]);
-        // P^T (16-bit) goes over the first BR/2 columns of the S^T tile,
-        // which this thread has already read.
-        tmem_st16(tS + lane_off + c0 / 2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kPFull));
-      // dS^T = P^T o (dP^T - D), written to shared memory as row r of the
-      // dS^T tile with the 128-byte swizzle (16-byte unit u of a row lives
-      // at unit u ^ (row % 8)).
-      if (!wait_uniform(bar(L::kDPFull), t & 1, abort)) { ok = false; break; }
-      if (t > 0 && !wait_uniform(bar(L::kDSEmpty), (t - 1) & 1, abort)) { ok = false; break; }
-      tc_fence_after();
-      #pragma unroll
-      for (int c0 = 0; c0 < BR; c0 += 32) {
-        uint32_t dr[32];
-        tmem_ld32(tdP + lane_off + c0, dr);
-        tmem_ld_wait();
-        reg_fence(dr);
-        uint32_t w[16];
-        #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const f2 diff = fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])},
-                                f2{sD[c0 + 2 * c], sD[c0 + 2 * c + 1]});
-          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]}, diff);
-          w[c] = pack2<BF16>(ds.x, ds.y);
-        }
-        #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const int u = c0 / 8 + u4, cb = u >> 3, uu = u & 7;
-          uint4* dst = reinterpret_cast<uint4*>(smem + L::kDSOff + cb * (kBC * 128) + r * 128 +
-                                                ((uu ^ (r & 7)) * 16));
-          *dst = make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::kDSFull));
-      if (t + 1 < n_steps) {
-        store_ld(t + 1);   // the other buffer: last read during step t - 1
-        __syncwarp();
-      }
-    }
-    // ------------------------------------------------------------ dK, dV epilogue
-    if (ok && wait_uniform(bar(L::kFinal), 0, abort)) {
-      tc_fence_after();
-      const bool in_range = kv < p.Nk;
-      const size_t row = (static_cast<size_t>(b) * p.Hkv + kh) * p.Nk + (in_range ? kv : 0);
-      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + row * D + dh * DH);
-      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + row * D + dh * DH);
-      #pragma unroll
-      for (int c0 = 0; c0 < DH; c0 += 32) {
-        uint32_t a[32], k2[32];
-        tmem_ld32(tdV + lane_off + c0, a);
-        tmem_ld32(tdK + lane_off + c0, k2);
-        tmem_ld_wait();
-        reg_fence(a);
-        reg_fence(k2);
-        uint32_t wv[16], wk[16];
-        #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          wv[c] = pack2<BF16>(__uint_as_float(a[2 * c]), __uint_as_float(a[2 * c + 1]));
-          wk[c] = pack2<BF16>(__uint_as_float(k2[2 * c]) * p.scale,
-                              __uint_as_float(k2[2 * c + 1]) * p.scale);
-        }
-        if (in_range) {
-          #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            dv_row[c0 / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
-            dk_row[c0 / 8 + i] = make_uint4(wk[4 * i], wk[4 * i + 1], wk[4 * i + 2], wk[4 * i + 3]);
-          }
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ dQ warps
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    for (int t = 0; p.with_dq && t < n_steps; ++t) {
-      const int h = kh * p.G + t / n_i, q0 = (i0 + t % n_i) * BR;
-      if (!wait_uniform(bar(L::kDQFull), t & 1, abort)) break;
-      tc_fence_after();
-      constexpr int kCols = L::kDqCols;
-      uint32_t v[kCols];
-      #pragma unroll
-      for (int c0 = 0; c0 < kCols; c0 += 32)
-        tmem_ld32(tdQ + lane_off + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
-      tmem_ld_wait();
-      reg_fence(v);
-      tc_fence_before();
-      mbar_arrive(bar(L::kDQEmpty));
-      const size_t head_row = (static_cast<size_t>(b) * p.H + h) * p.Nq;
-      if constexpr (L::kDqT) {
-        // lane r = column r of this CTA's half of d; v[c] = dQ[q0 + c][dh*DH + r]
-        float* base = p.dq_acc + (head_row + q0) * D + dh * DH + r;
-        const int n_valid = min(BR, p.Nq - q0);
-        #pragma unroll
-        for (int c = 0; c < BR; ++c)
-          if (c < n_valid) atomicAdd(base + static_cast<size_t>(c) * D, __uint_as_float(v[c]));
-      } else {
-        // lane r = query row q0 + r; v[c] = dQ[q0 + r][c]
-        if (q0 + r < p.Nq) {
-          float4* base = reinterpret_cast<float4*>(p.dq_acc + (head_row + q0 + r) * D);
-          #pragma unroll
-          for (int c = 0; c < kCols / 4; ++c)
-            atomicAdd(base + c, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                            __uint_as_float(v[4 * c + 2]),
-                                            __uint_as_float(v[4 * c + 3])));
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem, L::kTmemCols);
+int bwd_list_cap(int d) {
+  switch (d) {
+    case 64: return Cfg64::kListCap;
+    case 128: return Cfg128::kListCap;
+    default: return Cfg256::kListCap;
   }
 }
-
-// D_i = dO_i . O_i (fp32) and a zeroed dQ accumulator row, one warp per row.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256)
-bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-               float* __restrict__ delta, float* __restrict__ dq_acc, size_t rows) {
-  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;   // elements per lane: 2, 4 or 8
-  const uint16_t* orow = o + row * D + lane * kPer;
-  const uint16_t* drow = dout + row * D + lane * kPer;
-  uint32_t ow[kPer / 2], dw[kPer / 2];
-  if constexpr (kPer == 2) {
-    ow[0] = *reinterpret_cast<const uint32_t*>(orow);
-    dw[0] = *reinterpret_cast<const uint32_t*>(drow);
-  } else if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(orow), c = *reinterpret_cast<const uint2*>(drow);
-    ow[0] = a.x; ow[1] = a.y; dw[0] = c.x; dw[1] = c.y;
-  } else {
-    const uint4 a = *reinterpret_cast<const uint4*>(orow), c = *reinterpret_cast<const uint4*>(drow);
-    ow[0] = a.x; ow[1] = a.y; ow[2] = a.z; ow[3] = a.w;
-    dw[0] = c.x; dw[1] = c.y; dw[2] = c.z; dw[3] = c.w;
-  }
-  float acc = 0.f;
-  #pragma unroll
-  for (int i = 0; i < kPer / 2; ++i) {
-    float2 a, c;
-    if constexpr (BF16) {
-      a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
-      c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[i]));
-    } else {
-      a = __half22float2(*reinterpret_cast<const __half2*>(&ow[i]));
-      c = __half22float2(*reinterpret_cast<const __half2*>(&dw[i]));
-    }
-    acc = fmaf(a.x, c.x, acc);
-    acc = fmaf(a.y, c.y, acc);
-  }
-  #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) delta[row] = acc;
-  if (dq_acc == nullptr) return;
-  float* arow = dq_acc + row * D + lane * kPer;
-  #pragma unroll
-  for (int i = 0; i < kPer; i += 2) *reinterpret_cast<float2*>(arow + i) = make_float2(0.f, 0.f);
-}
-
-// dq = scale * dq_acc, converted to the output dtype; 8 elements per thread.
-template <bool BF16>
-__global__ void __launch_bounds__(256)
-bwd_convert_dq(const float* __restrict__ acc, uint16_t* __restrict__ dq, size_t n8, float scale) {
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    reinterpret_cast<uint4*>(dq)[i] =
-        make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
-                   pack2<BF16>(c.x * scale, c.y * scale), pack2<BF16>(c.z * scale, c.w * scale));
-  }
-}
-
-int g_num_sms = 0;
-
-template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16>
-cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D, DH, BR, QST>;
-  cudaError_t e;
-  const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
-  // 1. preprocess
-  int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
-  bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
-      a.deterministic ? nullptr : a.dq_acc, rows);
-  timing_end(slot, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // 2. main kernel
-  CUtensorMap tq, tk, tv, tdo;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.Nq, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
-  auto kern = bwd_kernel<D, DH, BR, QST, CAUSAL, BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc)) !=
-        cudaSuccess)
-      return e;
-    attr_set = true;
-  }
-  BwdParams p;
-  p.lse = a.lse;
-  p.delta = a.delta;
-  p.dq_acc = a.dq_acc;
-  p.dk = static_cast<uint16_t*>(a.dk);
-  p.dv = static_cast<uint16_t*>(a.dv);
-  p.H = pr.H;
-  p.Hkv = pr.Hkv;
-  p.Nq = pr.Nq;
-  p.Nk = pr.Nk;
-  p.off = pr.Nk - pr.Nq;
-  p.G = pr.H / pr.Hkv;
-  p.n_q_tiles = (pr.Nq + BR - 1) / BR;
-  p.scale = pr.scale;
-  p.scale_log2 = pr.scale * kLog2e;
-  p.err = pr.err;
-  p.with_dq = a.deterministic ? 0 : 1;
-  const int n_kv_tiles = (pr.Nk + kBC - 1) / kBC;
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
-  // Heavy-first order when the longest CTA holds more than a fifth of one
-  // SM's share of the work (long causal rows); otherwise L2 locality wins.
-  p.heavy_first = 0;
-  if (CAUSAL && n_kv_tiles <= 65535) {
-    double total = 0.0;
-    for (int j = 0; j < n_kv_tiles; ++j) total += p.n_q_tiles - std::max(0, j * kBC - p.off) / BR;
-    total *= static_cast<double>(p.G) * (D / DH) * pr.Hkv * pr.B;
-    const double longest = static_cast<double>(p.G) * p.n_q_tiles;
-    p.heavy_first = longest > 0.2 * total / g_num_sms ? 1 : 0;
-  }
-  dim3 grid = p.heavy_first ? dim3((D / DH) * pr.Hkv * pr.B, n_kv_tiles, 1)
-                            : dim3(n_kv_tiles * (D / DH), pr.Hkv, pr.B);
-  slot = timing_begin(FA_KERNEL_BWD_MAIN, stream);
-  kern<<<grid, kBwdThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
-  timing_end(slot, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // 3. dQ: the query-outer kernel (deterministic) or the accumulator's conversion
-  if (a.deterministic) return launch_bwd_dq(pr, a, stream);
-  const size_t n8 = rows * D / 8;
-  const unsigned blocks = static_cast<unsigned>(
-      std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(g_num_sms) * 8));
-  slot = timing_begin(FA_KERNEL_BWD_CONVERT, stream);
-  bwd_convert_dq<BF16><<<blocks, 256, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8,
-                                                   pr.scale);
-  timing_end(slot, stream);
-  return cudaGetLastError();
-}
-
-template <int D, int DH, int BR, int QST>
-cudaError_t dispatch_flags(const Problem& pr, const BwdArgs& a, cudaStream_t s) {
-  if (pr.causal)
-    return pr.bf16 ? launch_variant<D, DH, BR, QST, true, true>(pr, a, s)
-                   : launch_variant<D, DH, BR, QST, true, false>(pr, a, s);
-  return pr.bf16 ? launch_variant<D, DH, BR, QST, false, true>(pr, a, s)
-                 : launch_variant<D, DH, BR, QST, false, false>(pr, a, s);
-}
-
-}  // namespace
 
 cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  switch (pr.d) {
-    case 64: return dispatch_flags<64, 64, 128, 3>(pr, a, stream);
-    case 128: return dispatch_flags<128, 128, 64, 3>(pr, a, stream);
-    case 256: return dispatch_flags<256, 128, 64, 1>(pr, a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.mask.ptr != nullptr) return launch_bwd_blocksparse(pr, a, stream);
+  return launch_bwd_for<false>(pr, a, stream);
 }
 
 }  // namespace fa

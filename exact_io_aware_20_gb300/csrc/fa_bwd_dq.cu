@@ -1,374 +1,11 @@
-// Deterministic dQ for the backward pass: dQ = scale * sum_j dS_j K_j with
-// no atomics.  One CTA owns a 128-row query tile of one head and loops over
-// the key tiles in a fixed order, accumulating in TMEM, so the result is the
-// same bits on every run.
-//
-// It recomputes S = Q K^T and dP = dO V^T per key tile (the main backward
-// kernel, run in its dK/dV-only mode, computes them too): two extra products
-// per tile buy run-to-run reproducibility of dQ.  The pages note that dQ is
-// accumulated across key/value blocks with atomic adds and do not discuss
-// the resulting non-determinism ("FlashAttention-2: Faster Attention with
-// Better Parallelism and Work Partitioning", paper digest, section 7); this
-// kernel is the reproducible alternative.
-//
-// Per key tile j (64 keys): S_j = Q K_j^T and dP_j = dO V_j^T into one of
-// two TMEM buffer pairs (M = 128 query rows, N = 64); warps 2..5 (one query
-// row per thread) form P = exp(S * scale - L), dS = P o (dP - D) and write
-// dS (16-bit) over the S buffer; dQ += dS K_j reads dS from TMEM (A operand)
-// and K_j from shared memory (MN-major).  The next tile's S and dP are issued
-// before the current dQ product, so the exponentials overlap the tensor work.
-#include "fa.h"
-#include "fa_internal.h"
-#include "sm103_ptx.cuh"
+// Deterministic dQ, dense; the kernel is in fa_bwd_dq_kernel.cuh.
+#include "fa_bwd_dq_kernel.cuh"
 
 namespace fa {
 
-namespace {
-
-constexpr int kDqBR = 128;           // query rows per CTA (MMA M)
-constexpr int kDqBC = 64;            // keys per tile
-constexpr int kDqThreads = 192;
-constexpr float kDqLog2e = 1.4426950408889634f;
-
-template <int D, int KST>
-struct DqLayout {
-  static constexpr int kNch = D / 64;
-  static constexpr int kQBytes = kDqBR * D * 2;
-  static constexpr int kKVBytes = kDqBC * D * 2;
-  static constexpr int kQOff = 0;
-  static constexpr int kDOOff = kQBytes;
-  static constexpr int kKOff = 2 * kQBytes;
-  static constexpr int kVOff = kKOff + KST * kKVBytes;
-  static constexpr int kBarOff = kVOff + KST * kKVBytes;
-  static constexpr int kQDFull = 0;
-  static constexpr int kKFull = 1;
-  static constexpr int kKEmpty = kKFull + KST;
-  static constexpr int kVFull = kKEmpty + KST;
-  static constexpr int kVEmpty = kVFull + KST;
-  static constexpr int kSFull = kVEmpty + KST;   // 2: S and dP of a tile done
-  static constexpr int kDSFull = kSFull + 2;     // 2: dS of a tile in TMEM
-  static constexpr int kDQDone = kDSFull + 2;
-  static constexpr int kDrain = kDQDone + 1;
-  static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTS = 0, kTdP = 2 * kDqBC, kTdQ = 4 * kDqBC, kTmemCols = 512;
-  static_assert(kTdQ + D <= kTmemCols, "TMEM budget");
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
-};
-
-struct DqParams {
-  const float* lse;
-  const float* delta;
-  uint16_t* dq;
-  int H, Hkv, G;
-  int Nq, Nk, off;    // query / key lengths; off = Nk - Nq (bottom-right mask)
-  int num_q_tiles;
-  float scale, scale_log2;
-  unsigned int* err;
-};
-
-template <int D, int KST, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(kDqThreads, 1)
-bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const DqParams p) {
-  using L = DqLayout<D, KST>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sbase - raw);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = CAUSAL ? (p.num_q_tiles - 1 - static_cast<int>(blockIdx.x))
-                        : static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int kh = h / p.G;
-  int n_kv = (p.Nk + kDqBC - 1) / kDqBC;
-  if (CAUSAL) {
-    const int last_key = min((qt + 1) * kDqBR, p.Nq) - 1 + p.off;
-    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / kDqBC + 1);
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(L::kQDFull), 1);
-    for (int s = 0; s < KST; ++s) {
-      mbar_init(bar(L::kKFull + s), 1);
-      mbar_init(bar(L::kKEmpty + s), 1);
-      mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kVEmpty + s), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kDSFull + s), 128);
-    }
-    mbar_init(bar(L::kDQDone), 1);
-    mbar_init(bar(L::kDrain), 1);
-    *abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem + L::kTS, tdP = tmem + L::kTdP, tdQ = tmem + L::kTdQ;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
-    if (elect_one()) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(L::kQDFull), 2 * L::kQBytes);
-      #pragma unroll
-      for (int c = 0; c < L::kNch; ++c) {
-        tma_load_3d(sbase + L::kQOff + c * (kDqBR * 128), &tm_q, bar(L::kQDFull), c * 64,
-                    qt * kDqBR, zq);
-        tma_load_3d(sbase + L::kDOOff + c * (kDqBR * 128), &tm_do, bar(L::kQDFull), c * 64,
-                    qt * kDqBR, zq);
-      }
-    }
-    __syncwarp();
-    int k_issued = 0, v_issued = 0;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % KST;
-      if (j >= KST && !wait_uniform(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
-        #pragma unroll
-        for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (kDqBC * 128), &tm_k,
-                      bar(L::kKFull + s), c * 64, j * kDqBC, zkv);
-      }
-      __syncwarp();
-      ++k_issued;
-      if (j >= KST && !wait_uniform(bar(L::kVEmpty + s), ((j / KST) + 1) & 1, abort)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kVFull + s), L::kKVBytes);
-        #pragma unroll
-        for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kVOff + s * L::kKVBytes + c * (kDqBC * 128), &tm_v,
-                      bar(L::kVFull + s), c * 64, j * kDqBC, zkv);
-      }
-      __syncwarp();
-      ++v_issued;
-    }
-    drain_wait(bar(L::kQDFull), 0);
-    for (int j = max(0, k_issued - KST); j < k_issued; ++j)
-      drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
-    for (int j = max(0, v_issued - KST); j < v_issued; ++j)
-      drain_wait(bar(L::kVFull + j % KST), (j / KST) & 1);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_f16(kDqBR, kDqBC, BF16 ? 1 : 0, 0, 0);
-    constexpr uint32_t kIdQ = idesc_f16(kDqBR, D, BF16 ? 1 : 0, 0, 1);
-    const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
-    const uint64_t do_desc = smem_desc_sw128(sbase + L::kDOOff, 16, 1024);
-    const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
-    const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, 16, 1024);
-    const uint64_t k_mn = smem_desc_sw128(sbase + L::kKOff, kDqBC * 128, 1024);
-    // S_j = Q K_j^T and dP_j = dO V_j^T into buffer pair j & 1.
-    auto issue_sdp = [&](int j) -> bool {
-      const int s = j % KST;
-      if (!wait_uniform(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
-      if (!wait_uniform(bar(L::kVFull + s), (j / KST) & 1, abort)) return false;
-      tc_fence_after();
-      const uint32_t buf = (j & 1) * kDqBC;
-      #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t c = kk >> 2, w = kk & 3;
-        mma_ss(tS + buf, desc_add(q_desc, c * (kDqBR * 128) + w * 32),
-               desc_add(k_desc, s * L::kKVBytes + c * (kDqBC * 128) + w * 32), kIdS,
-               kk > 0 ? 1u : 0u);
-      }
-      #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t c = kk >> 2, w = kk & 3;
-        mma_ss(tdP + buf, desc_add(do_desc, c * (kDqBR * 128) + w * 32),
-               desc_add(v_desc, s * L::kKVBytes + c * (kDqBC * 128) + w * 32), kIdS,
-               kk > 0 ? 1u : 0u);
-      }
-      mma_commit(bar(L::kSFull + (j & 1)));
-      mma_commit(bar(L::kVEmpty + s));   // V_j is not read again
-      return true;
-    };
-    bool ok = wait_uniform(bar(L::kQDFull), 0, abort);
-    // With two or more K stages the next tile's S and dP go to the other
-    // buffer pair before this tile's dQ product.  With one stage K_{j+1}
-    // can only arrive after dQ_j (K_j's last reader) has run, so the tiles
-    // are processed one after the other.
-    if (ok && KST >= 2 && n_kv > 0) ok = issue_sdp(0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      if constexpr (KST >= 2) {
-        if (j + 1 < n_kv && !issue_sdp(j + 1)) break;
-      } else {
-        if (!issue_sdp(j)) break;
-      }
-      if (!wait_uniform(bar(L::kDSFull + (j & 1)), (j >> 1) & 1, abort)) break;
-      tc_fence_after();
-      const int s = j % KST;
-      const uint32_t a_tmem = tS + (j & 1) * kDqBC;
-      #pragma unroll
-      for (int kk = 0; kk < kDqBC / 16; ++kk)
-        mma_ts(tdQ, a_tmem + kk * 8, desc_add(k_mn, s * L::kKVBytes + kk * 2048), kIdQ,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(bar(L::kKEmpty + s));   // K_j's last reader
-    }
-    mma_commit(bar(L::kDQDone));
-    mma_commit(bar(L::kDrain));
-    drain_wait(bar(L::kDrain), 0);
-  } else {
-    // ------------------------------------------------------------ dS warps
-    const int quarter = warp & 3;
-    const int row = qt * kDqBR + quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const size_t row_idx = (static_cast<size_t>(b) * p.H + h) * p.Nq + (row < p.Nq ? row : 0);
-    // -L*log2(e) and -D of this thread's row (padding rows: P = 0)
-    const float nL = row < p.Nq ? -p.lse[row_idx] * kDqLog2e : -INFINITY;
-    const float nD = row < p.Nq ? -p.delta[row_idx] : 0.f;
-    const f2 cs = {p.scale_log2, p.scale_log2}, cl = {nL, nL}, cd = {nD, nD};
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!wait_uniform(bar(L::kSFull + (j & 1)), (j >> 1) & 1, abort)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t buf = (j & 1) * kDqBC;
-      uint32_t sr[kDqBC], dr[kDqBC];
-      #pragma unroll
-      for (int c = 0; c < kDqBC / 32; ++c) {
-        tmem_ld32(tS + buf + lane_off + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-        tmem_ld32(tdP + buf + lane_off + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&dr[32 * c]));
-      }
-      tmem_ld_wait();
-      reg_fence(sr);
-      reg_fence(dr);
-      const int col0 = j * kDqBC;
-      const bool masked =
-          (CAUSAL && col0 + kDqBC - 1 > qt * kDqBR + p.off) || (col0 + kDqBC > p.Nk);
-      uint32_t w[kDqBC / 2];
-      #pragma unroll
-      for (int c = 0; c < kDqBC; c += 2) {
-        const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs, cl);
-        f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
-        if (masked) {
-          if (col0 + c >= p.Nk || (CAUSAL && col0 + c > row + p.off)) pe.x = 0.f;
-          if (col0 + c + 1 >= p.Nk || (CAUSAL && col0 + c + 1 > row + p.off)) pe.y = 0.f;
-        }
-        const f2 ds = fmul2(pe, fadd2(f2{__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])}, cd));
-        w[c / 2] = pack2<BF16>(ds.x, ds.y);
-      }
-      // dS (16-bit) over the first 32 columns of the S buffer, already read
-      tmem_st32(tS + buf + lane_off, w);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kDSFull + (j & 1)));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && n_kv == 0) {
-      // no row of this tile sees any key: dQ = 0
-      if (row < p.Nq) {
-        uint4* out = reinterpret_cast<uint4*>(p.dq + row_idx * D);
-        #pragma unroll
-        for (int i = 0; i < D / 8; ++i) out[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    } else if (ok && wait_uniform(bar(L::kDQDone), 0, abort)) {
-      tc_fence_after();
-      uint4* out = reinterpret_cast<uint4*>(p.dq + row_idx * D);
-      #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tdQ + lane_off + c0, v);
-        tmem_ld_wait();
-        reg_fence(v);
-        uint32_t o[16];
-        #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          o[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * p.scale,
-                             __uint_as_float(v[2 * i + 1]) * p.scale);
-        if (row < p.Nq) {
-          #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            out[c0 / 8 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem, L::kTmemCols);
-  }
-}
-
-template <int D, int KST, bool CAUSAL, bool BF16>
-cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  using L = DqLayout<D, KST>;
-  CUtensorMap tq, tk, tv, tdo;
-  cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.Nq, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
-  auto kern = bwd_dq_kernel<D, KST, CAUSAL, BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc)) !=
-        cudaSuccess)
-      return e;
-    attr_set = true;
-  }
-  DqParams p;
-  p.lse = a.lse;
-  p.delta = a.delta;
-  p.dq = static_cast<uint16_t*>(a.dq);
-  p.H = pr.H;
-  p.Hkv = pr.Hkv;
-  p.Nq = pr.Nq;
-  p.Nk = pr.Nk;
-  p.off = pr.Nk - pr.Nq;
-  p.G = pr.H / pr.Hkv;
-  p.num_q_tiles = (pr.Nq + kDqBR - 1) / kDqBR;
-  p.scale = pr.scale;
-  p.scale_log2 = pr.scale * kDqLog2e;
-  p.err = pr.err;
-  dim3 grid(p.num_q_tiles, pr.H, pr.B);
-  const int slot = timing_begin(FA_KERNEL_BWD_DQ, stream);
-  kern<<<grid, kDqThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
-  timing_end(slot, stream);
-  return cudaGetLastError();
-}
-
-template <int D, int KST>
-cudaError_t dispatch_dq(const Problem& pr, const BwdArgs& a, cudaStream_t s) {
-  if (pr.causal)
-    return pr.bf16 ? launch_dq_variant<D, KST, true, true>(pr, a, s)
-                   : launch_dq_variant<D, KST, true, false>(pr, a, s);
-  return pr.bf16 ? launch_dq_variant<D, KST, false, true>(pr, a, s)
-                 : launch_dq_variant<D, KST, false, false>(pr, a, s);
-}
-
-}  // namespace
-
 cudaError_t launch_bwd_dq(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  switch (pr.d) {
-    case 64: return dispatch_dq<64, 4>(pr, a, stream);
-    case 128: return dispatch_dq<128, 3>(pr, a, stream);
-    case 256: return dispatch_dq<256, 1>(pr, a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.mask.ptr != nullptr) return launch_bwd_dq_blocksparse(pr, a, stream);
+  return launch_bwd_dq_for<false>(pr, a, stream);
 }
 
 }  // namespace fa

@@ -1,589 +1,14 @@
-// Forward pass of exact attention on sm_103a: O = softmax(scale * Q K^T) V
-// and the row logsumexp L, computed tile by tile without writing the score
-// matrix to memory.
-//
-// Method ("FlashAttention-2: Faster Attention with Better Parallelism and
-// Work Partitioning", paper digest):
-//  - section 2 Q2, improvement 2: the outer loop runs over query tiles, which
-//    are independent, so work units are (batch, head, query tile);
-//  - section 2 Q2, tweak 1: the output is kept unnormalised,
-//    O~(j) = diag(exp(m(j-1) - m(j))) O~(j-1) + exp(S(j) - m(j)) V(j), and is
-//    divided by the row sum l once at the end;
-//  - section 2 Q2, tweak 2: only L = m + log(l) is written for the backward;
-//  - section 2 Q2, causal masking: key tiles entirely above the diagonal are
-//    skipped and the mask is applied only on tiles that cross it;
-//  - section 4 "six checks", GQA/MQA: query head h reads key/value head
-//    h / (H / Hkv) by index, with no copy.
-//
-// GB300 design (not the pages' A100 design): one CTA per 128-row query tile,
-// warp-specialised:
-//   warp 0      TMA producer: Q once, then K_j / V_j through two smem rings;
-//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM score buffers,
-//               O += P_j V_j with P_j read from TMEM (tcgen05 "TS" form);
-//   warps 2..5  softmax: one query row per thread, read S_j from TMEM, mask,
-//               running max / sum, write P_j back into the score buffer as
-//               16-bit, rescale O in TMEM when the max moved, epilogue.
-// The O rescale is skipped while the running max has grown by at most 2^8
-// (log2 units); the final division and L use the same stale maximum, so the
-// result is unchanged.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "fa.h"
-#include "fa_internal.h"
-#include "sm103_ptx.cuh"
+// Forward pass, dense (causal or not, with or without key-axis splits); the
+// kernel is in fa_fwd_kernel.cuh.
+#include "fa_fwd_kernel.cuh"
 
 namespace fa {
-
-namespace {
-
-constexpr int kBR = 128;             // query rows per tile (= MMA M)
-constexpr int kThreads = 192;        // 6 warps
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr float kLn2 = 0.6931471805599453f;
-
-template <int D, int BC, int KST, int VST>
-struct FwdLayout {
-  static constexpr int kNch = D / 64;                 // 64-column (128-byte) chunks
-  static constexpr int kQBytes = kBR * D * 2;
-  static constexpr int kKVBytes = BC * D * 2;
-  // For d <= 128 each V stage is followed by a 64-column chunk of ones, so
-  // the P V product, widened to N = d + 16, also sums the rounded weights of
-  // every row into 16 extra TMEM columns (the row sum l_r without ALU work).
-  static constexpr bool kOnes = D <= 128;
-  static constexpr int kOnesCols = kOnes ? 16 : 0;
-  static constexpr int kVStage = kKVBytes + (kOnes ? BC * 128 : 0);
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBytes;
-  static constexpr int kVOff = kKOff + KST * kKVBytes;
-  static constexpr int kBarOff = kVOff + VST * kVStage;
-  // barrier indices
-  static constexpr int kQFull = 0;
-  static constexpr int kKFull = 1;
-  static constexpr int kKEmpty = kKFull + KST;
-  static constexpr int kVFull = kKEmpty + KST;
-  static constexpr int kVEmpty = kVFull + VST;
-  static constexpr int kSFull = kVEmpty + VST;   // 2
-  static constexpr int kPFull = kSFull + 2;      // 2
-  static constexpr int kODone = kPFull + 2;
-  static constexpr int kDrain = kODone + 1;
-  static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
-  // TMEM columns
-  static constexpr uint32_t kS0 = 0, kS1 = BC, kO = 2 * BC;
-  static constexpr uint32_t kTmemCols = 512;
-  static_assert(kO + D + kOnesCols <= kTmemCols, "TMEM budget");
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
-};
-
-struct FwdParams {
-  void* o;
-  float* lse;
-  int H, Hkv, G;
-  int Nq, Nk;         // query rows per head (packed rows, see mask_rows) / key length
-  int off;            // under the mask query i sees keys k <= i + off
-  int mask_rows;      // query index of a row for the mask: row % mask_rows (== Nq unless
-                      // the query heads of a KV group are packed into one row block)
-  int num_q_tiles;
-  int splits;         // > 1: each CTA covers tiles_per_split key tiles and writes a
-  int tiles_per_split;  // normalised partial O (fp32) and its L to o_part / lse_part
-  float* o_part;
-  float* lse_part;
-  float scale_log2;   // scale * log2(e)
-  unsigned int* err;
-};
-
-template <int D, int BC, bool CAUSAL, bool BF16, int KST, int VST>
-__global__ void __launch_bounds__(kThreads, 1)
-fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdLayout<D, BC, KST, VST>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sbase - raw);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = p.splits > 1 ? static_cast<int>(blockIdx.x) % p.splits : 0;
-  const int xt = p.splits > 1 ? static_cast<int>(blockIdx.x) / p.splits : static_cast<int>(blockIdx.x);
-  const int qt = CAUSAL ? (p.num_q_tiles - 1 - xt) : xt;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int kh = h / p.G;
-  const bool packed = p.mask_rows != p.Nq;
-  int n_kv = (p.Nk + BC - 1) / BC;
-  if (CAUSAL) {
-    // last key any row of this tile may see (bottom-right aligned mask);
-    // negative when every row of the tile sees none (only if Nq > Nk)
-    const int max_i = packed ? p.mask_rows - 1 : min((qt + 1) * kBR, p.Nq) - 1;
-    const int last_key = max_i + p.off;
-    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
-  }
-  // key tiles [j_base, j_base + n_kv) of this CTA
-  const int j_base = split * p.tiles_per_split;
-  if (p.splits > 1) n_kv = max(0, min(n_kv, j_base + p.tiles_per_split) - j_base);
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(L::kQFull), 1);
-    for (int s = 0; s < KST; ++s) {
-      mbar_init(bar(L::kKFull + s), 1);
-      mbar_init(bar(L::kKEmpty + s), 1);
-    }
-    for (int s = 0; s < VST; ++s) {
-      mbar_init(bar(L::kVFull + s), 1);
-      mbar_init(bar(L::kVEmpty + s), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kPFull + s), 128);
-    }
-    mbar_init(bar(L::kODone), 1);
-    mbar_init(bar(L::kDrain), 1);
-    *abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
-    tmem_relinquish();
-  }
-  if constexpr (L::kOnes) {
-    if (warp >= 2) {
-      // the ones chunks (any layout of all-ones is all-ones), written once
-      const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
-      for (int sv = 0; sv < VST; ++sv) {
-        uint4* dst = reinterpret_cast<uint4*>(smem + L::kVOff + sv * L::kVStage + L::kKVBytes);
-        for (int i = threadIdx.x - 64; i < BC * 128 / 16; i += 128)
-          dst[i] = make_uint4(one2, one2, one2, one2);
-      }
-      fence_proxy_async_smem();
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  const uint32_t tS0 = tmem + L::kS0, tS1 = tmem + L::kS1, tO = tmem + L::kO;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop; one elected lane issues the copies.
-    const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
-    if (elect_one()) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
-      #pragma unroll
-      for (int c = 0; c < L::kNch; ++c)
-        tma_load_3d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, qt * kBR, zq);
-    }
-    __syncwarp();
-    int k_issued = 0, v_issued = 0;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % KST;
-      if (j >= KST && !wait_uniform(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
-        #pragma unroll
-        for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
-                      bar(L::kKFull + s), c * 64, (j_base + j) * BC, zkv);
-      }
-      __syncwarp();
-      ++k_issued;
-      const int sv = j % VST;
-      if (j >= VST && !wait_uniform(bar(L::kVEmpty + sv), ((j / VST) + 1) & 1, abort)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
-        #pragma unroll
-        for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
-                      bar(L::kVFull + sv), c * 64, (j_base + j) * BC, zkv);
-      }
-      __syncwarp();
-      ++v_issued;
-    }
-    // Never leave the CTA with copies in flight: wait for every load issued
-    // (they have completed already on the normal path).
-    drain_wait(bar(L::kQFull), 0);
-    for (int j = max(0, k_issued - KST); j < k_issued; ++j)
-      drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
-    for (int j = max(0, v_issued - VST); j < v_issued; ++j)
-      drain_wait(bar(L::kVFull + j % VST), (j / VST) & 1);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Warp-wide; each tcgen05 instruction is issued by one elected lane.
-    // Descriptors are built once and advanced by constant offsets.
-    constexpr uint32_t kIdS = idesc_f16(kBR, BC, BF16 ? 1 : 0, 0, 0);
-    constexpr uint32_t kIdO = idesc_f16(kBR, D + L::kOnesCols, BF16 ? 1 : 0, 0, 1);
-    const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
-    const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
-    const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
-    auto issue_s = [&](int j) -> bool {
-      const int s = j % KST;
-      if (!wait_uniform(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
-      tc_fence_after();
-      const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
-      const uint64_t ks = desc_add(k_desc, s * L::kKVBytes);
-      #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t c = kk >> 2, w = kk & 3;
-        mma_ss(d_tmem, desc_add(q_desc, c * (kBR * 128) + w * 32),
-               desc_add(ks, c * (BC * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(bar(L::kSFull + (j & 1)));
-      mma_commit(bar(L::kKEmpty + s));
-      return true;
-    };
-    bool ok = wait_uniform(bar(L::kQFull), 0, abort);
-    if (ok && n_kv > 0) ok = issue_s(0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      if (j + 1 < n_kv && !issue_s(j + 1)) break;
-      if (!wait_uniform(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
-      const int sv = j % VST;
-      if (!wait_uniform(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
-      tc_fence_after();
-      const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
-      const uint64_t vs = desc_add(v_desc, sv * L::kVStage);
-      #pragma unroll
-      for (int kk = 0; kk < BC / 16; ++kk)
-        mma_ts(tO, a_tmem + kk * 8, desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(bar(L::kODone));
-      mma_commit(bar(L::kVEmpty + sv));
-    }
-    // Every MMA issued above completes before TMEM is released.
-    mma_commit(bar(L::kDrain));
-    drain_wait(bar(L::kDrain), 0);
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;                 // TMEM lanes this warp may access
-    const int r_tile = quarter * 32 + lane;
-    const int row = qt * kBR + r_tile;
-    const int qi = row % p.mask_rows;             // query index of this row for the mask
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
-    bool ok = true;
-    // A warp whose 32 rows all lie past the last query row (short or packed
-    // queries) only keeps the barrier protocol: its Q rows are zero-filled,
-    // so its scores are 0 and the P it leaves in TMEM is 0, and its rows are
-    // never stored.
-    const bool idle = qt * kBR + quarter * 32 >= p.Nq;
-    for (int j = 0; j < n_kv; ++j) {
-      const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
-      if (!wait_uniform(bar(L::kSFull + (j & 1)), (j >> 1) & 1, abort)) { ok = false; break; }
-      tc_fence_after();
-      if (idle) {
-        if (j > 0 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
-        tc_fence_before();
-        mbar_arrive(bar(L::kPFull + (j & 1)));
-        continue;
-      }
-      uint32_t sr[BC];
-      #pragma unroll
-      for (int c = 0; c < BC / 32; ++c)
-        tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_ld_wait();
-      reg_fence(sr);
-      float* s = reinterpret_cast<float*>(sr);
-      const int col0 = (j_base + j) * BC;
-      const int min_i = packed ? 0 : qt * kBR;
-      const bool need_mask = (CAUSAL && col0 + BC - 1 > min_i + p.off) || (col0 + BC > p.Nk);
-      if (need_mask) {
-        #pragma unroll
-        for (int i = 0; i < BC; ++i) {
-          const int col = col0 + i;
-          if (col >= p.Nk || (CAUSAL && col > qi + p.off)) s[i] = -INFINITY;
-        }
-      }
-      // Row max as a tree of three-input maxima (independent partial maxima
-      // keep the single warp per sub-partition busy instead of waiting on a
-      // 127-long dependent chain).
-      static_assert(BC % 16 == 0, "row max tree covers 16 columns per step");
-      float mpart[8];
-      #pragma unroll
-      for (int u = 0; u < 8; ++u) mpart[u] = fmaxf(s[2 * u], s[2 * u + 1]);
-      #pragma unroll
-      for (int i = 16; i < BC; i += 16) {
-        #pragma unroll
-        for (int u = 0; u < 8; ++u) mpart[u] = fmax3(mpart[u], s[i + 2 * u], s[i + 2 * u + 1]);
-      }
-      const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
-                             fmaxf(mpart[6], mpart[7]));
-      const float m_new = fmaxf(m_ref, mx * p.scale_log2);
-      const bool need = m_new > m_ref + kRescaleThreshold;
-      const bool any = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (any) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-        l *= alpha;
-        l_r *= alpha;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      uint32_t pk[BC / 2];
-      // Exponent arguments two at a time (packed FMA); four independent
-      // partial sums of each kind (exact, and of the rounded weights).
-      f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-      float rs_r[4] = {0.f, 0.f, 0.f, 0.f};
-      const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
-      #pragma unroll
-      for (int i = 0; i < BC / 2; ++i) {
-        const f2 arg = ffma2(f2{s[2 * i], s[2 * i + 1]}, cs, cm);
-        const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
-        pk[i] = pack2<BF16>(pe.x, pe.y);
-        rs[i & 3] = fadd2(rs[i & 3], pe);
-        // l_r sums the rounded weights the P V product uses, so the final
-        // division of O normalises exactly those weights; L uses the exact l.
-        // With the ones chunk the tensor core forms l_r next to O instead.
-        if constexpr (!L::kOnes) rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
-      }
-      const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
-      l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
-      l_r += (rs_r[0] + rs_r[1]) + (rs_r[2] + rs_r[3]);
-      #pragma unroll
-      for (int c = 0; c < BC / 64; ++c)
-        tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
-      tmem_st_wait();
-      // O_DONE completes once per P V product; every phase is consumed here,
-      // in order, so a parity wait can never be confused by a skipped phase.
-      // PV_j cannot start before this thread arrives on P_FULL below, so the
-      // barrier is at most one phase ahead.
-      if (j > 0 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
-      if (any && j > 0) {
-        // O holds P_0..P_{j-1} V, all complete: rescale it.
-        tc_fence_after();
-        #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t o2[64];
-          tmem_ld32(tO + lane_off + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
-          tmem_ld32(tO + lane_off + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
-          tmem_ld_wait();
-          reg_fence(o2);
-          #pragma unroll
-          for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
-          tmem_st32(tO + lane_off + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
-          tmem_st32(tO + lane_off + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
-        }
-        if constexpr (L::kOnes) {
-          uint32_t lr[16];
-          tmem_ld16(tO + lane_off + D, lr);
-          tmem_ld_wait();
-          reg_fence(lr);
-          #pragma unroll
-          for (int i = 0; i < 16; ++i) lr[i] = __float_as_uint(__uint_as_float(lr[i]) * alpha);
-          tmem_st16(tO + lane_off + D, lr);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::kPFull + (j & 1)));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && p.splits > 1 && n_kv == 0) {
-      // this split holds no key of these rows: partial O = 0, L = -inf
-      if (row < p.Nq) {
-        const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
-        const size_t rows_total = static_cast<size_t>(gridDim.z) * p.H * p.Nq;
-        float4* orow = reinterpret_cast<float4*>(p.o_part + (split * rows_total + r) * D);
-        #pragma unroll
-        for (int i = 0; i < D / 4; ++i) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.lse_part[split * rows_total + r] = -INFINITY;
-      }
-    } else if (ok && n_kv == 0) {
-      // no row of this tile sees any key: O = 0, L = -inf
-      if (row < p.Nq) {
-        const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + r * D);
-        #pragma unroll
-        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
-        p.lse[r] = -INFINITY;
-      }
-    } else if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
-      tc_fence_after();
-      if constexpr (L::kOnes) {
-        uint32_t lr[16];
-        tmem_ld16(tO + lane_off + D, lr);
-        tmem_ld_wait();
-        reg_fence(lr);
-        l_r = __uint_as_float(lr[0]);
-      }
-      const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
-      const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-      const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
-      const bool in_range = row < p.Nq;
-      if (p.splits > 1) {
-        // partial result of this key range, combined by fwd_combine_splits
-        const size_t rows_total = static_cast<size_t>(gridDim.z) * p.H * p.Nq;
-        const size_t r = split * rows_total + row_base + (in_range ? row : 0);
-        float4* orow = reinterpret_cast<float4*>(p.o_part + r * D);
-        #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o1[32];
-          tmem_ld32(tO + lane_off + 32 * c, o1);
-          tmem_ld_wait();
-          reg_fence(o1);
-          if (in_range) {
-            #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              orow[c * 8 + i] = make_float4(
-                  __uint_as_float(o1[4 * i]) * inv_l, __uint_as_float(o1[4 * i + 1]) * inv_l,
-                  __uint_as_float(o1[4 * i + 2]) * inv_l, __uint_as_float(o1[4 * i + 3]) * inv_l);
-          }
-        }
-        if (in_range) p.lse_part[r] = lse;
-      } else {
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                             (row_base + (in_range ? row : 0)) * D);
-      #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o1[32];
-        tmem_ld32(tO + lane_off + 32 * c, o1);
-        tmem_ld_wait();
-        reg_fence(o1);
-        uint32_t w[16];
-        #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l, __uint_as_float(o1[2 * i + 1]) * inv_l);
-        if (in_range) {
-          #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
-      }
-      if (in_range) p.lse[row_base + row] = lse;
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem, L::kTmemCols);
-  }
-}
-
-// Merge the per-split partial results of one query row: with L_s the split
-// logsumexps, L = ln sum_s exp(L_s) and O = sum_s exp(L_s - L) O_s.  One warp
-// per row.  A row no split has a key for gets O = 0, L = -inf.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256)
-fwd_combine_splits(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                   uint16_t* __restrict__ o, float* __restrict__ lse, size_t rows, int splits) {
-  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;
-  float m = -INFINITY;
-  for (int sp = 0; sp < splits; ++sp) m = fmaxf(m, lse_part[sp * rows + row]);
-  uint16_t* orow = o + row * D + lane * kPer;
-  if (m == -INFINITY) {
-    #pragma unroll
-    for (int i = 0; i < kPer; i += 2) *reinterpret_cast<uint32_t*>(orow + i) = 0u;
-    if (lane == 0) lse[row] = -INFINITY;
-    return;
-  }
-  float acc[kPer];
-  #pragma unroll
-  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-  float sum = 0.f;
-  for (int sp = 0; sp < splits; ++sp) {
-    const float ls = lse_part[sp * rows + row];
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - m);
-    sum += w;
-    const float* src = o_part + (sp * rows + row) * D + lane * kPer;
-    #pragma unroll
-    for (int i = 0; i < kPer; ++i) acc[i] = fmaf(w, src[i], acc[i]);
-  }
-  const float inv = 1.f / sum;
-  #pragma unroll
-  for (int i = 0; i < kPer; i += 2)
-    *reinterpret_cast<uint32_t*>(orow + i) = pack2<BF16>(acc[i] * inv, acc[i + 1] * inv);
-  if (lane == 0) lse[row] = m + logf(sum);
-}
-
-template <int D, int BC, bool CAUSAL, bool BF16, int KST, int VST>
-cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
-  using L = FwdLayout<D, BC, KST, VST>;
-  CUtensorMap tq, tk, tv;
-  cudaError_t e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
-  auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int G = pr.H / pr.Hkv;
-  FwdParams p;
-  p.o = a.o;
-  p.lse = a.lse;
-  // Packed: the G heads of a group are G * Nq consecutive rows of q, o and
-  // lse, so the group runs as one "head" of G * Nq query rows.
-  p.H = a.pack ? pr.Hkv : pr.H;
-  p.Hkv = pr.Hkv;
-  p.G = a.pack ? 1 : G;
-  p.Nq = a.pack ? G * pr.Nq : pr.Nq;
-  p.Nk = pr.Nk;
-  p.off = pr.Nk - pr.Nq;
-  p.mask_rows = pr.Nq;
-  p.num_q_tiles = (p.Nq + kBR - 1) / kBR;
-  p.scale_log2 = pr.scale * 1.4426950408889634f;
-  p.err = pr.err;
-  const int n_kv_tiles = (pr.Nk + BC - 1) / BC;
-  p.splits = 1;
-  p.tiles_per_split = n_kv_tiles;
-  p.o_part = a.o_part;
-  p.lse_part = a.lse_part;
-  if (a.splits > 1) {
-    p.tiles_per_split = (n_kv_tiles + a.splits - 1) / a.splits;
-    p.splits = (n_kv_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-  }
-  if ((e = make_tmap_3d(&tq, a.q, D, p.Nq, pr.B * p.H, 64, kBR)) != cudaSuccess) return e;
-  dim3 grid(p.num_q_tiles * p.splits, p.H, pr.B);
-  const int slot = timing_begin(FA_KERNEL_FWD, stream);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
-  timing_end(slot, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.splits > 1) {
-    const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
-    fwd_combine_splits<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        a.o_part, a.lse_part, static_cast<uint16_t*>(a.o), a.lse, rows, p.splits);
-    e = cudaGetLastError();
-  }
-  return e;
-}
-
-template <int D, int BC, int KST, int VST>
-cudaError_t dispatch_flags(const Problem& pr, const FwdArgs& a, cudaStream_t s) {
-  if (pr.causal) {
-    return pr.bf16 ? launch_variant<D, BC, true, true, KST, VST>(pr, a, s)
-                   : launch_variant<D, BC, true, false, KST, VST>(pr, a, s);
-  }
-  return pr.bf16 ? launch_variant<D, BC, false, true, KST, VST>(pr, a, s)
-                 : launch_variant<D, BC, false, false, KST, VST>(pr, a, s);
-}
-
-}  // namespace
 
 int fwd_key_tile(int d) { return d == 256 ? 64 : 128; }
 
 cudaError_t launch_fwd(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
-  switch (pr.d) {
-    case 64: return dispatch_flags<64, 128, 3, 3>(pr, a, stream);
-    case 128: return dispatch_flags<128, 128, 2, 2>(pr, a, stream);
-    case 256: return dispatch_flags<256, 64, 2, 2>(pr, a, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.mask.ptr != nullptr) return launch_fwd_blocksparse(pr, a, stream);
+  return launch_fwd_for<false>(pr, a, stream);
 }
 
 }  // namespace fa

@@ -18,6 +18,27 @@ struct Problem {
   unsigned int* err;   // device error word (bit 0: a bounded wait expired)
 };
 
+// Block mask of block-sparse attention: bytes [heads][nbr][nbc], block
+// (i, j) covering query rows [128 i, 128 i + 128) and keys [128 j, 128 j +
+// 128); nonzero = the block is computed.  heads is 1 (one mask for every
+// query head) or H.  ptr == nullptr: dense attention.
+constexpr int kMaskBlock = 128;
+struct BlockMask {
+  const unsigned char* ptr = nullptr;
+  int heads = 1;
+  int nbr = 0, nbc = 0;   // ceil(Nq / 128), ceil(Nk / 128)
+};
+
+// Capacity of the per-CTA step lists (entries) under a block mask: key tiles
+// of the forward and of the deterministic dQ kernel, (head, query tile)
+// steps of the backward main kernel.  The C-ABI layer rejects shapes whose
+// lists could exceed them.
+constexpr int kFwdListCap = 8192;
+constexpr int kDqListCap = 8192;
+constexpr int kDqKeyTile = 64;   // keys per tile of the deterministic dQ kernel
+int bwd_list_cap(int d);
+int bwd_query_tile(int d);
+
 struct FwdArgs {
   const void* q;
   const void* k;
@@ -28,6 +49,7 @@ struct FwdArgs {
   int splits = 1;            // > 1: split the key range, partials in o_part / lse_part
   float* o_part = nullptr;   // [splits][B*H*Nq][d] fp32
   float* lse_part = nullptr; // [splits][B*H*Nq] fp32
+  BlockMask mask;            // block-sparse (needs pack == 0, splits == 1)
 };
 
 // Key tiles of the forward kernel (for choosing a split count).
@@ -46,6 +68,7 @@ struct BwdArgs {
   float* delta;    // [B, H, Nq] fp32 scratch
   float* dq_acc;   // [B, H, Nq, d] fp32 scratch (unused when deterministic)
   int deterministic;   // dQ from the query-outer kernel, without atomics
+  BlockMask mask = {};  // block-sparse
 };
 
 // Encode a 3-D tiled tensor map over a [outer, rows, cols] 16-bit tensor
@@ -59,9 +82,12 @@ int timing_begin(int kind, cudaStream_t stream);
 void timing_end(int slot, cudaStream_t stream);
 
 cudaError_t launch_fwd(const Problem& p, const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_blocksparse(const Problem& p, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 // Deterministic dQ (query-outer, no atomics); needs D in a.delta.
 cudaError_t launch_bwd_dq(const Problem& p, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 
 // Bytes of backward scratch for a problem (delta + dq accumulator, each
 // rounded up to 256 bytes).

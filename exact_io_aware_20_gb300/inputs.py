@@ -75,3 +75,14 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu", Nk: int | None 
             t = t * w.value_scale
         out.append(t.to(w.torch_dtype).to(device))
     return tuple(out)
+
+
+def make_block_mask(heads: int, Nq: int, Nk: int, density: float, seed: int,
+                    device: str | torch.device = "cpu") -> torch.Tensor:
+    """Seeded random block mask for block-sparse attention: uint8
+    [heads, ceil(Nq/128), ceil(Nk/128)], each 128 x 128 block kept (1) with
+    probability ``density``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (heads, -(-Nq // 128), -(-Nk // 128))
+    return (torch.rand(shape, generator=g) < density).to(torch.uint8).to(device)

@@ -177,6 +177,40 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    int d, int causal, float scale, int dtype, fa_stream_t stream);
 
 /*
+ * Block-sparse attention ("FlashAttention: Fast and Memory-Efficient Exact
+ * Attention with IO-Awareness", abstract and "Key contributions": block-sparse
+ * FlashAttention computes attention only on the nonzero blocks of a given
+ * block pattern).  Read here as exact attention restricted to the kept
+ * blocks: query i of head h sees key k only where
+ *     block_mask[hm][i / 128][k / 128] != 0      (hm = 0 if mask_heads == 1, else h)
+ * and, when causal, k <= i + Nk - Nq.  The result is exact for that mask (an
+ * approximation of dense attention only through the mask itself); blocks
+ * whose mask byte is zero cost no loads and no products.  A query row that
+ * sees no key gets O = 0 and L = -inf; a key that no query sees gets
+ * dK = dV = 0.
+ *
+ * block_mask: device memory, bytes [mask_heads][ceil(Nq/128)][ceil(Nk/128)],
+ * row-major, any alignment, read-only, nonzero = the block is computed.
+ * mask_heads is 1 (one pattern for every query head) or H (one per query
+ * head).  Other arguments, layouts and outputs as fa_fwd_qk / fa_bwd_qk; the
+ * backward must get the forward's mask.  Limits (FA_ERR_INVALID_ARG beyond
+ * them, for the per-CTA work lists): ceil(Nk / 128) <= 8192 for the forward
+ * at d <= 128 (ceil(Nk / 64) <= 8192 at d = 256); for the backward,
+ * (H / Hkv) * ceil(Nq / 64) <= 8192 (d = 128), (H / Hkv) * ceil(Nq / 128) <=
+ * 8192 (d = 64), (H / Hkv) * ceil(Nq / 64) <= 4096 (d = 256), and with
+ * deterministic = 1 also ceil(Nk / 64) <= 8192.
+ */
+int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                       const unsigned char *block_mask, int mask_heads, fa_stream_t stream);
+
+int fa_bwd_blocksparse(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                       int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                       const unsigned char *block_mask, int mask_heads, int deterministic,
+                       void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports (and clears) the device-side error
  * word: FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
  * call, FA_ERR_CUDA if the stream itself failed, FA_OK otherwise.

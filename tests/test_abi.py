@@ -110,3 +110,39 @@ def test_splitkv_workspace_checks(lib):
     st = lib.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv, Nq, Nk, d, 1, 0.088,
                             binding.FA_BF16, -1, FAKE, 1 << 30, None)
     assert st == binding.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(mask=None), binding.FA_ERR_INVALID_ARG),
+    (dict(mask_heads=3), binding.FA_ERR_INVALID_ARG),      # neither 1 nor H
+    (dict(mask_heads=0), binding.FA_ERR_INVALID_ARG),
+    (dict(Nk=8193 * 128), binding.FA_ERR_INVALID_ARG),     # forward key-tile list
+    (dict(d=256, Nk=8193 * 64), binding.FA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), binding.FA_ERR_INVALID_ARG),
+    (dict(d=80), binding.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_blocksparse_rejects(lib, case, expect):
+    a = dict(q=FAKE, Nk=512, d=128, mask=FAKE, mask_heads=1)
+    a.update(case)
+    st = lib.fa_fwd_blocksparse(a["q"], FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 256, a["Nk"], a["d"], 0,
+                                0.1, binding.FA_BF16, a["mask"], a["mask_heads"], None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(mask=None), binding.FA_ERR_INVALID_ARG),
+    (dict(mask_heads=2), binding.FA_ERR_INVALID_ARG),
+    (dict(det=2), binding.FA_ERR_INVALID_ARG),
+    # (H / Hkv) * ceil(Nq / 64) above the d = 128 step list (8192)
+    (dict(H=8, Hkv=2, Nq=64 * 2049), binding.FA_ERR_INVALID_ARG),
+    (dict(d=256, H=4, Hkv=1, Nq=64 * 1025), binding.FA_ERR_INVALID_ARG),   # 4096 at d = 256
+    (dict(det=1, Nk=64 * 8193), binding.FA_ERR_INVALID_ARG),   # dQ kernel key-tile list
+    (dict(ws=None), binding.FA_ERR_WORKSPACE),
+])
+def test_bwd_blocksparse_rejects(lib, case, expect):
+    a = dict(H=4, Hkv=4, Nq=256, Nk=256, d=128, mask=FAKE, mask_heads=1, det=0, ws=FAKE)
+    a.update(case)
+    st = lib.fa_bwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, a["H"],
+                                a["Hkv"], a["Nq"], a["Nk"], a["d"], 1, 0.1, binding.FA_F16,
+                                a["mask"], a["mask_heads"], a["det"], a["ws"], 1 << 40, None)
+    assert st == expect
