@@ -40,7 +40,9 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "gqa8k"
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_fwd.cu", "exact_io_aware_20_gb300/csrc/fa_bwd.cu",
+KERNEL_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_fwd_kernel.cuh",
+                  "exact_io_aware_20_gb300/csrc/fa_bwd_kernel.cuh",
+                  "exact_io_aware_20_gb300/csrc/block_list.cuh",
                   "exact_io_aware_20_gb300/csrc/sm103_ptx.cuh"]
 
 
@@ -55,8 +57,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["train", "decode"], default="train",
-                    help="train: fwd+bwd step (the headline); decode: short-query forward")
+    ap.add_argument("--mode", choices=["train", "decode", "blocksparse"], default="train",
+                    help="train: fwd+bwd step (the headline); decode: short-query forward; "
+                         "blocksparse: fwd+bwd step under a random block mask")
+    ap.add_argument("--density", type=float, default=0.25,
+                    help="blocksparse: fraction of 128x128 blocks kept")
     ap.add_argument("--decode-nq", type=int, default=1)
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (smaller profiling captures)")
@@ -301,6 +306,79 @@ def run_decode(args):
     return 0
 
 
+# ---------------------------------------------------------------- block-sparse
+def kept_pairs(mask: torch.Tensor, N: int, causal: bool) -> int:
+    """(query, key) pairs a shared block mask [1, N/128, N/128] keeps per head
+    (N a multiple of 128), with the causal diagonal blocks half kept."""
+    nb = N // 128
+    keep = mask[0].bool().cpu()
+    if not causal:
+        return int(keep.sum()) * 128 * 128
+    below = int((keep & torch.ones(nb, nb, dtype=torch.bool).tril(-1)).sum())
+    diag = int((keep & torch.eye(nb, dtype=torch.bool)).sum())
+    return below * 128 * 128 + diag * (128 * 129 // 2)
+
+
+def run_blocksparse(args):
+    """fa_fwd_blocksparse + fa_bwd_blocksparse on the gqa8k shapes under a
+    seeded random block mask (one pattern for all heads): TFLOP/s counted on
+    the kept (query, key) pairs only, and the time against the dense step."""
+    torch.cuda.set_device(0)
+    from exact_io_aware_20_gb300 import binding
+    from exact_io_aware_20_gb300.inputs import make_block_mask
+    binding.load()
+    w = WORKLOADS[args.workload]
+    q, k, v, do = make_inputs(w, "cuda")
+    mask = make_block_mask(1, w.N, w.N, args.density, w.seed, "cuda")
+    pairs = kept_pairs(mask, w.N, w.causal) * w.B * w.H
+    flops = 4.0 * w.d * pairs * 3.5          # forward 4d, backward 2.5x that, per kept pair
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d), dtype=torch.uint8,
+                     device="cuda")
+
+    def sparse_step():
+        binding.forward_blocksparse(q, k, v, mask, w.causal, w.scale, o, lse)
+        binding.backward_blocksparse(q, k, v, o, lse, do, mask, w.causal, w.scale, dq, dk, dv, ws)
+
+    def dense_step():
+        binding.forward(q, k, v, w.causal, w.scale, o, lse)
+        binding.backward(q, k, v, o, lse, do, w.causal, w.scale, dq, dk, dv, ws)
+
+    res = {}
+    for name, fn in (("sparse", sparse_step), ("dense", dense_step)):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / args.steps
+    binding.device_status()
+    peaks, src = load_peaks()
+    value = flops / (res["sparse"] * 1e-3) / 1e12
+    dense_pairs = w.B * w.H * (w.N * (w.N + 1) // 2 if w.causal else w.N * w.N)
+    print(json.dumps({
+        "metric": "block-sparse attention fwd+bwd TFLOP/s (kept pairs)", "unit": "TFLOP/s",
+        "value": round(value, 1), "higher_is_better": True, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["sparse"], 4), "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name} (B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d}, "
+                               f"causal={w.causal}) under a random 128x128 block mask, "
+                               f"density {args.density}, shared by all heads; inputs larger "
+                               f"than L2"},
+        "kept_fraction": round(pairs / dense_pairs, 4),
+        "dense_ms_per_step": round(res["dense"], 4),
+        "speedup_vs_dense": round(res["dense"] / res["sparse"], 3),
+        "frac_of_burst": round(value / peaks["bf16_tflops"], 4), "peak_source": src}),
+        flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse_args()
@@ -308,6 +386,8 @@ def main():
         return run_reference(args)
     if args.mode == "decode":
         return run_decode(args)
+    if args.mode == "blocksparse":
+        return run_blocksparse(args)
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
