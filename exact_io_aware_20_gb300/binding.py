@@ -39,6 +39,9 @@ SIGNATURES = {
                                 _i, _vp]),
     "fa_bwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                 _i, _f, _i, _vp, _i, _i, _vp, _sz, _vp]),
+    "fa_fwd_strided": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_bwd_strided": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                            _f, _i, _vp, _i, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_selftest_expired_wait": (_i, [_i, _vp]),
@@ -141,17 +144,75 @@ def fa_get_device_status(stream=None) -> int:
 
 
 # ---------------------------------------------------------------- tensor helpers
-def _shapes(q, k, v):
-    """(B, H, Hkv, Nq, Nk, d) of q [B,H,Nq,d], k and v [B,Hkv,Nk,d]."""
+class FaStrides(ctypes.Structure):
+    """struct fa_strides: element strides (batch, head, row) of a [B][heads][N][d] view."""
+    _fields_ = [("batch", ctypes.c_longlong), ("head", ctypes.c_longlong),
+                ("row", ctypes.c_longlong)]
+
+
+def _shapes(q, k, v, contiguous=True):
+    """(B, H, Hkv, Nq, Nk, d) of q [B,H,Nq,d], k and v [B,Hkv,Nk,d] (views with
+    the last dimension contiguous are accepted when contiguous=False)."""
     if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
         raise ValueError("expected q [B,H,Nq,d], k and v [B,Hkv,Nk,d]")
     B, H, Nq, d = q.shape
     if k.shape[0] != B or k.shape[3] != d:
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)}")
     for t in (q, k, v):
-        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
-            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+        if not t.is_cuda or t.dtype != q.dtype:
+            raise ValueError("q, k, v must be CUDA tensors of one dtype")
+        if contiguous and not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+        if not contiguous and t.stride(3) != 1:
+            raise ValueError("the last (d) dimension must be contiguous")
     return B, H, k.shape[1], Nq, k.shape[2], d
+
+
+def _strides(*ts):
+    """fa_strides[len(ts)] of [B, heads, N, d] views (d contiguous)."""
+    arr = (FaStrides * len(ts))()
+    for i, t in enumerate(ts):
+        if t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError("expected a [B, heads, N, d] view with d contiguous")
+        arr[i] = FaStrides(t.stride(0), t.stride(1), t.stride(2))
+    return arr
+
+
+def forward_strided(q, k, v, causal: bool, scale: float, out=None, lse=None, stream=None):
+    """fa_fwd_strided: q [B,H,Nq,d], k, v [B,Hkv,Nk,d] given as any views whose
+    d elements are contiguous (e.g. x.transpose(1, 2) of a [B, N, H, d]
+    tensor); out (allocated like q's layout unless given) likewise.  Returns
+    (o, lse)."""
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v, contiguous=False)
+    if out is None:
+        out = torch.empty_like(q)   # same strides as q when q is dense in memory
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check(load().fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, Nq,
+                                 Nk, d, int(causal), float(scale), _dtype_code(q),
+                                 _strides(q, k, v, out), _stream_ptr(stream)), "fa_fwd_strided")
+    return out, lse
+
+
+def backward_strided(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None,
+                     dv=None, workspace=None, stream=None, deterministic: bool = False):
+    """fa_bwd_strided: the gradients of forward_strided; every tensor may be a
+    strided view (d contiguous); dq, dk, dv are allocated like q, k, v unless
+    given.  Returns (dq, dk, dv)."""
+    B, H, Hkv, Nq, Nk, d = _shapes(q, k, v, contiguous=False)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, H, Hkv, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(load().fa_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, Nq, Nk, d, int(causal),
+                                 float(scale), _dtype_code(q),
+                                 _strides(q, k, v, o, dout, dq, dk, dv), int(bool(deterministic)),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)), "fa_bwd_strided")
+    return dq, dk, dv
 
 
 def forward(q, k, v, causal: bool, scale: float, out=None, lse=None, stream=None):

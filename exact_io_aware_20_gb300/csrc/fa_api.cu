@@ -112,17 +112,17 @@ int validate(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float sca
 
 }  // namespace
 
-cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int cols, int rows, int outer,
-                         int box_cols, int box_rows) {
+cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int cols, int rows, int heads,
+                         int batch, const Strides& st, int box_cols, int box_rows) {
   std::call_once(g_encode_once, load_encoder);
   if (g_encode_err != cudaSuccess) return g_encode_err;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
-                           static_cast<cuuint64_t>(cols) * 2 * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims,
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                           static_cast<cuuint64_t>(st.b) * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -233,10 +233,25 @@ size_t splitkv_bytes(int B, int H, int Nq, int d, int splits) {
   return o + l;
 }
 
+// Strides of a caller's view: each a positive multiple of 8 elements (16
+// bytes, the tensor-map stride unit) below 2^39 elements.
+bool valid_strides(const fa_strides* s, int n, Strides* out) {
+  if (s == nullptr) return false;
+  for (int i = 0; i < n; ++i) {
+    const long long v[3] = {s[i].batch, s[i].head, s[i].row};
+    for (long long x : v)
+      if (x < 8 || x % 8 != 0 || x >= (1ll << 39)) return false;
+    out[i] = {s[i].batch, s[i].head, s[i].row};
+  }
+  return true;
+}
+
+// st: element strides of q, k, v, o (nullptr: contiguous).
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
                fa_stream_t stream, int splits = 1, void* workspace = nullptr,
-               size_t workspace_bytes = 0, const BlockMask* mask = nullptr) {
+               size_t workspace_bytes = 0, const BlockMask* mask = nullptr,
+               const Strides* strd = nullptr) {
   Problem pr;
   int st = validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
@@ -251,7 +266,18 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   }
   if ((st = check_device(&pr.err)) != FA_OK) return st;
   FwdArgs a{q, k, v, o, lse};
-  a.pack = pack_groups(H, Hkv, Nq) && mask == nullptr ? 1 : 0;
+  if (strd != nullptr) {
+    a.qs = strd[0];
+    a.ks = strd[1];
+    a.vs = strd[2];
+    a.os = strd[3];
+  } else {
+    a.qs = a.os = contiguous_strides(H, Nq, d);
+    a.ks = a.vs = contiguous_strides(Hkv, Nk, d);
+  }
+  // packing needs the G * Nq rows of a group evenly spaced in q and o
+  const bool even = Nq == 1 || (a.qs.h == Nq * a.qs.n && a.os.h == Nq * a.os.n);
+  a.pack = pack_groups(H, Hkv, Nq) && mask == nullptr && even ? 1 : 0;
   if (mask != nullptr) a.mask = *mask;
   a.splits = splits;
   if (splits > 1) {
@@ -335,6 +361,16 @@ extern "C" int fa_fwd_blocksparse(const void* q, const void* k, const void* v, v
                         nullptr, 0, &m);
 }
 
+extern "C" int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                              float scale, int dtype, const fa_strides* strides,
+                              fa_stream_t stream) {
+  fa::Strides st[4];
+  if (!fa::valid_strides(strides, 4, st)) return FA_ERR_INVALID_ARG;
+  return fa::fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream, 1,
+                        nullptr, 0, nullptr, st);
+}
+
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   Problem pr;
   if (fa::validate(B, H, Hkv, N, N, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
@@ -347,7 +383,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
                int Nk, int d, int causal, float scale, int dtype, void* workspace,
                size_t workspace_bytes, fa_stream_t stream, int deterministic,
-               const BlockMask* mask = nullptr);
+               const BlockMask* mask = nullptr, const Strides* strd = nullptr);
 }  // namespace
 }  // namespace fa
 
@@ -400,13 +436,26 @@ extern "C" int fa_bwd_blocksparse(const void* q, const void* k, const void* v, c
                         dtype, workspace, workspace_bytes, stream, deterministic, &m);
 }
 
+extern "C" int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int Hkv, int Nq, int Nk, int d, int causal,
+                              float scale, int dtype, const fa_strides* strides,
+                              int deterministic, void* workspace, size_t workspace_bytes,
+                              fa_stream_t stream) {
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+  fa::Strides st[8];
+  if (!fa::valid_strides(strides, 8, st)) return FA_ERR_INVALID_ARG;
+  return fa::bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, causal, scale,
+                        dtype, workspace, workspace_bytes, stream, deterministic, nullptr, st);
+}
+
 namespace fa {
 namespace {
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
                int Nk, int d, int causal, float scale, int dtype, void* workspace,
                size_t workspace_bytes, fa_stream_t stream, int deterministic,
-               const BlockMask* mask) {
+               const BlockMask* mask, const Strides* strd) {
   Problem pr;
   int st = fa::validate(B, H, Hkv, Nq, Nk, d, causal, scale, dtype, &pr);
   if (st != FA_OK) return st;
@@ -425,6 +474,19 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
                                         (rows * sizeof(float) + 255) / 256 * 256);
   fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};
   if (mask != nullptr) a.mask = *mask;
+  if (strd != nullptr) {
+    a.qs = strd[0];
+    a.ks = strd[1];
+    a.vs = strd[2];
+    a.os = strd[3];
+    a.dos = strd[4];
+    a.dqs = strd[5];
+    a.dks = strd[6];
+    a.dvs = strd[7];
+  } else {
+    a.qs = a.os = a.dos = a.dqs = contiguous_strides(H, Nq, d);
+    a.ks = a.vs = a.dks = a.dvs = contiguous_strides(Hkv, Nk, d);
+  }
   cudaError_t e = fa::launch_bwd(pr, a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fa::cuda_fail(e, "fa_bwd launch");
   return FA_OK;

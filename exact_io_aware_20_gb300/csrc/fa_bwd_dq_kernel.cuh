@@ -78,6 +78,7 @@ struct DqParams {
   int num_q_tiles;
   float scale, scale_log2;
   BlockMask mask;
+  Strides dqs;        // element strides of dq
   unsigned int* err;
 };
 
@@ -152,7 +153,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
     if (elect_one()) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
@@ -161,10 +161,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_arrive_expect_tx(bar(L::kQDFull), 2 * L::kQBytes);
       #pragma unroll
       for (int c = 0; c < L::kNch; ++c) {
-        tma_load_3d(sbase + L::kQOff + c * (kDqBR * 128), &tm_q, bar(L::kQDFull), c * 64,
-                    qt * kDqBR, zq);
-        tma_load_3d(sbase + L::kDOOff + c * (kDqBR * 128), &tm_do, bar(L::kQDFull), c * 64,
-                    qt * kDqBR, zq);
+        tma_load_4d(sbase + L::kQOff + c * (kDqBR * 128), &tm_q, bar(L::kQDFull), c * 64,
+                    qt * kDqBR, h, b);
+        tma_load_4d(sbase + L::kDOOff + c * (kDqBR * 128), &tm_do, bar(L::kQDFull), c * 64,
+                    qt * kDqBR, h, b);
       }
     }
     __syncwarp();
@@ -176,8 +176,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (kDqBC * 128), &tm_k,
-                      bar(L::kKFull + s), c * 64, key_tile(j) * kDqBC, zkv);
+          tma_load_4d(sbase + L::kKOff + s * L::kKVBytes + c * (kDqBC * 128), &tm_k,
+                      bar(L::kKFull + s), c * 64, key_tile(j) * kDqBC, kh, b);
       }
       __syncwarp();
       ++k_issued;
@@ -186,8 +186,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_arrive_expect_tx(bar(L::kVFull + s), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kVOff + s * L::kKVBytes + c * (kDqBC * 128), &tm_v,
-                      bar(L::kVFull + s), c * 64, key_tile(j) * kDqBC, zkv);
+          tma_load_4d(sbase + L::kVOff + s * L::kKVBytes + c * (kDqBC * 128), &tm_v,
+                      bar(L::kVFull + s), c * 64, key_tile(j) * kDqBC, kh, b);
       }
       __syncwarp();
       ++v_issued;
@@ -262,6 +262,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int row = qt * kDqBR + quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const size_t row_idx = (static_cast<size_t>(b) * p.H + h) * p.Nq + (row < p.Nq ? row : 0);
+    const long long dq_off =
+        b * p.dqs.b + h * p.dqs.h + static_cast<long long>(row < p.Nq ? row : 0) * p.dqs.n;
     // -L*log2(e) and -D of this thread's row (padding rows: P = 0)
     const float nL = row < p.Nq ? -p.lse[row_idx] * kDqLog2e : -INFINITY;
     const float nD = row < p.Nq ? -p.delta[row_idx] : 0.f;
@@ -305,13 +307,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (ok && n_kv == 0) {
       // no row of this tile sees any key: dQ = 0
       if (row < p.Nq) {
-        uint4* out = reinterpret_cast<uint4*>(p.dq + row_idx * D);
+        uint4* out = reinterpret_cast<uint4*>(p.dq + dq_off);
         #pragma unroll
         for (int i = 0; i < D / 8; ++i) out[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     } else if (ok && wait_uniform(bar(L::kDQDone), 0, abort)) {
       tc_fence_after();
-      uint4* out = reinterpret_cast<uint4*>(p.dq + row_idx * D);
+      uint4* out = reinterpret_cast<uint4*>(p.dq + dq_off);
       #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
@@ -347,10 +349,11 @@ cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t 
   using L = DqLayout<D, KST>;
   CUtensorMap tq, tk, tv, tdo;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.Nq, pr.B * pr.H, 64, kDqBR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, kDqBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tq, a.q, D, pr.Nq, pr.H, pr.B, a.qs, 64, kDqBR)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tdo, a.dout, D, pr.Nq, pr.H, pr.B, a.dos, 64, kDqBR)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_4d(&tk, a.k, D, pr.Nk, pr.Hkv, pr.B, a.ks, 64, kDqBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tv, a.v, D, pr.Nk, pr.Hkv, pr.B, a.vs, 64, kDqBC)) != cudaSuccess) return e;
   auto kern = bwd_dq_kernel<D, KST, CAUSAL, BF16, SPARSE>;
   constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
   static bool attr_set = false;
@@ -374,6 +377,7 @@ cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t 
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kDqLog2e;
   p.mask = a.mask;
+  p.dqs = a.dqs;
   p.err = pr.err;
   dim3 grid(p.num_q_tiles, pr.H, pr.B);
   const int slot = timing_begin(FA_KERNEL_BWD_DQ, stream);

@@ -116,6 +116,7 @@ struct BwdParams {
   int heavy_first;   // dispatch order, see bwd_kernel
   int with_dq;       // 0: dK and dV only (dQ comes from the query-outer kernel)
   BlockMask mask;    // block-sparse: only the kept blocks' steps
+  Strides dks, dvs;  // element strides of dk, dv
   unsigned int* err;
 };
 
@@ -229,7 +230,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop; one elected lane issues the copies.
-    const int zkv = b * p.Hkv + kh;
     if (elect_one()) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -238,8 +238,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kKBytes);
       #pragma unroll
       for (int c = 0; c < L::kNch; ++c) {
-        tma_load_3d(sbase + L::kKOff + c * (kBC * 128), &tm_k, bar(L::kKVFull), c * 64, kv0, zkv);
-        tma_load_3d(sbase + L::kVOff + c * (kBC * 128), &tm_v, bar(L::kKVFull), c * 64, kv0, zkv);
+        tma_load_4d(sbase + L::kKOff + c * (kBC * 128), &tm_k, bar(L::kKVFull), c * 64, kv0, kh, b);
+        tma_load_4d(sbase + L::kVOff + c * (kBC * 128), &tm_v, bar(L::kKVFull), c * 64, kv0, kh, b);
       }
     }
     __syncwarp();
@@ -249,15 +249,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (t >= QST && !wait_uniform(bar(L::kQDEmpty + st), ((t / QST) + 1) & 1, abort)) break;
       int h, q0;
       step_hq(t, h, q0);
-      const int zq = b * p.H + h;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kQDFull + st), 2 * L::kQBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c) {
-          tma_load_3d(sbase + L::kQOff + st * L::kQBytes + c * (BR * 128), &tm_q,
-                      bar(L::kQDFull + st), c * 64, q0, zq);
-          tma_load_3d(sbase + L::kDOOff + st * L::kQBytes + c * (BR * 128), &tm_do,
-                      bar(L::kQDFull + st), c * 64, q0, zq);
+          tma_load_4d(sbase + L::kQOff + st * L::kQBytes + c * (BR * 128), &tm_q,
+                      bar(L::kQDFull + st), c * 64, q0, h, b);
+          tma_load_4d(sbase + L::kDOOff + st * L::kQBytes + c * (BR * 128), &tm_do,
+                      bar(L::kQDFull + st), c * 64, q0, h, b);
         }
       }
       __syncwarp();
@@ -497,9 +496,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (ok && wait_uniform(bar(L::kFinal), 0, abort)) {
       tc_fence_after();
       const bool in_range = kv < p.Nk;
-      const size_t row = (static_cast<size_t>(b) * p.Hkv + kh) * p.Nk + (in_range ? kv : 0);
-      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + row * D + dh * DH);
-      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + row * D + dh * DH);
+      const long long kvr = in_range ? kv : 0;
+      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + b * p.dvs.b + kh * p.dvs.h + kvr * p.dvs.n +
+                                               dh * DH);
+      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + b * p.dks.b + kh * p.dks.h + kvr * p.dks.n +
+                                               dh * DH);
       // a key tile no step reached (block mask) has dK = dV = 0; its TMEM
       // accumulators were never written
       const uint32_t live = n_steps > 0 ? 0xffffffffu : 0u;
@@ -583,17 +584,26 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
 }
 
-// D_i = dO_i . O_i (fp32) and a zeroed dQ accumulator row, one warp per row.
+// Element offset of row (b * H + h) * N + i of a strided [B][H][N][d] view.
+__device__ __forceinline__ long long view_offset(size_t row, int H, int N, const Strides& s) {
+  const size_t bh = row / N;
+  const long long i = static_cast<long long>(row - bh * N);
+  return static_cast<long long>(bh / H) * s.b + static_cast<long long>(bh % H) * s.h + i * s.n;
+}
+
+// D_i = dO_i . O_i (fp32) and a zeroed dQ accumulator row, one warp per row
+// (delta and the accumulator are contiguous; o and dout strided).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-               float* __restrict__ delta, float* __restrict__ dq_acc, size_t rows) {
+               float* __restrict__ delta, float* __restrict__ dq_acc, size_t rows, int H, int N,
+               Strides os, Strides dos) {
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   constexpr int kPer = D / 32;   // elements per lane: 2, 4 or 8
-  const uint16_t* orow = o + row * D + lane * kPer;
-  const uint16_t* drow = dout + row * D + lane * kPer;
+  const uint16_t* orow = o + view_offset(row, H, N, os) + lane * kPer;
+  const uint16_t* drow = dout + view_offset(row, H, N, dos) + lane * kPer;
   uint32_t ow[kPer / 2], dw[kPer / 2];
   if constexpr (kPer == 2) {
     ow[0] = *reinterpret_cast<const uint32_t*>(orow);
@@ -629,15 +639,19 @@ bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout
   for (int i = 0; i < kPer; i += 2) *reinterpret_cast<float2*>(arow + i) = make_float2(0.f, 0.f);
 }
 
-// dq = scale * dq_acc, converted to the output dtype; 8 elements per thread.
-template <bool BF16>
+// dq = scale * dq_acc (contiguous), converted to the output dtype and
+// written to the strided dq view; 8 elements per thread.
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
-bwd_convert_dq(const float* __restrict__ acc, uint16_t* __restrict__ dq, size_t n8, float scale) {
+bwd_convert_dq(const float* __restrict__ acc, uint16_t* __restrict__ dq, size_t n8, float scale,
+               int H, int N, Strides dqs) {
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
     const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    reinterpret_cast<uint4*>(dq)[i] =
+    const size_t row = i / (D / 8);
+    const int col = static_cast<int>(i - row * (D / 8)) * 8;
+    *reinterpret_cast<uint4*>(dq + view_offset(row, H, N, dqs) + col) =
         make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
                    pack2<BF16>(c.x * scale, c.y * scale), pack2<BF16>(c.z * scale, c.w * scale));
   }
@@ -654,15 +668,15 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
   bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
-      a.deterministic ? nullptr : a.dq_acc, rows);
+      a.deterministic ? nullptr : a.dq_acc, rows, pr.H, pr.Nq, a.os, a.dos);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 2. main kernel
   CUtensorMap tq, tk, tv, tdo;
-  if ((e = make_tmap_3d(&tq, a.q, D, pr.Nq, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, D, pr.Nq, pr.B * pr.H, 64, BR)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, kBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tq, a.q, D, pr.Nq, pr.H, pr.B, a.qs, 64, BR)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tdo, a.dout, D, pr.Nq, pr.H, pr.B, a.dos, 64, BR)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tk, a.k, D, pr.Nk, pr.Hkv, pr.B, a.ks, 64, kBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tv, a.v, D, pr.Nk, pr.Hkv, pr.B, a.vs, 64, kBC)) != cudaSuccess) return e;
   auto kern = bwd_kernel<D, DH, BR, QST, CAUSAL, BF16, SPARSE>;
   constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
   static bool attr_set = false;
@@ -690,6 +704,8 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.err = pr.err;
   p.with_dq = a.deterministic ? 0 : 1;
   p.mask = a.mask;
+  p.dks = a.dks;
+  p.dvs = a.dvs;
   const int n_kv_tiles = (pr.Nk + kBC - 1) / kBC;
   if (g_num_sms == 0) {
     int dev = 0;
@@ -719,8 +735,8 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   const unsigned blocks = static_cast<unsigned>(
       std::min<size_t>((n8 + 255) / 256, static_cast<size_t>(g_num_sms) * 8));
   slot = timing_begin(FA_KERNEL_BWD_CONVERT, stream);
-  bwd_convert_dq<BF16><<<blocks, 256, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8,
-                                                   pr.scale);
+  bwd_convert_dq<D, BF16><<<blocks, 256, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8,
+                                                      pr.scale, pr.H, pr.Nq, a.dqs);
   timing_end(slot, stream);
   return cudaGetLastError();
 }

@@ -103,6 +103,8 @@ struct FwdParams {
   float* lse_part;
   float scale_log2;   // scale * log2(e)
   BlockMask mask;     // block-sparse: only kept blocks' key tiles (splits == 1, no packing)
+  long long o_sb, o_sh, o_sn;   // element strides of o over (batch, head, row) in this
+                                // kernel's view (packed rows: row stride and group stride)
   unsigned int* err;
 };
 
@@ -203,7 +205,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop; one elected lane issues the copies.
-    const int zq = b * p.H + h, zkv = b * p.Hkv + kh;
     if (elect_one()) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -211,7 +212,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
       #pragma unroll
       for (int c = 0; c < L::kNch; ++c)
-        tma_load_3d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, qt * kBR, zq);
+        tma_load_4d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, qt * kBR, h, b);
     }
     __syncwarp();
     int k_issued = 0, v_issued = 0;
@@ -222,8 +223,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
-                      bar(L::kKFull + s), c * 64, key_tile(j) * BC, zkv);
+          tma_load_4d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
+                      bar(L::kKFull + s), c * 64, key_tile(j) * BC, kh, b);
       }
       __syncwarp();
       ++k_issued;
@@ -233,8 +234,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
-          tma_load_3d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
-                      bar(L::kVFull + sv), c * 64, key_tile(j) * BC, zkv);
+          tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
+                      bar(L::kVFull + sv), c * 64, key_tile(j) * BC, kh, b);
       }
       __syncwarp();
       ++v_issued;
@@ -429,7 +430,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       // no row of this tile sees any key: O = 0, L = -inf
       if (row < p.Nq) {
         const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + r * D);
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
+                                               h * p.o_sh + row * p.o_sn);
         #pragma unroll
         for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
         p.lse[r] = -INFINITY;
@@ -468,8 +470,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         if (in_range) p.lse_part[r] = lse;
       } else {
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                             (row_base + (in_range ? row : 0)) * D);
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
+                                             h * p.o_sh + (in_range ? row : 0) * p.o_sn);
       #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o1[32];
@@ -507,14 +509,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 fwd_combine_splits(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                   uint16_t* __restrict__ o, float* __restrict__ lse, size_t rows, int splits) {
+                   uint16_t* __restrict__ o, float* __restrict__ lse, size_t rows, int splits,
+                   int H, int Nq, Strides os) {
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   constexpr int kPer = D / 32;
   float m = -INFINITY;
   for (int sp = 0; sp < splits; ++sp) m = fmaxf(m, lse_part[sp * rows + row]);
-  uint16_t* orow = o + row * D + lane * kPer;
+  // row = (b * H + h) * Nq + i of the output view
+  const size_t bh = row / Nq;
+  const long long i = static_cast<long long>(row - bh * Nq);
+  const long long hh = static_cast<long long>(bh % H), bb = static_cast<long long>(bh / H);
+  uint16_t* orow = o + bb * os.b + hh * os.h + i * os.n + lane * kPer;
   if (m == -INFINITY) {
     #pragma unroll
     for (int i = 0; i < kPer; i += 2) *reinterpret_cast<uint32_t*>(orow + i) = 0u;
@@ -546,8 +553,8 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   using L = FwdLayout<D, BC, KST, VST>;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tk, a.k, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
-  if ((e = make_tmap_3d(&tv, a.v, D, pr.Nk, pr.B * pr.Hkv, 64, BC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tk, a.k, D, pr.Nk, pr.Hkv, pr.B, a.ks, 64, BC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tv, a.v, D, pr.Nk, pr.Hkv, pr.B, a.vs, 64, BC)) != cudaSuccess) return e;
   auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST, SPARSE>;
   // without a block mask the list is never touched and not allocated
   constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
@@ -583,7 +590,18 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
     p.tiles_per_split = (n_kv_tiles + a.splits - 1) / a.splits;
     p.splits = (n_kv_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
   }
-  if ((e = make_tmap_3d(&tq, a.q, D, p.Nq, pr.B * p.H, 64, kBR)) != cudaSuccess) return e;
+  // Packed: row r = g * Nq + i of KV group kh is query head kh * G + g, row i;
+  // the caller packs only when those rows are evenly spaced (Nq == 1, or
+  // head stride == Nq * row stride), so the group is one strided view.
+  Strides qv = a.qs, ov = a.os;
+  if (a.pack) {
+    qv = {a.qs.b, G * a.qs.h, pr.Nq == 1 ? a.qs.h : a.qs.n};
+    ov = {a.os.b, G * a.os.h, pr.Nq == 1 ? a.os.h : a.os.n};
+  }
+  p.o_sb = ov.b;
+  p.o_sh = ov.h;
+  p.o_sn = ov.n;
+  if ((e = make_tmap_4d(&tq, a.q, D, p.Nq, p.H, pr.B, qv, 64, kBR)) != cudaSuccess) return e;
   dim3 grid(p.num_q_tiles * p.splits, p.H, pr.B);
   const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
@@ -592,7 +610,8 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   if (!SPARSE && p.splits > 1) {
     const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
     fwd_combine_splits<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        a.o_part, a.lse_part, static_cast<uint16_t*>(a.o), a.lse, rows, p.splits);
+        a.o_part, a.lse_part, static_cast<uint16_t*>(a.o), a.lse, rows, p.splits, pr.H, pr.Nq,
+        a.os);
     e = cudaGetLastError();
   }
   return e;

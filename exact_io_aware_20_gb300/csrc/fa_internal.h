@@ -18,6 +18,16 @@ struct Problem {
   unsigned int* err;   // device error word (bit 0: a bounded wait expired)
 };
 
+// Element strides of a 16-bit [batch][heads][rows][d] view whose d elements
+// are contiguous (the layout of every q, k, v, o and gradient tensor; the
+// contiguous case is {heads * rows * d, rows * d, d}).
+struct Strides {
+  long long b = 0, h = 0, n = 0;
+};
+inline Strides contiguous_strides(int heads, int rows, int d) {
+  return {static_cast<long long>(heads) * rows * d, static_cast<long long>(rows) * d, d};
+}
+
 // Block mask of block-sparse attention: bytes [heads][nbr][nbc], block
 // (i, j) covering query rows [128 i, 128 i + 128) and keys [128 j, 128 j +
 // 128); nonzero = the block is computed.  heads is 1 (one mask for every
@@ -50,6 +60,7 @@ struct FwdArgs {
   float* o_part = nullptr;   // [splits][B*H*Nq][d] fp32
   float* lse_part = nullptr; // [splits][B*H*Nq] fp32
   BlockMask mask;            // block-sparse (needs pack == 0, splits == 1)
+  Strides qs, ks, vs, os;    // element strides of q, k, v, o (set by the caller)
 };
 
 // Key tiles of the forward kernel (for choosing a split count).
@@ -69,12 +80,17 @@ struct BwdArgs {
   float* dq_acc;   // [B, H, Nq, d] fp32 scratch (unused when deterministic)
   int deterministic;   // dQ from the query-outer kernel, without atomics
   BlockMask mask = {};  // block-sparse
+  // element strides of q, k, v, o, dout, dq, dk, dv (set by the caller); the
+  // scratch (delta, dq_acc) and lse are always contiguous
+  Strides qs = {}, ks = {}, vs = {}, os = {}, dos = {}, dqs = {}, dks = {}, dvs = {};
 };
 
-// Encode a 3-D tiled tensor map over a [outer, rows, cols] 16-bit tensor
-// (cols contiguous) with a box of box_cols x box_rows and 128-byte swizzle.
-cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, int cols, int rows, int outer,
-                         int box_cols, int box_rows);
+// Encode a 4-D tiled tensor map over a 16-bit [batch][heads][rows][cols]
+// view (cols contiguous, element strides st) with a box of box_cols x
+// box_rows of one (head, batch) and 128-byte swizzle; TMA coordinates are
+// (col, row, head, batch).
+cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int cols, int rows, int heads,
+                         int batch, const Strides& st, int box_cols, int box_rows);
 
 // Diagnostics timing (see fa_timing_enable in fa.h): returns a slot to pass
 // to timing_end, or -1 when timing is off or out of event pairs.

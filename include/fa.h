@@ -177,6 +177,37 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    int d, int causal, float scale, int dtype, fa_stream_t stream);
 
 /*
+ * Strided views (no counterpart on the pages: they let framework tensors,
+ * e.g. [B][N][H][d] or a packed [B][N][3][H][d] QKV buffer, be used without
+ * a copy).  Each of q, k, v, o (and dout, dq, dk, dv) is described as the
+ * logical [B][heads][N][d] view with the d elements contiguous and element
+ * strides
+ *     element (b, h, n, c) at  base + b * batch + h * head + n * row + c.
+ * Every stride must be a positive multiple of 8 elements (16 bytes) below
+ * 2^39; base pointers 16-byte aligned.  The contiguous layout of fa_fwd is
+ * {H * N * d, N * d, d}; [B][N][H][d] is {N * H * d, d, H * d}.  lse stays
+ * contiguous [B][H][Nq] fp32.  Output views must not overlap themselves or
+ * the inputs.  The results are those of fa_fwd_qk / fa_bwd_qk on the same
+ * values (the same bits: only the addressing differs).
+ */
+typedef struct fa_strides {
+  long long batch, head, row; /* element strides */
+} fa_strides;
+
+/* strides[4]: q, k, v, o.  Otherwise as fa_fwd_qk. */
+int fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,
+                   const fa_strides *strides, fa_stream_t stream);
+
+/* strides[8]: q, k, v, o, dout, dq, dk, dv.  Otherwise as fa_bwd_qk (the
+ * workspace is fa_bwd_workspace_size(B, H, Hkv, Nq, d) bytes). */
+int fa_bwd_strided(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int Nq,
+                   int Nk, int d, int causal, float scale, int dtype, const fa_strides *strides,
+                   int deterministic, void *workspace, size_t workspace_bytes,
+                   fa_stream_t stream);
+
+/*
  * Block-sparse attention ("FlashAttention: Fast and Memory-Efficient Exact
  * Attention with IO-Awareness", abstract and "Key contributions": block-sparse
  * FlashAttention computes attention only on the nonzero blocks of a given

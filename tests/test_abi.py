@@ -146,3 +146,24 @@ def test_bwd_blocksparse_rejects(lib, case, expect):
                                 a["Hkv"], a["Nq"], a["Nk"], a["d"], 1, 0.1, binding.FA_F16,
                                 a["mask"], a["mask_heads"], a["det"], a["ws"], 1 << 40, None)
     assert st == expect
+
+
+def _fa_strides(vals):
+    arr = (binding.FaStrides * len(vals))()
+    for i, v in enumerate(vals):
+        arr[i] = binding.FaStrides(*v)
+    return arr
+
+
+@pytest.mark.parametrize("bad", [None, (0, 64, 8192), (8192, 64, 12), (-64, 64, 8192),
+                                 (1 << 40, 64, 8192)])
+def test_strided_rejects(lib, bad):
+    good = (4 * 256 * 64, 256 * 64, 64)
+    fwd = None if bad is None else _fa_strides([good, good, bad, good])
+    st = lib.fa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 4, 256, 256, 64, 0, 0.1,
+                            binding.FA_BF16, fwd, None)
+    assert st == binding.FA_ERR_INVALID_ARG
+    bwd = None if bad is None else _fa_strides([good] * 7 + [bad])
+    st = lib.fa_bwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 4, 256,
+                            256, 64, 0, 0.1, binding.FA_BF16, bwd, 0, FAKE, 1 << 30, None)
+    assert st == binding.FA_ERR_INVALID_ARG

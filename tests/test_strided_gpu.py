@@ -1,0 +1,99 @@
+"""Strided views through fa_fwd_strided / fa_bwd_strided: [B, N, H, d]
+tensors, a packed [B, N, 3, H, d] QKV buffer and short queries.  Only the
+addressing differs from the contiguous entry points, so where both take the
+same tiles the results must be the same bits; the rest is checked against the
+fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_io_aware_20_gb300 import binding
+from exact_io_aware_20_gb300.inputs import Workload, make_inputs
+from parity import check_forward, check_grads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _bnhd(t):
+    """The same values in a [B, N, H, d] buffer, returned as its [B, H, N, d] view."""
+    return t.transpose(1, 2).contiguous().transpose(1, 2)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(300, 300), (128, 640), (1000, 333)])
+def test_bnhd_equals_contiguous_bitwise(d, causal, Nq, Nk):
+    w = Workload("bnhd", 2, 4, 2, Nq, d, "bf16", causal, 5 + d + Nq + 7 * Nk)
+    q, k, v, do = (t.to(DEV) for t in make_inputs(w, Nk=Nk))
+    o_c, l_c = binding.forward(q, k, v, causal, w.scale)
+    g_c = binding.backward(q, k, v, o_c, l_c, do, causal, w.scale, deterministic=True)
+    qs, ks, vs, dos = (_bnhd(t) for t in (q, k, v, do))
+    o_s, l_s = binding.forward_strided(qs, ks, vs, causal, w.scale, out=_bnhd(torch.empty_like(q)))
+    g_s = binding.backward_strided(qs, ks, vs, o_s, l_s, dos, causal, w.scale,
+                                   dq=_bnhd(torch.empty_like(q)), dk=_bnhd(torch.empty_like(k)),
+                                   dv=_bnhd(torch.empty_like(v)), deterministic=True)
+    g_a = binding.backward_strided(qs, ks, vs, o_s, l_s, dos, causal, w.scale)
+    binding.device_status()
+    assert o_s.stride() == qs.stride()
+    assert torch.equal(o_s, o_c) and torch.equal(l_s, l_c)
+    for a, b in zip(g_s, g_c):
+        assert torch.equal(a, b)
+    # atomic dQ path: dK, dV in a fixed order (same bits), dQ against the oracle
+    assert torch.equal(g_a[1], g_c[1]) and torch.equal(g_a[2], g_c[2])
+    if d == 128 and causal:
+        dq_r, dk_r, dv_r = oracle.backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), causal, w.scale)
+        check_grads([("dq", g_a[0].cpu(), dq_r), ("dk", g_a[1].cpu(), dk_r),
+                     ("dv", g_a[2].cpu(), dv_r)], f"strided bnhd d{d} {Nq}x{Nk}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_qkv_buffer(causal):
+    """q, k, v as slices of one [B, N, 3, H, d] tensor (a fused QKV projection)."""
+    B, N, H, d = 2, 700, 8, 128
+    g = torch.Generator().manual_seed(31)
+    qkv = torch.randn(B, N, 3, H, d, generator=g).to(torch.bfloat16).to(DEV)
+    do = torch.randn(B, N, H, d, generator=g).to(torch.bfloat16).to(DEV)
+    q, k, v = (qkv[:, :, i].transpose(1, 2) for i in range(3))
+    dov = do.transpose(1, 2)
+    scale = d ** -0.5
+    o, lse = binding.forward_strided(q, k, v, causal, scale,
+                                     out=torch.empty(B, N, H, d, dtype=q.dtype,
+                                                     device=DEV).transpose(1, 2))
+    dqkv = torch.empty_like(qkv)
+    dq, dk, dv = (dqkv[:, :, i].transpose(1, 2) for i in range(3))
+    binding.backward_strided(q, k, v, o, lse, dov, causal, scale, dq=dq, dk=dk, dv=dv)
+    binding.device_status()
+    qc, kc, vc, doc = (t.contiguous().cpu() for t in (q, k, v, dov))
+    o_r, l_r = oracle.forward(qc, kc, vc, causal, scale)
+    check_forward(o.cpu(), lse.cpu().double().numpy(), o_r, l_r, f"qkv fwd c{causal}")
+    dq_r, dk_r, dv_r = oracle.backward(qc, kc, vc, doc, causal, scale)
+    check_grads([("dq", dq.cpu(), dq_r), ("dk", dk.cpu(), dk_r), ("dv", dv.cpu(), dv_r)],
+                f"qkv bwd c{causal}")
+
+
+@pytest.mark.parametrize("Nq", [1, 4, 64])
+def test_short_queries_bnhd(Nq):
+    """Decode-like shapes in [B, N, H, d]: Nq = 1 keeps the GQA row packing
+    (the group's heads are evenly spaced), Nq > 1 runs unpacked."""
+    w = Workload("dec", 2, 8, 2, Nq, 128, "bf16", True, 40 + Nq)
+    q, k, v, _ = make_inputs(w, Nk=2000)
+    qs, ks, vs = (_bnhd(t.to(DEV)) for t in (q, k, v))
+    o, lse = binding.forward_strided(qs, ks, vs, True, w.scale)
+    binding.device_status()
+    o_r, l_r = oracle.forward(q, k, v, True, w.scale)
+    check_forward(o.cpu(), lse.cpu().double().numpy(), o_r, l_r, f"bnhd decode Nq{Nq}")
+
+
+def test_contiguous_strides_equal_fa_fwd_qk():
+    w = Workload("cs", 1, 4, 1, 513, 64, "f16", True, 3)
+    q, k, v, do = (t.to(DEV) for t in make_inputs(w, Nk=700))
+    o1, l1 = binding.forward(q, k, v, True, w.scale)
+    o2, l2 = binding.forward_strided(q, k, v, True, w.scale)
+    g1 = binding.backward(q, k, v, o1, l1, do, True, w.scale, deterministic=True)
+    g2 = binding.backward_strided(q, k, v, o1, l1, do, True, w.scale, deterministic=True)
+    binding.device_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
