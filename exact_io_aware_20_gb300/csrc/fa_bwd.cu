@@ -3,7 +3,7 @@
 
 namespace fa {
 
-int bwd_query_tile(int d) { return d == 64 ? 128 : 64; }
+int bwd_query_tile(int d) { return d == 256 ? 64 : 128; }
 
 int bwd_list_cap(int d) {
   switch (d) {

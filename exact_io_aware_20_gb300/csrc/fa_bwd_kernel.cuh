@@ -42,6 +42,8 @@
 //   computed by both), because dK + dV for all 256 columns would fill TMEM.
 #pragma once
 
+#include <type_traits>
+
 #include "block_list.cuh"
 #include "fa.h"
 #include "fa_internal.h"
@@ -162,21 +164,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   const int n_i = p.n_q_tiles - i0;
   int n_steps = p.G * n_i;
   constexpr bool sparse = SPARSE;
+  // Step order: query tiles from the last down to i0, the G heads of the
+  // group innermost.  CTAs of a group that run together then work on the
+  // same query tiles at the same time, so the dQ accumulator rows they add
+  // into (and the Q / dO tiles they load) stay in L2.
   if (sparse && warp == 2) {
-    // steps g * n_q_tiles + i of the blocks kept in this key tile's mask
-    // column, over the G heads of the group, query tiles i0 .. n_q_tiles-1
-    constexpr int kSub = kMaskBlock / BR;
-    const int nbr = p.mask.nbr;
-    const int cnt = compact_steps<kSub>(
-        p.G * nbr,
+    // the kept steps of that order: mask block (query block of tile i, this
+    // key tile) nonzero for head g's pattern
+    const int cnt = compact_steps<1>(
+        p.G * n_i,
         [&](int e) {
-          const int g = e / nbr, qb = e - g * nbr;
+          const int i = p.n_q_tiles - 1 - e / p.G, g = e % p.G;
           const int mh = p.mask.heads == 1 ? 0 : kh * p.G + g;
-          return p.mask.ptr[(static_cast<size_t>(mh) * nbr + qb) * p.mask.nbc + jt] != 0;
+          const int qb = i * BR / kMaskBlock;
+          return p.mask.ptr[(static_cast<size_t>(mh) * p.mask.nbr + qb) * p.mask.nbc + jt] != 0;
         },
-        [&](int e, int sub) {
-          const int g = e / nbr, i = (e - g * nbr) * kSub + sub;
-          return (i >= i0 && i < p.n_q_tiles) ? g * p.n_q_tiles + i : -1;
+        [&](int e, int) {
+          const int i = p.n_q_tiles - 1 - e / p.G, g = e % p.G;
+          return g * p.n_q_tiles + i;
         },
         step_list, L::kListCap);
     if (lane == 0) *list_count = min(cnt, L::kListCap);
@@ -189,8 +194,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       g = c / p.n_q_tiles;
       i = c - g * p.n_q_tiles;
     } else {
-      g = t / n_i;
-      i = i0 + t % n_i;
+      g = t % p.G;
+      i = p.n_q_tiles - 1 - t / p.G;
     }
     h = kh * p.G + g;
     q0 = i * BR;
@@ -584,6 +589,456 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 128: 128 query rows per step.
+//
+// On sm_103a an M = 128 tcgen05.mma of kind::f16 occupies the tensor pipe
+// for 64 cycles whenever N <= 128 (measured: N = 16, 64 and 128 all take 64
+// cycles, N = 256 takes 126), so with 64-row steps the products S^T, dP^T and
+// dQ^T (N = 64) run at half rate.  With 128-row steps every product has
+// N = 128.  TMEM then holds dV (128 columns), dK (128), S^T (128, P^T written
+// over it in 16 bits) and dP^T (128); dQ^T of a step is written into the dP^T
+// columns once the dS warps have read dP^T, and the next dP^T waits until the
+// dQ warps have read dQ^T out.  Issue order per step t:
+//   dV(t), S(t+1), dQ^T(t), dK(t), dP(t+1)
+// so the exponentials of step t+1 overlap dQ^T(t) and dK(t), and dP(t+1)
+// overlaps the dS of nothing but is ready before P(t+1) is done.
+// Warps: 0 TMA producer (K, V once; Q in two stages, dO in one), 1 MMA
+// issuer, 2..9 P / dS (a key row per thread; warps w and w + 4 share a TMEM
+// lane quarter and split the 128 query columns in halves), 10..13 dQ.
+
+constexpr int kB128Threads = 448;
+
+struct B128Layout {
+  static constexpr int kTile = 128 * 128 * 2;      // one 128 x 128 16-bit tile
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTile;
+  static constexpr int kQOff = 2 * kTile;          // two stages
+  static constexpr int kDOOff = 4 * kTile;         // one stage
+  static constexpr int kDSOff = 5 * kTile;         // dS^T [keys][q]
+  static constexpr int kLDOff = 6 * kTile;         // 8 warps x 2 bufs x {-L*log2e, -D} x 64
+  static constexpr int kBarOff = kLDOff + 8 * 2 * 2 * 64 * 4;
+  static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kDOFull = 5, kDOEmpty = 6,
+                       kSFull = 7, kDPFull = 8, kPFull = 9, kDSFull = 10, kDSEmpty = 11,
+                       kDQFull = 12, kDQEmpty = 13, kFinal = 14, kDrain = 15, kNumBars = 16;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kListCap = 8192;            // (head, query tile) steps under a mask
+  static constexpr int kListOff = kMiscOff + 16;
+  static constexpr int kBytes = kListOff + kListCap * 2;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr int kAllocDense = kListOff + 1024;   // without the list
+  static constexpr uint32_t kTdV = 0, kTdK = 128, kTS = 256, kTdP = 384, kTmemCols = 512;
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <bool CAUSAL, bool BF16, bool SPARSE>
+__global__ void __launch_bounds__(kB128Threads, 1)
+bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const BwdParams p) {
+  using L = B128Layout;
+  constexpr int D = 128, BR = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  int* list_count = reinterpret_cast<int*>(smem + L::kMiscOff + 8);
+  uint16_t* step_list = reinterpret_cast<uint16_t*>(smem + L::kListOff);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // dispatch orders as in bwd_kernel (one CTA per key tile: no d split)
+  int jt, kh, b;
+  if (p.heavy_first) {
+    jt = blockIdx.y;
+    kh = blockIdx.x % p.Hkv;
+    b = blockIdx.x / p.Hkv;
+  } else {
+    jt = blockIdx.x;
+    kh = blockIdx.y;
+    b = blockIdx.z;
+  }
+  const int kv0 = jt * kBC;
+  const int i0 = CAUSAL ? max(0, kv0 - p.off) / BR : 0;
+  const int n_i = p.n_q_tiles - i0;
+  int n_steps = p.G * n_i;
+  constexpr bool sparse = SPARSE;
+  // step order as in bwd_kernel: query tiles descending, heads innermost
+  if (sparse && warp == 2) {
+    const int cnt = compact_steps<1>(
+        p.G * n_i,
+        [&](int e) {
+          const int i = p.n_q_tiles - 1 - e / p.G, g = e % p.G;
+          const int mh = p.mask.heads == 1 ? 0 : kh * p.G + g;
+          return p.mask.ptr[(static_cast<size_t>(mh) * p.mask.nbr + i) * p.mask.nbc + jt] != 0;
+        },
+        [&](int e, int) {
+          const int i = p.n_q_tiles - 1 - e / p.G, g = e % p.G;
+          return g * p.n_q_tiles + i;
+        },
+        step_list, L::kListCap);
+    if (lane == 0) *list_count = min(cnt, L::kListCap);
+  }
+  auto step_hq = [&](int t, int& h, int& q0) {
+    int g, i;
+    if (sparse) {
+      const int c = step_list[t];
+      g = c / p.n_q_tiles;
+      i = c - g * p.n_q_tiles;
+    } else {
+      g = t % p.G;
+      i = p.n_q_tiles - 1 - t / p.G;
+    }
+    h = kh * p.G + g;
+    q0 = i * BR;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kKVFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kQFull + s), 1);
+      mbar_init(bar(L::kQEmpty + s), 1);
+    }
+    mbar_init(bar(L::kDOFull), 1);
+    mbar_init(bar(L::kDOEmpty), 1);
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kDPFull), 1);
+    mbar_init(bar(L::kPFull), 256);
+    mbar_init(bar(L::kDSFull), 256);
+    mbar_init(bar(L::kDSEmpty), 1);
+    mbar_init(bar(L::kDQFull), 1);
+    mbar_init(bar(L::kDQEmpty), 128);
+    mbar_init(bar(L::kFinal), 1);
+    mbar_init(bar(L::kDrain), 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (sparse) n_steps = *list_count;
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tdV = tmem + L::kTdV, tdK = tmem + L::kTdK, tS = tmem + L::kTS,
+                 tdP = tmem + L::kTdP;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kTile);
+      #pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(sbase + L::kKOff + c * (kBC * 128), &tm_k, bar(L::kKVFull), c * 64, kv0, kh, b);
+        tma_load_4d(sbase + L::kVOff + c * (kBC * 128), &tm_v, bar(L::kKVFull), c * 64, kv0, kh, b);
+      }
+    }
+    __syncwarp();
+    int q_issued = 0, do_issued = 0;
+    for (int t = 0; t < n_steps; ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !wait_uniform(bar(L::kQEmpty + s), ((t >> 1) + 1) & 1, abort)) break;
+      int h, q0;
+      step_hq(t, h, q0);
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kQFull + s), L::kTile);
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kQOff + s * L::kTile + c * (BR * 128), &tm_q, bar(L::kQFull + s),
+                      c * 64, q0, h, b);
+      }
+      __syncwarp();
+      ++q_issued;
+      if (t >= 1 && !wait_uniform(bar(L::kDOEmpty), (t - 1) & 1, abort)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kDOFull), L::kTile);
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kDOOff + c * (BR * 128), &tm_do, bar(L::kDOFull), c * 64, q0, h, b);
+      }
+      __syncwarp();
+      ++do_issued;
+    }
+    drain_wait(bar(L::kKVFull), 0);
+    for (int t = max(0, q_issued - 2); t < q_issued; ++t)
+      drain_wait(bar(L::kQFull + (t & 1)), (t >> 1) & 1);
+    if (do_issued > 0) drain_wait(bar(L::kDOFull), (do_issued - 1) & 1);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(kBC, BR, BF16 ? 1 : 0, 0, 0);    // S^T, dP^T
+    constexpr uint32_t kIdKV = idesc_f16(kBC, D, BF16 ? 1 : 0, 0, 1);    // dV, dK
+    constexpr uint32_t kIdQ = idesc_f16(D, BR, BF16 ? 1 : 0, 1, 1);      // dQ^T
+    const uint64_t k_kmaj = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
+    const uint64_t v_kmaj = smem_desc_sw128(sbase + L::kVOff, 16, 1024);
+    const uint64_t q_kmaj = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+    const uint64_t do_kmaj = smem_desc_sw128(sbase + L::kDOOff, 16, 1024);
+    const uint64_t ds_kmaj = smem_desc_sw128(sbase + L::kDSOff, 16, 1024);
+    const uint64_t q_mn = smem_desc_sw128(sbase + L::kQOff, BR * 128, 1024);
+    const uint64_t do_mn = smem_desc_sw128(sbase + L::kDOOff, BR * 128, 1024);
+    const uint64_t k_mn = smem_desc_sw128(sbase + L::kKOff, kBC * 128, 1024);
+    const uint64_t ds_mn = smem_desc_sw128(sbase + L::kDSOff, kBC * 128, 1024);
+    // S^T_t = K Q_t^T into the S columns
+    auto issue_s = [&](int t) -> bool {
+      if (!wait_uniform(bar(L::kQFull + (t & 1)), (t >> 1) & 1, abort)) return false;
+      tc_fence_after();
+      const uint32_t qs = (t & 1) * L::kTile;
+      #pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t c = kk >> 2, w = kk & 3;
+        mma_ss(tS, desc_add(k_kmaj, c * (kBC * 128) + w * 32),
+               desc_add(q_kmaj, qs + c * (BR * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kSFull));
+      return true;
+    };
+    // dP^T_t = V dO_t^T into the dP columns
+    auto issue_dp = [&](int t) -> bool {
+      if (!wait_uniform(bar(L::kDOFull), t & 1, abort)) return false;
+      tc_fence_after();
+      #pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t c = kk >> 2, w = kk & 3;
+        mma_ss(tdP, desc_add(v_kmaj, c * (kBC * 128) + w * 32),
+               desc_add(do_kmaj, c * (BR * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kDPFull));
+      return true;
+    };
+    bool ok = wait_uniform(bar(L::kKVFull), 0, abort);
+    if (ok && n_steps > 0) ok = issue_s(0) && issue_dp(0);
+    for (int t = 0; ok && t < n_steps; ++t) {
+      const uint32_t qs = (t & 1) * L::kTile;
+      // dV += P^T dO: P^T (16-bit) sits in the first 32 columns of each
+      // 64-column half of the S columns (one half per P / dS warp).
+      if (!wait_uniform(bar(L::kPFull), t & 1, abort)) break;
+      tc_fence_after();
+      #pragma unroll
+      for (int kk = 0; kk < BR / 16; ++kk)
+        mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(do_mn, kk * 2048), kIdKV,
+               (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar(L::kDOEmpty));      // dP_t and dV_t were dO_t's readers
+      if (t + 1 < n_steps && !issue_s(t + 1)) break;
+      if (!wait_uniform(bar(L::kDSFull), t & 1, abort)) break;
+      tc_fence_after();
+      if (p.with_dq) {
+        // dQ^T = K^T dS^T over the dP columns (their dP^T has been read)
+        #pragma unroll
+        for (int kk = 0; kk < kBC / 16; ++kk)
+          mma_ss(tdP, desc_add(k_mn, kk * 2048), desc_add(ds_mn, kk * 2048), kIdQ,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(bar(L::kDQFull));
+      }
+      // dK += dS^T Q
+      #pragma unroll
+      for (int kk = 0; kk < BR / 16; ++kk)
+        mma_ss(tdK, desc_add(ds_kmaj, (kk >> 2) * (kBC * 128) + (kk & 3) * 32),
+               desc_add(q_mn, qs + kk * 2048), kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar(L::kQEmpty + (t & 1)));
+      mma_commit(bar(L::kDSEmpty));
+      if (t + 1 < n_steps) {
+        if (p.with_dq && !wait_uniform(bar(L::kDQEmpty), t & 1, abort)) break;
+        if (!issue_dp(t + 1)) break;
+      }
+    }
+    mma_commit(bar(L::kFinal));
+    mma_commit(bar(L::kDrain));
+    drain_wait(bar(L::kDrain), 0);
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ P / dS warps
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;            // query columns [64 half, 64 half + 64)
+    const int r = quarter * 32 + lane;           // key row within the tile
+    const int kv = kv0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float* ld_base = reinterpret_cast<float*>(smem + L::kLDOff) + (warp - 2) * 2 * 2 * 64;
+    float rl[2], rd[2];
+    auto load_ld = [&](int t) {
+      int h, q0;
+      step_hq(t, h, q0);
+      const size_t base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
+      #pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = q0 + 64 * half + lane + 32 * u;
+        rl[u] = q < p.Nq ? -p.lse[base + q] * kLog2e : -INFINITY;
+        rd[u] = q < p.Nq ? -p.delta[base + q] : 0.f;
+      }
+    };
+    auto store_ld = [&](int t) {
+      float* dst = ld_base + (t & 1) * 128;
+      #pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        dst[lane + 32 * u] = rl[u];
+        dst[64 + lane + 32 * u] = rd[u];
+      }
+    };
+    if (n_steps > 0) {
+      load_ld(0);
+      store_ld(0);
+    }
+    __syncwarp();
+    bool ok = true;
+    for (int t = 0; t < n_steps; ++t) {
+      int h_t, q0;
+      step_hq(t, h_t, q0);
+      (void)h_t;
+      const float* sL = ld_base + (t & 1) * 128;   // -L * log2(e) of this half's columns
+      const float* sD = sL + 64;                     // -D
+      if (t + 1 < n_steps) load_ld(t + 1);
+      if (!wait_uniform(bar(L::kSFull), t & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      const bool kv_out = kv >= p.Nk;
+      const bool diag = CAUSAL && (q0 + p.off < kv0 + kBC);
+      const bool masked = __any_sync(0xffffffffu, kv_out || diag);
+      const f2 cs = {p.scale_log2, p.scale_log2};
+      const int qc0 = q0 + 64 * half;              // first query of this half
+      float P[64];
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t sr[32];
+        tmem_ld32(tS + lane_off + 64 * half + c0, sr);
+        tmem_ld_wait();
+        reg_fence(sr);
+        #pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs,
+                               f2{sL[c0 + c], sL[c0 + c + 1]});
+          P[c0 + c] = ex2_approx(arg.x);
+          P[c0 + c + 1] = ex2_approx(arg.y);
+        }
+        if (masked) {
+          #pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (kv_out || (diag && kv > qc0 + c0 + c + p.off)) P[c0 + c] = 0.f;
+        }
+        uint32_t pk[16];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(P[c0 + 2 * c], P[c0 + 2 * c + 1]);
+        // P^T over the first 32 columns of this half, already read
+        tmem_st16(tS + lane_off + 64 * half + c0 / 2, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull));
+      // dS^T = P^T o (dP^T - D) into the swizzled dS^T tile (chunk = half)
+      if (!wait_uniform(bar(L::kDPFull), t & 1, abort)) { ok = false; break; }
+      if (t > 0 && !wait_uniform(bar(L::kDSEmpty), (t - 1) & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      // 16 columns at a time: P (64 values) stays live across the loop
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        uint32_t dr[16];
+        tmem_ld16(tdP + lane_off + 64 * half + c0, dr);
+        tmem_ld_wait();
+        reg_fence(dr);
+        uint32_t w[8];
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const f2 diff = fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])},
+                                f2{sD[c0 + 2 * c], sD[c0 + 2 * c + 1]});
+          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]}, diff);
+          w[c] = pack2<BF16>(ds.x, ds.y);
+        }
+        #pragma unroll
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int u = c0 / 8 + u2;
+          uint4* dst = reinterpret_cast<uint4*>(smem + L::kDSOff + half * (kBC * 128) + r * 128 +
+                                                ((u ^ (r & 7)) * 16));
+          *dst = make_uint4(w[4 * u2], w[4 * u2 + 1], w[4 * u2 + 2], w[4 * u2 + 3]);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::kDSFull));
+      if (t + 1 < n_steps) {
+        store_ld(t + 1);
+        __syncwarp();
+      }
+    }
+    // ------------------------------------------------------------ dK, dV epilogue
+    if (ok && wait_uniform(bar(L::kFinal), 0, abort)) {
+      tc_fence_after();
+      const bool in_range = kv < p.Nk;
+      const long long kvr = in_range ? kv : 0;
+      uint4* dv_row = reinterpret_cast<uint4*>(p.dv + b * p.dvs.b + kh * p.dvs.h + kvr * p.dvs.n +
+                                               64 * half);
+      uint4* dk_row = reinterpret_cast<uint4*>(p.dk + b * p.dks.b + kh * p.dks.h + kvr * p.dks.n +
+                                               64 * half);
+      const uint32_t live = n_steps > 0 ? 0xffffffffu : 0u;
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t a[32], k2[32];
+        tmem_ld32(tdV + lane_off + 64 * half + c0, a);
+        tmem_ld32(tdK + lane_off + 64 * half + c0, k2);
+        tmem_ld_wait();
+        reg_fence(a);
+        reg_fence(k2);
+        uint32_t wv[16], wk[16];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          wv[c] = pack2<BF16>(__uint_as_float(a[2 * c] & live), __uint_as_float(a[2 * c + 1] & live));
+          wk[c] = pack2<BF16>(__uint_as_float(k2[2 * c] & live) * p.scale,
+                              __uint_as_float(k2[2 * c + 1] & live) * p.scale);
+        }
+        if (in_range) {
+          #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            dv_row[c0 / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+            dk_row[c0 / 8 + i] = make_uint4(wk[4 * i], wk[4 * i + 1], wk[4 * i + 2], wk[4 * i + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warps
+    // lane r = column r of d; dQ^T row r holds dQ[q0 + c][r] for the 128 c
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int t = 0; ok && p.with_dq && t < n_steps; ++t) {
+      int h, q0;
+      step_hq(t, h, q0);
+      if (!wait_uniform(bar(L::kDQFull), t & 1, abort)) break;
+      tc_fence_after();
+      float* base = p.dq_acc + ((static_cast<size_t>(b) * p.H + h) * p.Nq + q0) * D + r;
+      const int n_valid = min(BR, p.Nq - q0);
+      #pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[16];
+        tmem_ld16(tdP + lane_off + 16 * c, v);
+        tmem_ld_wait();
+        reg_fence(v);
+        if (c == 7) {
+          // all of dQ^T_t is in registers: dP_{t+1} may overwrite it
+          tc_fence_before();
+          mbar_arrive(bar(L::kDQEmpty));
+        }
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (16 * c + i < n_valid)
+            atomicAdd(base + static_cast<size_t>(16 * c + i) * D, __uint_as_float(v[i]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
 // Element offset of row (b * H + h) * N + i of a strided [B][H][N][d] view.
 __device__ __forceinline__ long long view_offset(size_t row, int H, int N, const Strides& s) {
   const size_t bh = row / N;
@@ -659,9 +1114,11 @@ bwd_convert_dq(const float* __restrict__ acc, uint16_t* __restrict__ dq, size_t 
 
 int g_num_sms = 0;
 
-template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16, bool SPARSE>
+// WIDE: the d = 128 kernel with 128-row steps (bwd128_kernel).
+template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16, bool SPARSE, bool WIDE = false>
 cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D, DH, BR, QST>;
+  using L = std::conditional_t<WIDE, B128Layout, BwdLayout<D, DH, BR, QST>>;
+  static_assert(!WIDE || (D == 128 && DH == 128 && BR == 128), "wide kernel shape");
   cudaError_t e;
   const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
   // 1. preprocess
@@ -677,7 +1134,13 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   if ((e = make_tmap_4d(&tdo, a.dout, D, pr.Nq, pr.H, pr.B, a.dos, 64, BR)) != cudaSuccess) return e;
   if ((e = make_tmap_4d(&tk, a.k, D, pr.Nk, pr.Hkv, pr.B, a.ks, 64, kBC)) != cudaSuccess) return e;
   if ((e = make_tmap_4d(&tv, a.v, D, pr.Nk, pr.Hkv, pr.B, a.vs, 64, kBC)) != cudaSuccess) return e;
-  auto kern = bwd_kernel<D, DH, BR, QST, CAUSAL, BF16, SPARSE>;
+  auto kern = [] {
+    if constexpr (WIDE)
+      return bwd128_kernel<CAUSAL, BF16, SPARSE>;
+    else
+      return bwd_kernel<D, DH, BR, QST, CAUSAL, BF16, SPARSE>;
+  }();
+  constexpr int kThreadsMain = WIDE ? kB128Threads : kBwdThreads;
   constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
   static bool attr_set = false;
   if (!attr_set) {
@@ -726,7 +1189,7 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   dim3 grid = p.heavy_first ? dim3((D / DH) * pr.Hkv * pr.B, n_kv_tiles, 1)
                             : dim3(n_kv_tiles * (D / DH), pr.Hkv, pr.B);
   slot = timing_begin(FA_KERNEL_BWD_MAIN, stream);
-  kern<<<grid, kBwdThreads, kSmem, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, kThreadsMain, kSmem, stream>>>(tq, tk, tv, tdo, p);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 3. dQ: the query-outer kernel (deterministic) or the accumulator's conversion
@@ -741,26 +1204,27 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   return cudaGetLastError();
 }
 
-template <int D, int DH, int BR, int QST, bool SPARSE>
+template <int D, int DH, int BR, int QST, bool SPARSE, bool WIDE = false>
 cudaError_t dispatch_flags(const Problem& pr, const BwdArgs& a, cudaStream_t s) {
   if (pr.causal)
-    return pr.bf16 ? launch_variant<D, DH, BR, QST, true, true, SPARSE>(pr, a, s)
-                   : launch_variant<D, DH, BR, QST, true, false, SPARSE>(pr, a, s);
-  return pr.bf16 ? launch_variant<D, DH, BR, QST, false, true, SPARSE>(pr, a, s)
-                 : launch_variant<D, DH, BR, QST, false, false, SPARSE>(pr, a, s);
+    return pr.bf16 ? launch_variant<D, DH, BR, QST, true, true, SPARSE, WIDE>(pr, a, s)
+                   : launch_variant<D, DH, BR, QST, true, false, SPARSE, WIDE>(pr, a, s);
+  return pr.bf16 ? launch_variant<D, DH, BR, QST, false, true, SPARSE, WIDE>(pr, a, s)
+                 : launch_variant<D, DH, BR, QST, false, false, SPARSE, WIDE>(pr, a, s);
 }
 
 // Tile configuration per head dimension: output half DH, query rows per step
 // BR, Q / dO ring stages.
+// d = 128 runs bwd128_kernel (128 query rows per step, two Q stages).
 using Cfg64 = BwdLayout<64, 64, 128, 3>;
-using Cfg128 = BwdLayout<128, 128, 64, 3>;
+using Cfg128 = B128Layout;
 using Cfg256 = BwdLayout<256, 128, 64, 1>;
 
 template <bool SPARSE>
 cudaError_t launch_bwd_for(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
   switch (pr.d) {
     case 64: return dispatch_flags<64, 64, 128, 3, SPARSE>(pr, a, stream);
-    case 128: return dispatch_flags<128, 128, 64, 3, SPARSE>(pr, a, stream);
+    case 128: return dispatch_flags<128, 128, 128, 2, SPARSE, true>(pr, a, stream);
     case 256: return dispatch_flags<256, 128, 64, 1, SPARSE>(pr, a, stream);
     default: return cudaErrorInvalidValue;
   }

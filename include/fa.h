@@ -227,9 +227,9 @@ int fa_bwd_strided(const void *q, const void *k, const void *v, const void *o, c
  * backward must get the forward's mask.  Limits (FA_ERR_INVALID_ARG beyond
  * them, for the per-CTA work lists): ceil(Nk / 128) <= 8192 for the forward
  * at d <= 128 (ceil(Nk / 64) <= 8192 at d = 256); for the backward,
- * (H / Hkv) * ceil(Nq / 64) <= 8192 (d = 128), (H / Hkv) * ceil(Nq / 128) <=
- * 8192 (d = 64), (H / Hkv) * ceil(Nq / 64) <= 4096 (d = 256), and with
- * deterministic = 1 also ceil(Nk / 64) <= 8192.
+ * (H / Hkv) * ceil(Nq / 128) <= 8192 (d = 64 and 128), (H / Hkv) *
+ * ceil(Nq / 64) <= 4096 (d = 256), and with deterministic = 1 also
+ * ceil(Nk / 64) <= 8192.
  */
 int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                        int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, int dtype,

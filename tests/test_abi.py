@@ -133,8 +133,8 @@ def test_fwd_blocksparse_rejects(lib, case, expect):
     (dict(mask=None), binding.FA_ERR_INVALID_ARG),
     (dict(mask_heads=2), binding.FA_ERR_INVALID_ARG),
     (dict(det=2), binding.FA_ERR_INVALID_ARG),
-    # (H / Hkv) * ceil(Nq / 64) above the d = 128 step list (8192)
-    (dict(H=8, Hkv=2, Nq=64 * 2049), binding.FA_ERR_INVALID_ARG),
+    # (H / Hkv) * ceil(Nq / 128) above the d = 128 step list (8192)
+    (dict(H=8, Hkv=2, Nq=128 * 2049), binding.FA_ERR_INVALID_ARG),
     (dict(d=256, H=4, Hkv=1, Nq=64 * 1025), binding.FA_ERR_INVALID_ARG),   # 4096 at d = 256
     (dict(det=1, Nk=64 * 8193), binding.FA_ERR_INVALID_ARG),   # dQ kernel key-tile list
     (dict(ws=None), binding.FA_ERR_WORKSPACE),
