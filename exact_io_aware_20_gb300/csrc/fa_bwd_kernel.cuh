@@ -1002,29 +1002,30 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    bool ok = true;
-    for (int t = 0; ok && p.with_dq && t < n_steps; ++t) {
+    for (int t = 0; p.with_dq && t < n_steps; ++t) {
       int h, q0;
       step_hq(t, h, q0);
       if (!wait_uniform(bar(L::kDQFull), t & 1, abort)) break;
       tc_fence_after();
       float* base = p.dq_acc + ((static_cast<size_t>(b) * p.H + h) * p.Nq + q0) * D + r;
       const int n_valid = min(BR, p.Nq - q0);
-      #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tdP + lane_off + 16 * c, v);
+      // two halves of 64 columns (128 values would not fit the register
+      // budget); DQEmpty once both are in registers
+      #pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t v[64];
+        tmem_ld32(tdP + lane_off + 64 * part, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tdP + lane_off + 64 * part + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_ld_wait();
         reg_fence(v);
-        if (c == 7) {
-          // all of dQ^T_t is in registers: dP_{t+1} may overwrite it
+        if (part == 1) {
           tc_fence_before();
           mbar_arrive(bar(L::kDQEmpty));
         }
         #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (16 * c + i < n_valid)
-            atomicAdd(base + static_cast<size_t>(16 * c + i) * D, __uint_as_float(v[i]));
+        for (int c = 0; c < 64; ++c)
+          if (64 * part + c < n_valid)
+            atomicAdd(base + static_cast<size_t>(64 * part + c) * D, __uint_as_float(v[c]));
       }
     }
   }
