@@ -503,6 +503,410 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 128, two query tiles per CTA (long queries without the causal mask).
+//
+// With one tile per CTA the tensor pipe idles while the softmax of tile j
+// runs (P V_j needs P_j) and the softmax warps idle while the products run.
+// Here a CTA holds query tiles A and B (rows [256 t, 256 t + 128) and
+// [256 t + 128, 256 t + 256)) with one softmax warpgroup each; every key
+// tile is loaded once for both, and the MMA warp interleaves the tiles:
+//   P V_A(j), S_A(j+1), P V_B(j), S_B(j+1), ...
+// so while one warpgroup exponentiates, the pipe works for the other.
+// TMEM: S_A, S_B, O_A, O_B (128 columns each; P written over S in 16 bits).
+// The row sums are formed on the ALU (no room for the ones columns).
+// Warps: 0 TMA producer, 1 MMA issuer, 2..5 softmax tile A, 6..9 tile B.
+constexpr int kFwd2Threads = 320;
+
+struct Fwd2Layout {
+  static constexpr int kTile = 128 * 128 * 2;   // one 128 x 128 16-bit tile (32 KB)
+  static constexpr int kQOff = 0;               // Q_A, Q_B
+  static constexpr int kKOff = 2 * kTile;       // two stages
+  static constexpr int kVOff = 4 * kTile;       // two stages
+  static constexpr int kBarOff = 6 * kTile;
+  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7,
+                       kSFull = 9, kPFull = 11, kODone = 13, kDrain = 15, kNumBars = 16;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr uint32_t kTS = 0, kTO = 256, kTmemCols = 512;
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kFwd2Threads, 1)
+fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = Fwd2Layout;
+  constexpr int D = 128, BC = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int xt = static_cast<int>(blockIdx.x);
+  const int qt = CAUSAL ? (p.num_q_tiles - 1 - xt) : xt;   // 256-row block, longest first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kh = h / p.G;
+  // key tiles of each query tile (0 if the tile holds no query row, or if
+  // under the mask no row of it sees a key)
+  int n_kv[2];
+  #pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int first = qt * 256 + 128 * u;
+    n_kv[u] = (p.Nk + BC - 1) / BC;
+    if (first >= p.Nq) {
+      n_kv[u] = 0;
+    } else if (CAUSAL) {
+      const int last_key = min(first + 128, p.Nq) - 1 + p.off;
+      n_kv[u] = last_key < 0 ? 0 : min(n_kv[u], last_key / BC + 1);
+    }
+  }
+  const int n_max = max(n_kv[0], n_kv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+      mbar_init(bar(L::kSFull + s), 1);
+      mbar_init(bar(L::kPFull + s), 128);
+      mbar_init(bar(L::kODone + s), 1);
+    }
+    mbar_init(bar(L::kDrain), 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(L::kQFull), 2 * L::kTile);
+      #pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kQOff + u * L::kTile + c * (128 * 128), &tm_q, bar(L::kQFull),
+                      c * 64, qt * 256 + 128 * u, h, b);
+      }
+    }
+    __syncwarp();
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < n_max; ++j) {
+      const int s = j & 1;
+      if (j >= 2 && !wait_uniform(bar(L::kKEmpty + s), ((j >> 1) + 1) & 1, abort)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTile);
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kKOff + s * L::kTile + c * (BC * 128), &tm_k, bar(L::kKFull + s),
+                      c * 64, j * BC, kh, b);
+      }
+      __syncwarp();
+      ++k_issued;
+      if (j >= 2 && !wait_uniform(bar(L::kVEmpty + s), ((j >> 1) + 1) & 1, abort)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTile);
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kVOff + s * L::kTile + c * (BC * 128), &tm_v, bar(L::kVFull + s),
+                      c * 64, j * BC, kh, b);
+      }
+      __syncwarp();
+      ++v_issued;
+    }
+    drain_wait(bar(L::kQFull), 0);
+    for (int j = max(0, k_issued - 2); j < k_issued; ++j)
+      drain_wait(bar(L::kKFull + (j & 1)), (j >> 1) & 1);
+    for (int j = max(0, v_issued - 2); j < v_issued; ++j)
+      drain_wait(bar(L::kVFull + (j & 1)), (j >> 1) & 1);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(128, BC, BF16 ? 1 : 0, 0, 0);
+    constexpr uint32_t kIdO = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+    const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+    const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
+    const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
+    auto issue_s = [&](int u, int j) {
+      const uint64_t qs = desc_add(q_desc, u * L::kTile);
+      const uint64_t ks = desc_add(k_desc, (j & 1) * L::kTile);
+      #pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t c = kk >> 2, w = kk & 3;
+        mma_ss(tmem + L::kTS + 128 * u, desc_add(qs, c * (128 * 128) + w * 32),
+               desc_add(ks, c * (BC * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kSFull + u));
+    };
+    bool ok = wait_uniform(bar(L::kQFull), 0, abort);
+    if (ok && n_max > 0) {
+      ok = wait_uniform(bar(L::kKFull), 0, abort);
+      if (ok) {
+        tc_fence_after();
+        if (n_kv[0] > 0) issue_s(0, 0);
+        if (n_kv[1] > 0) issue_s(1, 0);
+        mma_commit(bar(L::kKEmpty));
+      }
+    }
+    for (int j = 0; ok && j < n_max; ++j) {
+      const int s = j & 1;
+      if (!wait_uniform(bar(L::kVFull + s), (j >> 1) & 1, abort)) break;
+      const bool next_k = j + 1 < n_max;
+      bool k_ready = false;
+      #pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (j >= n_kv[u]) continue;
+        if (!wait_uniform(bar(L::kPFull + u), j & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t vs = desc_add(v_desc, s * L::kTile);
+        #pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_ts(tmem + L::kTO + 128 * u, tmem + L::kTS + 128 * u + kk * 8,
+                 desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kODone + u));
+        if (j + 1 < n_kv[u]) {
+          if (!k_ready) {
+            if (!wait_uniform(bar(L::kKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            k_ready = true;
+          }
+          issue_s(u, j + 1);
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar(L::kVEmpty + s));
+      if (next_k && k_ready) mma_commit(bar(L::kKEmpty + ((j + 1) & 1)));
+    }
+    mma_commit(bar(L::kDrain));
+    drain_wait(bar(L::kDrain), 0);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int u = (warp - 2) >> 2;                // query tile of this warpgroup
+    const int quarter = warp & 3;
+    const int r_tile = quarter * 32 + lane;
+    const int row = qt * 256 + 128 * u + r_tile;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + L::kTS + 128 * u + lane_off;
+    const uint32_t tO = tmem + L::kTO + 128 * u + lane_off;
+    const int nk = n_kv[u];
+    float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
+    bool ok = true;
+    const bool idle = qt * 256 + 128 * u + quarter * 32 >= p.Nq;
+    for (int j = 0; j < nk; ++j) {
+      if (!wait_uniform(bar(L::kSFull + u), j & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      if (idle) {
+        if (j > 0 && !wait_uniform(bar(L::kODone + u), (j - 1) & 1, abort)) { ok = false; break; }
+        tc_fence_before();
+        mbar_arrive(bar(L::kPFull + u));
+        continue;
+      }
+      const int col0 = j * BC;
+      const bool need_mask =
+          (CAUSAL && col0 + BC - 1 > qt * 256 + 128 * u + p.off) || (col0 + BC > p.Nk);
+      // pass 1: row maximum (two halves of 64 columns)
+      float mpart[8];
+      #pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[64];
+        tmem_ld32(tS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_wait();
+        reg_fence(sr);
+        float* s = reinterpret_cast<float*>(sr);
+        if (need_mask) {
+          #pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const int col = col0 + 64 * hh + i;
+            if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
+          }
+        }
+        #pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          const float a = fmaxf(s[2 * uu], s[2 * uu + 1]);
+          mpart[uu] = hh == 0 ? a : fmaxf(mpart[uu], a);
+        }
+        #pragma unroll
+        for (int i = 16; i < 64; i += 16) {
+          #pragma unroll
+          for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmax3(mpart[uu], s[i + 2 * uu], s[i + 2 * uu + 1]);
+        }
+      }
+      const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
+                             fmaxf(mpart[6], mpart[7]));
+      const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+      const bool need = m_new > m_ref + kRescaleThreshold;
+      const bool any = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (any) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+        l *= alpha;
+        l_r *= alpha;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // pass 2: weights (read again from TMEM), written over S as 16 bits
+      f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      float rs_r[4] = {0.f, 0.f, 0.f, 0.f};
+      const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
+      #pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[64];
+        tmem_ld32(tS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_wait();
+        reg_fence(sr);
+        float* s = reinterpret_cast<float*>(sr);
+        if (need_mask) {
+          #pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const int col = col0 + 64 * hh + i;
+            if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
+          }
+        }
+        uint32_t pk[32];
+        #pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const f2 arg = ffma2(f2{s[2 * i], s[2 * i + 1]}, cs, cm);
+          const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
+          pk[i] = pack2<BF16>(pe.x, pe.y);
+          rs[i & 3] = fadd2(rs[i & 3], pe);
+          // l_r: the rounded weights the P V product uses (O is divided by
+          // it); L uses the exact sum l
+          rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
+        }
+        // P over the first half of this 64-column part, already read
+        tmem_st32(tS + 32 * hh, pk);
+      }
+      const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+      l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
+      l_r += (rs_r[0] + rs_r[1]) + (rs_r[2] + rs_r[3]);
+      tmem_st_wait();
+      if (j > 0 && !wait_uniform(bar(L::kODone + u), (j - 1) & 1, abort)) { ok = false; break; }
+      if (any && j > 0) {
+        tc_fence_after();
+        #pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o2[64];
+          tmem_ld32(tO + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
+          tmem_ld32(tO + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
+          tmem_ld_wait();
+          reg_fence(o2);
+          #pragma unroll
+          for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
+          tmem_st32(tO + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
+          tmem_st32(tO + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kPFull + u));
+    }
+    // ------------------------------------------------------------ epilogue
+    const bool in_range = row < p.Nq;
+    const size_t lrow = (static_cast<size_t>(b) * p.H + h) * p.Nq + (in_range ? row : 0);
+    uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
+                                           h * p.o_sh + (in_range ? row : 0) * p.o_sn);
+    if (ok && nk == 0) {
+      // no row of this tile sees any key: O = 0, L = -inf
+      if (in_range) {
+        #pragma unroll
+        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[lrow] = -INFINITY;
+      }
+    } else if (ok && wait_uniform(bar(L::kODone + u), (nk - 1) & 1, abort)) {
+      tc_fence_after();
+      const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
+      const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      #pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o1[32];
+        tmem_ld32(tO + 32 * c, o1);
+        tmem_ld_wait();
+        reg_fence(o1);
+        uint32_t w[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l, __uint_as_float(o1[2 * i + 1]) * inv_l);
+        if (in_range) {
+          #pragma unroll
+          for (int i = 0; i < 4; ++i)
+            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (in_range) p.lse[lrow] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_fwd2(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
+  using L = Fwd2Layout;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e;
+  if ((e = make_tmap_4d(&tq, a.q, 128, pr.Nq, pr.H, pr.B, a.qs, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tk, a.k, 128, pr.Nk, pr.Hkv, pr.B, a.ks, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tv, a.v, 128, pr.Nk, pr.Hkv, pr.B, a.vs, 64, 128)) != cudaSuccess) return e;
+  auto kern = fwd2_kernel<CAUSAL, BF16>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  FwdParams p = {};
+  p.o = a.o;
+  p.lse = a.lse;
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.G = pr.H / pr.Hkv;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.off = pr.Nk - pr.Nq;
+  p.mask_rows = pr.Nq;
+  p.num_q_tiles = (pr.Nq + 255) / 256;
+  p.splits = 1;
+  p.scale_log2 = pr.scale * 1.4426950408889634f;
+  p.o_sb = a.os.b;
+  p.o_sh = a.os.h;
+  p.o_sn = a.os.n;
+  p.err = pr.err;
+  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  const int slot = timing_begin(FA_KERNEL_FWD, stream);
+  kern<<<grid, kFwd2Threads, L::kAlloc, stream>>>(tq, tk, tv, p);
+  timing_end(slot, stream);
+  return cudaGetLastError();
+}
+
 // Merge the per-split partial results of one query row: with L_s the split
 // logsumexps, L = ln sum_s exp(L_s) and O = sum_s exp(L_s - L) O_s.  One warp
 // per row.  A row no split has a key for gets O = 0, L = -inf.
@@ -630,6 +1034,11 @@ cudaError_t dispatch_flags(const Problem& pr, const FwdArgs& a, cudaStream_t s) 
 // Tile configuration per head dimension: key tile BC, K and V ring stages.
 template <bool SPARSE>
 cudaError_t launch_fwd_for(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
+  // d = 128, long queries without the mask, one pass: two query tiles per
+  // CTA (measured faster there; under the mask the one-tile kernel with the
+  // row sums on the tensor core is faster)
+  if (!SPARSE && pr.d == 128 && !pr.causal && !a.pack && a.splits <= 1 && pr.Nq > 128)
+    return pr.bf16 ? launch_fwd2<false, true>(pr, a, stream) : launch_fwd2<false, false>(pr, a, stream);
   switch (pr.d) {
     case 64: return dispatch_flags<64, 128, 3, 3, SPARSE>(pr, a, stream);
     case 128: return dispatch_flags<128, 128, 2, 2, SPARSE>(pr, a, stream);
