@@ -504,7 +504,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 }
 
 // ---------------------------------------------------------------------------
-// d = 128, two query tiles per CTA (long queries without the causal mask).
+// d = 128, two query tiles per CTA (the path for long queries).
 //
 // With one tile per CTA the tensor pipe idles while the softmax of tile j
 // runs (P V_j needs P_j) and the softmax warps idle while the products run.
@@ -514,7 +514,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 //   P V_A(j), S_A(j+1), P V_B(j), S_B(j+1), ...
 // so while one warpgroup exponentiates, the pipe works for the other.
 // TMEM: S_A, S_B, O_A, O_B (128 columns each; P written over S in 16 bits).
-// The row sums are formed on the ALU (no room for the ones columns).
+// The row sums are formed on the ALU (no room for the ones columns), and O
+// is divided by the exact sum of the weights.
 // Warps: 0 TMA producer, 1 MMA issuer, 2..5 softmax tile A, 6..9 tile B.
 constexpr int kFwd2Threads = 320;
 
@@ -709,7 +710,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t tS = tmem + L::kTS + 128 * u + lane_off;
     const uint32_t tO = tmem + L::kTO + 128 * u + lane_off;
     const int nk = n_kv[u];
-    float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     const bool idle = qt * 256 + 128 * u + quarter * 32 >= p.Nq;
     for (int j = 0; j < nk; ++j) {
@@ -724,33 +725,27 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       const int col0 = j * BC;
       const bool need_mask =
           (CAUSAL && col0 + BC - 1 > qt * 256 + 128 * u + p.off) || (col0 + BC > p.Nk);
-      // pass 1: row maximum (two halves of 64 columns)
+      uint32_t sr[BC];
+      #pragma unroll
+      for (int c = 0; c < BC / 32; ++c)
+        tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      tmem_ld_wait();
+      reg_fence(sr);
+      float* s = reinterpret_cast<float*>(sr);
+      if (need_mask) {
+        #pragma unroll
+        for (int i = 0; i < BC; ++i) {
+          const int col = col0 + i;
+          if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
+        }
+      }
       float mpart[8];
       #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[64];
-        tmem_ld32(tS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld_wait();
-        reg_fence(sr);
-        float* s = reinterpret_cast<float*>(sr);
-        if (need_mask) {
-          #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const int col = col0 + 64 * hh + i;
-            if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
-          }
-        }
+      for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmaxf(s[2 * uu], s[2 * uu + 1]);
+      #pragma unroll
+      for (int i = 16; i < BC; i += 16) {
         #pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          const float a = fmaxf(s[2 * uu], s[2 * uu + 1]);
-          mpart[uu] = hh == 0 ? a : fmaxf(mpart[uu], a);
-        }
-        #pragma unroll
-        for (int i = 16; i < 64; i += 16) {
-          #pragma unroll
-          for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmax3(mpart[uu], s[i + 2 * uu], s[i + 2 * uu + 1]);
-        }
+        for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmax3(mpart[uu], s[i + 2 * uu], s[i + 2 * uu + 1]);
       }
       const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
                              fmaxf(mpart[6], mpart[7]));
@@ -762,45 +757,27 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
         m_ref = m_new;
         l *= alpha;
-        l_r *= alpha;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // pass 2: weights (read again from TMEM), written over S as 16 bits
+      // weights written over S as 16 bits, 32 columns at a time; the exact
+      // sum l serves both L and the final division (rounding to nearest
+      // leaves the rounded weights' sum unbiased)
       f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-      float rs_r[4] = {0.f, 0.f, 0.f, 0.f};
       const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
       #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[64];
-        tmem_ld32(tS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld_wait();
-        reg_fence(sr);
-        float* s = reinterpret_cast<float*>(sr);
-        if (need_mask) {
-          #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const int col = col0 + 64 * hh + i;
-            if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
-          }
-        }
-        uint32_t pk[32];
+      for (int c = 0; c < BC / 32; ++c) {
+        uint32_t pk[16];
         #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const f2 arg = ffma2(f2{s[2 * i], s[2 * i + 1]}, cs, cm);
+        for (int i = 0; i < 16; ++i) {
+          const f2 arg = ffma2(f2{s[32 * c + 2 * i], s[32 * c + 2 * i + 1]}, cs, cm);
           const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
           pk[i] = pack2<BF16>(pe.x, pe.y);
           rs[i & 3] = fadd2(rs[i & 3], pe);
-          // l_r: the rounded weights the P V product uses (O is divided by
-          // it); L uses the exact sum l
-          rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
         }
-        // P over the first half of this 64-column part, already read
-        tmem_st32(tS + 32 * hh, pk);
+        tmem_st16(tS + 16 * c, pk);
       }
       const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
       l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
-      l_r += (rs_r[0] + rs_r[1]) + (rs_r[2] + rs_r[3]);
       tmem_st_wait();
       if (j > 0 && !wait_uniform(bar(L::kODone + u), (j - 1) & 1, abort)) { ok = false; break; }
       if (any && j > 0) {
@@ -836,7 +813,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
     } else if (ok && wait_uniform(bar(L::kODone + u), (nk - 1) & 1, abort)) {
       tc_fence_after();
-      const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -1034,11 +1011,12 @@ cudaError_t dispatch_flags(const Problem& pr, const FwdArgs& a, cudaStream_t s) 
 // Tile configuration per head dimension: key tile BC, K and V ring stages.
 template <bool SPARSE>
 cudaError_t launch_fwd_for(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
-  // d = 128, long queries without the mask, one pass: two query tiles per
-  // CTA (measured faster there; under the mask the one-tile kernel with the
-  // row sums on the tensor core is faster)
-  if (!SPARSE && pr.d == 128 && !pr.causal && !a.pack && a.splits <= 1 && pr.Nq > 128)
+  // d = 128, long queries, one pass: two query tiles per CTA
+  if (!SPARSE && pr.d == 128 && !a.pack && a.splits <= 1 && pr.Nq > 128) {
+    if (pr.causal)
+      return pr.bf16 ? launch_fwd2<true, true>(pr, a, stream) : launch_fwd2<true, false>(pr, a, stream);
     return pr.bf16 ? launch_fwd2<false, true>(pr, a, stream) : launch_fwd2<false, false>(pr, a, stream);
+  }
   switch (pr.d) {
     case 64: return dispatch_flags<64, 128, 3, 3, SPARSE>(pr, a, stream);
     case 128: return dispatch_flags<128, 128, 2, 2, SPARSE>(pr, a, stream);

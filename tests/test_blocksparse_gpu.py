@@ -83,9 +83,9 @@ def test_blocksparse_matches_oracle(d, causal, Nq, Nk, per_head):
 def test_all_ones_mask_is_the_dense_kernel(d, causal):
     """Every block kept: the same tiles in the same order as the dense path,
     so the forward and the deterministic backward agree with it bit for bit.
-    (The dense forward at d = 128 without the mask runs the two-tile kernel,
-    which sums the row weights on the ALU instead of the tensor core: there
-    the forward is compared within the parity tolerances.)"""
+    (The dense forward at d = 128 runs the two-tile kernel, which sums the
+    row weights on the ALU and divides by their exact sum: there the forward
+    is compared within the parity tolerances.)"""
     w = Workload("bs1", 2, 4, 1, 640, d, "f16", causal, 90 + d)
     q, k, v, do = (t.to(DEV) for t in make_inputs(w))
     ones = torch.ones((1, 5, 5), dtype=torch.uint8, device=DEV)
@@ -95,7 +95,7 @@ def test_all_ones_mask_is_the_dense_kernel(d, causal):
                                        deterministic=True)
     g_d = binding.backward(q, k, v, o_d, l_d, do, causal, w.scale, deterministic=True)
     binding.device_status()
-    if d == 128 and not causal:
+    if d == 128:
         assert (o_s.float() - o_d.float()).abs().max().item() <= 2e-3
         assert (l_s - l_d).abs().max().item() <= 1e-5
     else:
