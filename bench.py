@@ -42,6 +42,8 @@ L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_fwd_kernel.cuh",
                   "exact_io_aware_20_gb300/csrc/fa_bwd_kernel.cuh",
+                  "exact_io_aware_20_gb300/csrc/fa_bwd_dq_kernel.cuh",
+                  "exact_io_aware_20_gb300/csrc/fa_api.cu",
                   "exact_io_aware_20_gb300/csrc/block_list.cuh",
                   "exact_io_aware_20_gb300/csrc/sm103_ptx.cuh"]
 
@@ -490,8 +492,14 @@ def main():
     dom = max(kernel_times, key=lambda kk: kernel_times[kk][0])
     dom_ms, dom_n = kernel_times[dom]
     per_launch_ms = dom_ms / max(dom_n, 1)
-    if dom in ("fwd", "bwd_main"):
-        fl = w.flops_fwd() if dom == "fwd" else w.flops_bwd()
+    if dom in ("fwd", "bwd_main", "bwd_dq"):
+        # products per kernel, each w.flops_fwd() / 2: forward 2; backward 5,
+        # or 4 in the main kernel and 3 in the query-outer dQ kernel when dQ
+        # is computed there (S and dP formed again)
+        dq_outer = kernel_times.get("bwd_dq", (0.0, 0))[1] > 0
+        fl = {"fwd": 2.0, "bwd_main": 4.0 if dq_outer else 5.0, "bwd_dq": 3.0}[dom] * \
+            w.flops_fwd() / 2
+
         achieved = fl / (per_launch_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
@@ -515,8 +523,8 @@ def main():
             kernels[kind] = {"ms_per_launch": round(ms / n, 4), "launches": n,
                              "share": round(ms / sum(x[0] for x in kernel_times.values()), 4)}
     fwd_ms = kernel_times["fwd"][0] / max(kernel_times["fwd"][1], 1)
-    bwd_ms = sum(kernel_times[kk][0] for kk in ("bwd_pre", "bwd_main", "bwd_convert")) / \
-        max(kernel_times["bwd_main"][1], 1)
+    bwd_ms = sum(kernel_times[kk][0] for kk in ("bwd_pre", "bwd_main", "bwd_convert", "bwd_dq")
+                 if kk in kernel_times) / max(kernel_times["bwd_main"][1], 1)
     gpu_launches = sum(n for _, n in kernel_times.values())
 
     line = {

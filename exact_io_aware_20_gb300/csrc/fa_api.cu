@@ -472,6 +472,12 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
   float* delta = static_cast<float*>(workspace);
   float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);
+  // dQ strategy, chosen by measurement on GB300: at d = 128 the query-outer
+  // kernel (S and dP formed again, no atomics) is faster than adding every
+  // key tile's contribution into the fp32 accumulator, whose reductions bound
+  // the key-outer kernel; at d = 64 and 256 the atomic path is faster.  Under
+  // a block mask the atomic path is kept unless reproducibility is asked for.
+  if (d == 128 && mask == nullptr) deterministic = 1;
   fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};
   if (mask != nullptr) a.mask = *mask;
   if (strd != nullptr) {

@@ -386,6 +386,359 @@ cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// d = 128: 128-key tiles, so every product is an N = 128 tcgen05.mma (full
+// rate; with 64-key tiles S and dP ran at half rate).
+// TMEM: S (two buffers, 128 columns each; dS written over S in 16 bits),
+// dP (128), dQ (128).  Warps: 0 TMA producer (Q, dO once; K, V rings),
+// 1 MMA issuer, 2..9 dS warps (a query row per thread; warps w and w + 4
+// share a TMEM lane quarter and split the 128 key columns in halves).
+// Issue order per key tile j: S(j+1), [dS(j)] dP(j+1), dQ += dS(j) K_j.
+// dS stays in TMEM and is the A operand of the dQ product (TS form).
+constexpr int kDq128Threads = 320;
+
+// KST: K stages.  K_j is read until dQ_j, the last product of the tile, so
+// with two stages the load of K_{j+2} would start only when dQ_j is done;
+// the dense kernel has room for a third.
+template <int KST>
+struct Dq128Layout {
+  static constexpr int kTile = 128 * 128 * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kTile;
+  static constexpr int kKOff = 2 * kTile;             // KST stages
+  static constexpr int kVOff = (2 + KST) * kTile;     // two stages
+  static constexpr int kBarOff = (4 + KST) * kTile;
+  static constexpr int kQDFull = 0, kKFull = 1, kKEmpty = kKFull + KST, kVFull = kKEmpty + KST,
+                       kVEmpty = kVFull + 2, kSFull = kVEmpty + 2, kDPFull = kSFull + 2,
+                       kDSFull = kDPFull + 1, kDQDone = kDSFull + 1, kDrain = kDQDone + 1,
+                       kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kListOff = kMiscOff + 16;
+  static constexpr int kBytes = kListOff + kDqListCap * 2;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr int kAllocDense = kListOff + 1024;
+  static constexpr uint32_t kTS = 0, kTdP = 256, kTdQ = 384, kTmemCols = 512;
+  static_assert(kAllocDense <= 227 * 1024, "shared memory budget");
+};
+
+template <bool CAUSAL, bool BF16, bool SPARSE>
+__global__ void __launch_bounds__(kDq128Threads, 1)
+bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                 const DqParams p) {
+  constexpr int KST = SPARSE ? 2 : 3;
+  using L = Dq128Layout<KST>;
+  static_assert(!SPARSE || L::kAlloc <= 227 * 1024, "shared memory budget");
+  constexpr int D = 128, BR = 128, BC = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  int* list_count = reinterpret_cast<int*>(smem + L::kMiscOff + 8);
+  uint16_t* tile_list = reinterpret_cast<uint16_t*>(smem + L::kListOff);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = CAUSAL ? (p.num_q_tiles - 1 - static_cast<int>(blockIdx.x))
+                        : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kh = h / p.G;
+  int n_kv = (p.Nk + BC - 1) / BC;
+  if (CAUSAL) {
+    const int last_key = min((qt + 1) * BR, p.Nq) - 1 + p.off;
+    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
+  }
+  constexpr bool sparse = SPARSE;
+  if (sparse && warp == 2) {
+    const int mh = p.mask.heads == 1 ? 0 : h;
+    const unsigned char* mrow =
+        p.mask.ptr + (static_cast<size_t>(mh) * p.mask.nbr + qt) * p.mask.nbc;
+    const int lim = n_kv;
+    const int cnt = compact_steps<1>(
+        p.mask.nbc, [&](int e) { return mrow[e] != 0; },
+        [&](int e, int) { return e < lim ? e : -1; }, tile_list, kDqListCap);
+    if (lane == 0) *list_count = min(cnt, kDqListCap);
+  }
+  auto key_tile = [&](int j) -> int { return sparse ? static_cast<int>(tile_list[j]) : j; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQDFull), 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+      mbar_init(bar(L::kSFull + s), 1);
+    }
+    mbar_init(bar(L::kDPFull), 1);
+    mbar_init(bar(L::kDSFull), 256);
+    mbar_init(bar(L::kDQDone), 1);
+    mbar_init(bar(L::kDrain), 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (sparse) n_kv = *list_count;
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tdP = tmem + L::kTdP, tdQ = tmem + L::kTdQ;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(L::kQDFull), 2 * L::kTile);
+      #pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(sbase + L::kQOff + c * (BR * 128), &tm_q, bar(L::kQDFull), c * 64, qt * BR, h, b);
+        tma_load_4d(sbase + L::kDOOff + c * (BR * 128), &tm_do, bar(L::kQDFull), c * 64, qt * BR,
+                    h, b);
+      }
+    }
+    __syncwarp();
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j & 1, sk = j % KST;
+      if (j >= KST && !wait_uniform(bar(L::kKEmpty + sk), ((j / KST) + 1) & 1, abort)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kKFull + sk), L::kTile);
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kKOff + sk * L::kTile + c * (BC * 128), &tm_k, bar(L::kKFull + sk),
+                      c * 64, key_tile(j) * BC, kh, b);
+      }
+      __syncwarp();
+      ++k_issued;
+      if (j >= 2 && !wait_uniform(bar(L::kVEmpty + s), ((j >> 1) + 1) & 1, abort)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTile);
+        #pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + L::kVOff + s * L::kTile + c * (BC * 128), &tm_v, bar(L::kVFull + s),
+                      c * 64, key_tile(j) * BC, kh, b);
+      }
+      __syncwarp();
+      ++v_issued;
+    }
+    drain_wait(bar(L::kQDFull), 0);
+    for (int j = max(0, k_issued - KST); j < k_issued; ++j)
+      drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
+    for (int j = max(0, v_issued - 2); j < v_issued; ++j)
+      drain_wait(bar(L::kVFull + (j & 1)), (j >> 1) & 1);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(BR, BC, BF16 ? 1 : 0, 0, 0);   // S, dP
+    constexpr uint32_t kIdQ = idesc_f16(BR, D, BF16 ? 1 : 0, 0, 1);    // dQ (B = K MN-major)
+    const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+    const uint64_t do_desc = smem_desc_sw128(sbase + L::kDOOff, 16, 1024);
+    const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
+    const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, 16, 1024);
+    const uint64_t k_mn = smem_desc_sw128(sbase + L::kKOff, BC * 128, 1024);
+    auto issue_s = [&](int j) -> bool {
+      const int s = j & 1, sk = j % KST;
+      if (!wait_uniform(bar(L::kKFull + sk), (j / KST) & 1, abort)) return false;
+      tc_fence_after();
+      #pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t c = kk >> 2, w = kk & 3;
+        mma_ss(tmem + L::kTS + 128 * s, desc_add(q_desc, c * (BR * 128) + w * 32),
+               desc_add(k_desc, sk * L::kTile + c * (BC * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kSFull + s));
+      return true;
+    };
+    auto issue_dp = [&](int j) -> bool {
+      const int s = j & 1;
+      if (!wait_uniform(bar(L::kVFull + s), (j >> 1) & 1, abort)) return false;
+      tc_fence_after();
+      #pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t c = kk >> 2, w = kk & 3;
+        mma_ss(tdP, desc_add(do_desc, c * (BR * 128) + w * 32),
+               desc_add(v_desc, s * L::kTile + c * (BC * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kDPFull));
+      mma_commit(bar(L::kVEmpty + s));   // V_j is not read again
+      return true;
+    };
+    bool ok = wait_uniform(bar(L::kQDFull), 0, abort);
+    if (ok && n_kv > 0) ok = issue_s(0) && issue_dp(0);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j & 1;
+      // the other S buffer: its dS (tile j - 1) was read by dQ_{j-1}, issued earlier
+      if (j + 1 < n_kv && !issue_s(j + 1)) break;
+      if (!wait_uniform(bar(L::kDSFull), j & 1, abort)) break;
+      tc_fence_after();
+      // the dS warps have read dP_j: the next dP goes first, so they can
+      // start on it while dQ_j runs
+      if (j + 1 < n_kv && !issue_dp(j + 1)) break;
+      // dQ += dS_j K_j: dS (16-bit) in the first 32 columns of each 64-column
+      // half of S buffer s (one half per dS warp)
+      const int sk = j % KST;
+      #pragma unroll
+      for (int kk = 0; kk < BC / 16; ++kk)
+        mma_ts(tdQ, tmem + L::kTS + 128 * s + (kk >> 2) * 64 + (kk & 3) * 8,
+               desc_add(k_mn, sk * L::kTile + kk * 2048), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar(L::kKEmpty + sk));   // S_j and dQ_j were K_j's readers
+    }
+    mma_commit(bar(L::kDQDone));
+    mma_commit(bar(L::kDrain));
+    drain_wait(bar(L::kDrain), 0);
+  } else {
+    // ------------------------------------------------------------ dS warps
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;          // key columns [64 half, 64 half + 64)
+    const int row = qt * BR + quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const size_t row_idx = (static_cast<size_t>(b) * p.H + h) * p.Nq + (row < p.Nq ? row : 0);
+    const long long dq_off =
+        b * p.dqs.b + h * p.dqs.h + static_cast<long long>(row < p.Nq ? row : 0) * p.dqs.n;
+    const float nL = row < p.Nq ? -p.lse[row_idx] * kDqLog2e : -INFINITY;
+    const float nD = row < p.Nq ? -p.delta[row_idx] : 0.f;
+    const f2 cs = {p.scale_log2, p.scale_log2}, cl = {nL, nL}, cd = {nD, nD};
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j & 1;
+      const uint32_t tSb = tmem + L::kTS + 128 * s + lane_off + 64 * half;
+      if (!wait_uniform(bar(L::kSFull + s), (j >> 1) & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      const int col0 = key_tile(j) * BC + 64 * half;
+      const bool masked = (CAUSAL && col0 + 63 > qt * BR + p.off) || (col0 + 64 > p.Nk);
+      float P[64];
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t sr[32];
+        tmem_ld32(tSb + c0, sr);
+        tmem_ld_wait();
+        reg_fence(sr);
+        #pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs, cl);
+          P[c0 + c] = ex2_approx(arg.x);
+          P[c0 + c + 1] = ex2_approx(arg.y);
+        }
+        if (masked) {
+          #pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int col = col0 + c0 + c;
+            if (col >= p.Nk || (CAUSAL && col > row + p.off)) P[c0 + c] = 0.f;
+          }
+        }
+      }
+      if (!wait_uniform(bar(L::kDPFull), j & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t dr[32];
+        tmem_ld32(tdP + lane_off + 64 * half + c0, dr);
+        tmem_ld_wait();
+        reg_fence(dr);
+        uint32_t w[16];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]},
+                              fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])}, cd));
+          w[c] = pack2<BF16>(ds.x, ds.y);
+        }
+        // dS (16-bit) over the first 32 columns of this half, already read
+        tmem_st16(tSb + c0 / 2, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kDSFull));
+    }
+    // ------------------------------------------------------------ epilogue
+    uint4* out = reinterpret_cast<uint4*>(p.dq + dq_off + 64 * half);
+    if (ok && n_kv == 0) {
+      if (row < p.Nq) {
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else if (ok && wait_uniform(bar(L::kDQDone), 0, abort)) {
+      tc_fence_after();
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tdQ + lane_off + 64 * half + c0, v);
+        tmem_ld_wait();
+        reg_fence(v);
+        uint32_t o[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * p.scale, __uint_as_float(v[2 * i + 1]) * p.scale);
+        if (row < p.Nq) {
+          #pragma unroll
+          for (int i = 0; i < 4; ++i)
+            out[c0 / 8 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <bool CAUSAL, bool BF16, bool SPARSE>
+cudaError_t launch_dq128(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
+  using L = Dq128Layout<SPARSE ? 2 : 3>;
+  CUtensorMap tq, tk, tv, tdo;
+  cudaError_t e;
+  if ((e = make_tmap_4d(&tq, a.q, 128, pr.Nq, pr.H, pr.B, a.qs, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tdo, a.dout, 128, pr.Nq, pr.H, pr.B, a.dos, 64, 128)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_4d(&tk, a.k, 128, pr.Nk, pr.Hkv, pr.B, a.ks, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tv, a.v, 128, pr.Nk, pr.Hkv, pr.B, a.vs, 64, 128)) != cudaSuccess) return e;
+  auto kern = bwd_dq128_kernel<CAUSAL, BF16, SPARSE>;
+  constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+        cudaSuccess)
+      return e;
+    attr_set = true;
+  }
+  DqParams p;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq = static_cast<uint16_t*>(a.dq);
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.off = pr.Nk - pr.Nq;
+  p.G = pr.H / pr.Hkv;
+  p.num_q_tiles = (pr.Nq + 127) / 128;
+  p.scale = pr.scale;
+  p.scale_log2 = pr.scale * kDqLog2e;
+  p.mask = a.mask;
+  p.dqs = a.dqs;
+  p.err = pr.err;
+  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  const int slot = timing_begin(FA_KERNEL_BWD_DQ, stream);
+  kern<<<grid, kDq128Threads, kSmem, stream>>>(tq, tk, tv, tdo, p);
+  timing_end(slot, stream);
+  return cudaGetLastError();
+}
+
 template <int D, int KST, bool SPARSE>
 cudaError_t dispatch_dq(const Problem& pr, const BwdArgs& a, cudaStream_t s) {
   if (pr.causal)
@@ -398,9 +751,15 @@ cudaError_t dispatch_dq(const Problem& pr, const BwdArgs& a, cudaStream_t s) {
 // K / V ring stages per head dimension.
 template <bool SPARSE>
 cudaError_t launch_bwd_dq_for(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
+  if (pr.d == 128) {
+    if (pr.causal)
+      return pr.bf16 ? launch_dq128<true, true, SPARSE>(pr, a, stream)
+                     : launch_dq128<true, false, SPARSE>(pr, a, stream);
+    return pr.bf16 ? launch_dq128<false, true, SPARSE>(pr, a, stream)
+                   : launch_dq128<false, false, SPARSE>(pr, a, stream);
+  }
   switch (pr.d) {
     case 64: return dispatch_dq<64, 4, SPARSE>(pr, a, stream);
-    case 128: return dispatch_dq<128, 3, SPARSE>(pr, a, stream);
     case 256: return dispatch_dq<256, 1, SPARSE>(pr, a, stream);
     default: return cudaErrorInvalidValue;
   }

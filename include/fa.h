@@ -121,6 +121,11 @@ size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  * heads that share each key/value head).  workspace must be a device buffer
  * of at least fa_bwd_workspace_size(...) bytes, 256-byte aligned; its
  * contents on entry do not matter and are garbage on exit.
+ * dQ strategy (chosen by measurement): at d = 128 dQ comes from the
+ * query-outer kernel of fa_bwd_deterministic, which is the faster one there
+ * (every output is then bitwise reproducible); at d = 64 and 256 each key
+ * tile's contribution is added to an fp32 accumulator with atomic adds, the
+ * pages' scheme, whose summation order varies from run to run.
  */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
@@ -130,8 +135,9 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 /*
  * Backward pass of fa_fwd_qk: separate query and key lengths, the same mask.
  * dq [B][H][Nq][d], dk, dv [B][Hkv][Nk][d].  deterministic = 1 selects the
- * reproducible dQ path of fa_bwd_deterministic, 0 the one of fa_bwd.  The
- * workspace is fa_bwd_workspace_size(B, H, Hkv, Nq, d) bytes.
+ * reproducible dQ path of fa_bwd_deterministic for every head dim, 0 the
+ * choice of fa_bwd.  The workspace is fa_bwd_workspace_size(B, H, Hkv, Nq, d)
+ * bytes.
  */
 int fa_bwd_qk(const void *q, const void *k, const void *v, const void *o, const float *lse,
               const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int Nq,

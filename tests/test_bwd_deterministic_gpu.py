@@ -42,12 +42,17 @@ def test_deterministic_is_bitwise_reproducible(d):
     o, lse = binding.forward(q, k, v, w.causal, w.scale)
     r1 = binding.backward(q, k, v, o, lse, do, w.causal, w.scale, deterministic=True)
     r2 = binding.backward(q, k, v, o, lse, do, w.causal, w.scale, deterministic=True)
-    r3 = binding.backward(q, k, v, o, lse, do, w.causal, w.scale)   # atomic dQ
+    r3 = binding.backward(q, k, v, o, lse, do, w.causal, w.scale)   # fa_bwd's own choice
     binding.device_status()
     for a, b in zip(r1, r2):
         assert torch.equal(a, b)
     assert torch.equal(r1[1], r3[1]) and torch.equal(r1[2], r3[2])   # same dK / dV kernel
-    assert (r1[0].float() - r3[0].float()).abs().max().item() < 2e-2
+    if d == 128:
+        # fa_bwd computes dQ query-outer at d = 128: the same bits
+        assert torch.equal(r1[0], r3[0])
+    else:
+        # atomic dQ: equal up to the order of the additions
+        assert (r1[0].float() - r3[0].float()).abs().max().item() < 2e-2
 
 
 @pytest.mark.parametrize("name", ["gpt_layer_causal", "gqa8k"])

@@ -40,7 +40,7 @@ def test_bnhd_equals_contiguous_bitwise(d, causal, Nq, Nk):
     assert torch.equal(o_s, o_c) and torch.equal(l_s, l_c)
     for a, b in zip(g_s, g_c):
         assert torch.equal(a, b)
-    # atomic dQ path: dK, dV in a fixed order (same bits), dQ against the oracle
+    # fa_bwd's default dQ path: dK, dV in a fixed order (same bits), dQ against the oracle
     assert torch.equal(g_a[1], g_c[1]) and torch.equal(g_a[2], g_c[2])
     if d == 128 and causal:
         dq_r, dk_r, dv_r = oracle.backward(q.cpu(), k.cpu(), v.cpu(), do.cpu(), causal, w.scale)
