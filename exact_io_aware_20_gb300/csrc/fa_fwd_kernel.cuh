@@ -92,6 +92,8 @@ struct FwdParams {
   void* o;
   float* lse;
   int H, Hkv, G;
+  int B_;             // batch (the persistent kernel derives its units from it)
+  int sec_heads;      // persistent causal order: (batch, head) pairs per section
   int Nq, Nk;         // query rows per head (packed rows, see mask_rows) / key length
   int off;            // under the mask query i sees keys k <= i + off
   int mask_rows;      // query index of a row for the mask: row % mask_rows (== Nq unless
@@ -504,18 +506,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 }
 
 // ---------------------------------------------------------------------------
-// d = 128, two query tiles per CTA (the path for long queries).
+// d = 128, two query tiles per CTA (the path for long queries), persistent.
 //
 // With one tile per CTA the tensor pipe idles while the softmax of tile j
 // runs (P V_j needs P_j) and the softmax warps idle while the products run.
-// Here a CTA holds query tiles A and B (rows [256 t, 256 t + 128) and
-// [256 t + 128, 256 t + 256)) with one softmax warpgroup each; every key
-// tile is loaded once for both, and the MMA warp interleaves the tiles:
-//   P V_A(j), S_A(j+1), P V_B(j), S_B(j+1), ...
+// Here a work unit is two query tiles A and B (rows [256 t, 256 t + 128) and
+// [256 t + 128, 256 t + 256) of one head) with one softmax warpgroup each;
+// every key tile is loaded once for both, and the MMA warp interleaves the
+// tiles:  P V_A(j), S_A(j+1), P V_B(j), S_B(j+1), ...
 // so while one warpgroup exponentiates, the pipe works for the other.
 // TMEM: S_A, S_B, O_A, O_B (128 columns each; P written over S in 16 bits).
 // The row sums are formed on the ALU (no room for the ones columns), and O
 // is divided by the exact sum of the weights.
+//
+// Persistent: one CTA per SM walks a list of units in which (under the
+// mask) the longest come first, taking one unit of every round of gridDim.x
+// (forwards and backwards in turn, see fwd2_unit_index).  TMEM,
+// barriers and the K/V ring live across units (phase counters continue), the
+// next unit's scores start while the previous unit's epilogue drains O, and
+// its K/V tiles stream behind the previous unit's without a gap.
 // Warps: 0 TMA producer, 1 MMA issuer, 2..5 softmax tile A, 6..9 tile B.
 constexpr int kFwd2Threads = 320;
 
@@ -525,14 +534,68 @@ struct Fwd2Layout {
   static constexpr int kKOff = 2 * kTile;       // two stages
   static constexpr int kVOff = 4 * kTile;       // two stages
   static constexpr int kBarOff = 6 * kTile;
-  static constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7,
-                       kSFull = 9, kPFull = 11, kODone = 13, kDrain = 15, kNumBars = 16;
+  static constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6,
+                       kVEmpty = 8, kSFull = 10, kPFull = 12, kODone = 14, kOFree = 16,
+                       kDrain = 18, kNumBars = 19;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kTS = 0, kTO = 256, kTmemCols = 512;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
+
+// Work unit x of the persistent forward: 256-row block, head, batch, and the
+// key tiles of its two query tiles (0 if a tile holds no query row, or if
+// under the mask none of its rows sees a key).
+struct Fwd2Unit {
+  int blk, h, b, n_kv[2], n_max;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Fwd2Unit fwd2_unit(const FwdParams& p, int x) {
+  Fwd2Unit w;
+  int bh;
+  if (CAUSAL) {
+    // (batch, head) pairs in sections whose K / V fit in L2 together; in a
+    // section the longest 256-row blocks come first, then the next ones, the
+    // section's heads innermost
+    const int hb = p.H * p.B_;
+    const int per_sec = p.sec_heads * p.num_q_tiles;
+    const int sec = x / per_sec, r = x - sec * per_sec;
+    const int width = min(p.sec_heads, hb - sec * p.sec_heads);
+    w.blk = p.num_q_tiles - 1 - r / width;
+    bh = sec * p.sec_heads + r % width;
+  } else {
+    // consecutive units are consecutive blocks of one head (shared K / V)
+    w.blk = x % p.num_q_tiles;
+    bh = x / p.num_q_tiles;
+  }
+  w.b = bh / p.H;
+  w.h = bh - w.b * p.H;
+  #pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int first = w.blk * 256 + 128 * u;
+    w.n_kv[u] = (p.Nk + 127) / 128;
+    if (first >= p.Nq) {
+      w.n_kv[u] = 0;
+    } else if (CAUSAL) {
+      const int last_key = min(first + 128, p.Nq) - 1 + p.off;
+      w.n_kv[u] = last_key < 0 ? 0 : min(w.n_kv[u], last_key / 128 + 1);
+    }
+  }
+  w.n_max = max(w.n_kv[0], w.n_kv[1]);
+  return w;
+}
+
+// The i-th unit of this CTA, or -1 past the end: rounds of gridDim.x units,
+// walked forwards in even rounds and backwards in odd ones, so that over two
+// rounds of a longest-first list every CTA gets about the same work.
+__device__ __forceinline__ int fwd2_unit_index(int i, int n_units) {
+  const int base = i * static_cast<int>(gridDim.x);
+  const int x = base + ((i & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                                 : static_cast<int>(blockIdx.x));
+  return (base < n_units && x < n_units) ? x : -1;
+}
 
 template <bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kFwd2Threads, 1)
@@ -549,28 +612,11 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int xt = static_cast<int>(blockIdx.x);
-  const int qt = CAUSAL ? (p.num_q_tiles - 1 - xt) : xt;   // 256-row block, longest first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int kh = h / p.G;
-  // key tiles of each query tile (0 if the tile holds no query row, or if
-  // under the mask no row of it sees a key)
-  int n_kv[2];
-  #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int first = qt * 256 + 128 * u;
-    n_kv[u] = (p.Nk + BC - 1) / BC;
-    if (first >= p.Nq) {
-      n_kv[u] = 0;
-    } else if (CAUSAL) {
-      const int last_key = min(first + 128, p.Nq) - 1 + p.off;
-      n_kv[u] = last_key < 0 ? 0 : min(n_kv[u], last_key / BC + 1);
-    }
-  }
-  const int n_max = max(n_kv[0], n_kv[1]);
+  const int n_units = p.num_q_tiles * p.H * p.B_;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
+    mbar_init(bar(L::kQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kKEmpty + s), 1);
@@ -579,6 +625,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(bar(L::kSFull + s), 1);
       mbar_init(bar(L::kPFull + s), 128);
       mbar_init(bar(L::kODone + s), 1);
+      mbar_init(bar(L::kOFree + s), 128);
     }
     mbar_init(bar(L::kDrain), 1);
     *abort = 0;
@@ -599,45 +646,63 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(L::kQFull), 2 * L::kTile);
-      #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tma_load_4d(sbase + L::kQOff + u * L::kTile + c * (128 * 128), &tm_q, bar(L::kQFull),
-                      c * 64, qt * 256 + 128 * u, h, b);
-      }
     }
     __syncwarp();
-    int k_issued = 0, v_issued = 0;
-    for (int j = 0; j < n_max; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !wait_uniform(bar(L::kKEmpty + s), ((j >> 1) + 1) & 1, abort)) break;
+    int it = 0, kt = 0;                 // units and key tiles loaded so far
+    int k_issued = 0, v_issued = 0, q_issued = 0;
+    bool ok = true;
+    auto load_kv = [&](const Fwd2Unit& w, int j) -> bool {
+      const int g = kt + j, s = g & 1;
+      const int kh = w.h / p.G;
+      if (g >= 2 && !wait_uniform(bar(L::kKEmpty + s), ((g >> 1) + 1) & 1, abort)) return false;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTile);
         #pragma unroll
         for (int c = 0; c < 2; ++c)
           tma_load_4d(sbase + L::kKOff + s * L::kTile + c * (BC * 128), &tm_k, bar(L::kKFull + s),
-                      c * 64, j * BC, kh, b);
+                      c * 64, j * BC, kh, w.b);
       }
       __syncwarp();
       ++k_issued;
-      if (j >= 2 && !wait_uniform(bar(L::kVEmpty + s), ((j >> 1) + 1) & 1, abort)) break;
+      if (g >= 2 && !wait_uniform(bar(L::kVEmpty + s), ((g >> 1) + 1) & 1, abort)) return false;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTile);
         #pragma unroll
         for (int c = 0; c < 2; ++c)
           tma_load_4d(sbase + L::kVOff + s * L::kTile + c * (BC * 128), &tm_v, bar(L::kVFull + s),
-                      c * 64, j * BC, kh, b);
+                      c * 64, j * BC, kh, w.b);
       }
       __syncwarp();
       ++v_issued;
+      return true;
+    };
+    for (int x = fwd2_unit_index(0, n_units); ok && x >= 0; x = fwd2_unit_index(++it, n_units)) {
+      const Fwd2Unit w = fwd2_unit<CAUSAL>(p, x);
+      // the first key tile streams behind the previous unit's; Q waits until
+      // the previous unit's scores have all been issued and have completed
+      if (w.n_max > 0 && !load_kv(w, 0)) { ok = false; break; }
+      if (it >= 1 && !wait_uniform(bar(L::kQEmpty), (it - 1) & 1, abort)) { ok = false; break; }
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(L::kQFull), 2 * L::kTile);
+        #pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          #pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sbase + L::kQOff + u * L::kTile + c * (128 * 128), &tm_q, bar(L::kQFull),
+                        c * 64, w.blk * 256 + 128 * u, w.h, w.b);
+        }
+      }
+      __syncwarp();
+      ++q_issued;
+      for (int j = 1; j < w.n_max; ++j)
+        if (!load_kv(w, j)) { ok = false; break; }
+      kt += w.n_max;
     }
-    drain_wait(bar(L::kQFull), 0);
-    for (int j = max(0, k_issued - 2); j < k_issued; ++j)
-      drain_wait(bar(L::kKFull + (j & 1)), (j >> 1) & 1);
-    for (int j = max(0, v_issued - 2); j < v_issued; ++j)
-      drain_wait(bar(L::kVFull + (j & 1)), (j >> 1) & 1);
+    if (q_issued > 0) drain_wait(bar(L::kQFull), (q_issued - 1) & 1);
+    for (int g = max(0, k_issued - 2); g < k_issued; ++g)
+      drain_wait(bar(L::kKFull + (g & 1)), (g >> 1) & 1);
+    for (int g = max(0, v_issued - 2); g < v_issued; ++g)
+      drain_wait(bar(L::kVFull + (g & 1)), (g >> 1) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_f16(128, BC, BF16 ? 1 : 0, 0, 0);
@@ -645,9 +710,9 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
     const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
     const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
-    auto issue_s = [&](int u, int j) {
+    auto issue_s = [&](int u, int stage) {
       const uint64_t qs = desc_add(q_desc, u * L::kTile);
-      const uint64_t ks = desc_add(k_desc, (j & 1) * L::kTile);
+      const uint64_t ks = desc_add(k_desc, stage * L::kTile);
       #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t c = kk >> 2, w = kk & 3;
@@ -656,47 +721,69 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       }
       mma_commit(bar(L::kSFull + u));
     };
-    bool ok = wait_uniform(bar(L::kQFull), 0, abort);
-    if (ok && n_max > 0) {
-      ok = wait_uniform(bar(L::kKFull), 0, abort);
-      if (ok) {
+    int it = 0, kt = 0;
+    int cp[2] = {0, 0};                  // P_FULL phases consumed per tile
+    int of[2] = {0, 0};                  // units so far with products on each tile
+    bool ok = true;
+    for (int x = fwd2_unit_index(0, n_units); ok && x >= 0; x = fwd2_unit_index(++it, n_units)) {
+      const Fwd2Unit w = fwd2_unit<CAUSAL>(p, x);
+      if (!wait_uniform(bar(L::kQFull), it & 1, abort)) { ok = false; break; }
+      if (w.n_max > 0) {
+        if (!wait_uniform(bar(L::kKFull + (kt & 1)), (kt >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
-        if (n_kv[0] > 0) issue_s(0, 0);
-        if (n_kv[1] > 0) issue_s(1, 0);
-        mma_commit(bar(L::kKEmpty));
+        if (w.n_kv[0] > 0) issue_s(0, kt & 1);
+        if (w.n_kv[1] > 0) issue_s(1, kt & 1);
+        mma_commit(bar(L::kKEmpty + (kt & 1)));
       }
-    }
-    for (int j = 0; ok && j < n_max; ++j) {
-      const int s = j & 1;
-      if (!wait_uniform(bar(L::kVFull + s), (j >> 1) & 1, abort)) break;
-      const bool next_k = j + 1 < n_max;
-      bool k_ready = false;
+      // Q is free for the next unit once the last score product of this one
+      // completes (the scores of key tile j + 1 are issued in step j)
+      if (w.n_max <= 1) mma_commit(bar(L::kQEmpty));
+      // the last epilogue that read O_u out is done before P V overwrites it
+      // (O_FREE completes once per unit with products on the tile, so it
+      // never runs two phases ahead of this wait)
       #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        if (j >= n_kv[u]) continue;
-        if (!wait_uniform(bar(L::kPFull + u), j & 1, abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t vs = desc_add(v_desc, s * L::kTile);
-        #pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk)
-          mma_ts(tmem + L::kTO + 128 * u, tmem + L::kTS + 128 * u + kk * 8,
-                 desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::kODone + u));
-        if (j + 1 < n_kv[u]) {
-          if (!k_ready) {
-            if (!wait_uniform(bar(L::kKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            k_ready = true;
-          }
-          issue_s(u, j + 1);
+        if (w.n_kv[u] > 0 && of[u] > 0 && !wait_uniform(bar(L::kOFree + u), (of[u] - 1) & 1, abort)) {
+          ok = false;
+          break;
         }
+        of[u] += w.n_kv[u] > 0 ? 1 : 0;
       }
       if (!ok) break;
-      mma_commit(bar(L::kVEmpty + s));
-      if (next_k && k_ready) mma_commit(bar(L::kKEmpty + ((j + 1) & 1)));
+      for (int j = 0; ok && j < w.n_max; ++j) {
+        const int g = kt + j, s = g & 1;
+        if (!wait_uniform(bar(L::kVFull + s), (g >> 1) & 1, abort)) { ok = false; break; }
+        bool k_ready = false;
+        #pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (j >= w.n_kv[u]) continue;
+          if (!wait_uniform(bar(L::kPFull + u), cp[u] & 1, abort)) { ok = false; break; }
+          ++cp[u];
+          tc_fence_after();
+          const uint64_t vs = desc_add(v_desc, s * L::kTile);
+          #pragma unroll
+          for (int kk = 0; kk < BC / 16; ++kk)
+            mma_ts(tmem + L::kTO + 128 * u, tmem + L::kTS + 128 * u + kk * 8,
+                   desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::kODone + u));
+          if (j + 1 < w.n_kv[u]) {
+            if (!k_ready) {
+              if (!wait_uniform(bar(L::kKFull + ((g + 1) & 1)), ((g + 1) >> 1) & 1, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(u, (g + 1) & 1);
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(L::kVEmpty + s));
+        if (k_ready) mma_commit(bar(L::kKEmpty + ((g + 1) & 1)));
+        if (j + 2 == w.n_max) mma_commit(bar(L::kQEmpty));
+      }
+      kt += w.n_max;
     }
     mma_commit(bar(L::kDrain));
     drain_wait(bar(L::kDrain), 0);
@@ -705,133 +792,159 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const int u = (warp - 2) >> 2;                // query tile of this warpgroup
     const int quarter = warp & 3;
     const int r_tile = quarter * 32 + lane;
-    const int row = qt * 256 + 128 * u + r_tile;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + L::kTS + 128 * u + lane_off;
     const uint32_t tO = tmem + L::kTO + 128 * u + lane_off;
-    const int nk = n_kv[u];
-    float m_ref = -INFINITY, l = 0.f;
+    int cs = 0, co = 0;                           // S_FULL / O_DONE phases consumed
     bool ok = true;
-    const bool idle = qt * 256 + 128 * u + quarter * 32 >= p.Nq;
-    for (int j = 0; j < nk; ++j) {
-      if (!wait_uniform(bar(L::kSFull + u), j & 1, abort)) { ok = false; break; }
-      tc_fence_after();
-      if (idle) {
-        if (j > 0 && !wait_uniform(bar(L::kODone + u), (j - 1) & 1, abort)) { ok = false; break; }
+    for (int i = 0, x = fwd2_unit_index(0, n_units); ok && x >= 0;
+         x = fwd2_unit_index(++i, n_units)) {
+      int row0, nk;                               // first row of the tile, its key tiles
+      {
+        const Fwd2Unit w = fwd2_unit<CAUSAL>(p, x);
+        row0 = w.blk * 256 + 128 * u;
+        nk = w.n_kv[u];
+      }
+      const int row = row0 + r_tile;
+      float m_ref = -INFINITY, l = 0.f;
+      const bool idle = row0 + quarter * 32 >= p.Nq;
+      for (int j = 0; j < nk; ++j) {
+        if (!wait_uniform(bar(L::kSFull + u), cs & 1, abort)) { ok = false; break; }
+        ++cs;
+        tc_fence_after();
+        if (idle) {
+          if (j > 0) {
+            if (!wait_uniform(bar(L::kODone + u), co & 1, abort)) { ok = false; break; }
+            ++co;
+          }
+          tc_fence_before();
+          mbar_arrive(bar(L::kPFull + u));
+          continue;
+        }
+        const int col0 = j * BC;
+        const bool need_mask =
+            (CAUSAL && col0 + BC - 1 > row0 + p.off) || (col0 + BC > p.Nk);
+        uint32_t sr[BC];
+        #pragma unroll
+        for (int c = 0; c < BC / 32; ++c)
+          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_ld_wait();
+        reg_fence(sr);
+        float* s = reinterpret_cast<float*>(sr);
+        if (need_mask) {
+          #pragma unroll
+          for (int i = 0; i < BC; ++i) {
+            const int col = col0 + i;
+            if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
+          }
+        }
+        float mpart[8];
+        #pragma unroll
+        for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmaxf(s[2 * uu], s[2 * uu + 1]);
+        #pragma unroll
+        for (int i = 16; i < BC; i += 16) {
+          #pragma unroll
+          for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmax3(mpart[uu], s[i + 2 * uu], s[i + 2 * uu + 1]);
+        }
+        const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
+                               fmaxf(mpart[6], mpart[7]));
+        const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        const bool any = __any_sync(0xffffffffu, need);
+        float alpha = 1.f;
+        if (any) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          l *= alpha;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // weights written over S as 16 bits, 32 columns at a time; the exact
+        // sum l serves both L and the final division (rounding to nearest
+        // leaves the rounded weights' sum unbiased)
+        f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        const f2 cs2 = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
+        #pragma unroll
+        for (int c = 0; c < BC / 32; ++c) {
+          uint32_t pk[16];
+          #pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const f2 arg = ffma2(f2{s[32 * c + 2 * i], s[32 * c + 2 * i + 1]}, cs2, cm);
+            const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
+            pk[i] = pack2<BF16>(pe.x, pe.y);
+            rs[i & 3] = fadd2(rs[i & 3], pe);
+          }
+          tmem_st16(tS + 16 * c, pk);
+        }
+        const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+        l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
+        tmem_st_wait();
+        // O_DONE completes once per P V product of this tile; every phase is
+        // consumed here, in order
+        if (j > 0) {
+          if (!wait_uniform(bar(L::kODone + u), co & 1, abort)) { ok = false; break; }
+          ++co;
+        }
+        if (any && j > 0) {
+          tc_fence_after();
+          #pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t o2[64];
+            tmem_ld32(tO + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
+            tmem_ld32(tO + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
+            tmem_ld_wait();
+            reg_fence(o2);
+            #pragma unroll
+            for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
+            tmem_st32(tO + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
+            tmem_st32(tO + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
+          }
+          tmem_st_wait();
+        }
         tc_fence_before();
         mbar_arrive(bar(L::kPFull + u));
-        continue;
       }
-      const int col0 = j * BC;
-      const bool need_mask =
-          (CAUSAL && col0 + BC - 1 > qt * 256 + 128 * u + p.off) || (col0 + BC > p.Nk);
-      uint32_t sr[BC];
-      #pragma unroll
-      for (int c = 0; c < BC / 32; ++c)
-        tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_ld_wait();
-      reg_fence(sr);
-      float* s = reinterpret_cast<float*>(sr);
-      if (need_mask) {
-        #pragma unroll
-        for (int i = 0; i < BC; ++i) {
-          const int col = col0 + i;
-          if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
-        }
-      }
-      float mpart[8];
-      #pragma unroll
-      for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmaxf(s[2 * uu], s[2 * uu + 1]);
-      #pragma unroll
-      for (int i = 16; i < BC; i += 16) {
-        #pragma unroll
-        for (int uu = 0; uu < 8; ++uu) mpart[uu] = fmax3(mpart[uu], s[i + 2 * uu], s[i + 2 * uu + 1]);
-      }
-      const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
-                             fmaxf(mpart[6], mpart[7]));
-      const float m_new = fmaxf(m_ref, mx * p.scale_log2);
-      const bool need = m_new > m_ref + kRescaleThreshold;
-      const bool any = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (any) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-        l *= alpha;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // weights written over S as 16 bits, 32 columns at a time; the exact
-      // sum l serves both L and the final division (rounding to nearest
-      // leaves the rounded weights' sum unbiased)
-      f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-      const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
-      #pragma unroll
-      for (int c = 0; c < BC / 32; ++c) {
-        uint32_t pk[16];
-        #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const f2 arg = ffma2(f2{s[32 * c + 2 * i], s[32 * c + 2 * i + 1]}, cs, cm);
-          const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
-          pk[i] = pack2<BF16>(pe.x, pe.y);
-          rs[i & 3] = fadd2(rs[i & 3], pe);
-        }
-        tmem_st16(tS + 16 * c, pk);
-      }
-      const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
-      l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
-      tmem_st_wait();
-      if (j > 0 && !wait_uniform(bar(L::kODone + u), (j - 1) & 1, abort)) { ok = false; break; }
-      if (any && j > 0) {
-        tc_fence_after();
-        #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t o2[64];
-          tmem_ld32(tO + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
-          tmem_ld32(tO + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
-          tmem_ld_wait();
-          reg_fence(o2);
-          #pragma unroll
-          for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
-          tmem_st32(tO + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
-          tmem_st32(tO + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::kPFull + u));
-    }
-    // ------------------------------------------------------------ epilogue
-    const bool in_range = row < p.Nq;
-    const size_t lrow = (static_cast<size_t>(b) * p.H + h) * p.Nq + (in_range ? row : 0);
-    uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
-                                           h * p.o_sh + (in_range ? row : 0) * p.o_sn);
-    if (ok && nk == 0) {
-      // no row of this tile sees any key: O = 0, L = -inf
-      if (in_range) {
-        #pragma unroll
-        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
-        p.lse[lrow] = -INFINITY;
-      }
-    } else if (ok && wait_uniform(bar(L::kODone + u), (nk - 1) & 1, abort)) {
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-      #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o1[32];
-        tmem_ld32(tO + 32 * c, o1);
-        tmem_ld_wait();
-        reg_fence(o1);
-        uint32_t w[16];
-        #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l, __uint_as_float(o1[2 * i + 1]) * inv_l);
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      const bool in_range = row < p.Nq;
+      const Fwd2Unit w = fwd2_unit<CAUSAL>(p, x);   // recomputed: h and b
+      const size_t lrow = (static_cast<size_t>(w.b) * p.H + w.h) * p.Nq + (in_range ? row : 0);
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + w.b * p.o_sb +
+                                             w.h * p.o_sh + (in_range ? row : 0) * p.o_sn);
+      if (nk == 0) {
+        // no row of this tile sees any key: O = 0, L = -inf
         if (in_range) {
           #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[lrow] = -INFINITY;
         }
+      } else {
+        if (!wait_uniform(bar(L::kODone + u), co & 1, abort)) { ok = false; break; }
+        ++co;
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o1[32];
+          tmem_ld32(tO + 32 * c, o1);
+          tmem_ld_wait();
+          reg_fence(o1);
+          uint32_t wv[16];
+          #pragma unroll
+          for (int i = 0; i < 16; ++i)
+            wv[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l,
+                                __uint_as_float(o1[2 * i + 1]) * inv_l);
+          if (in_range) {
+            #pragma unroll
+            for (int i = 0; i < 4; ++i)
+              orow[c * 4 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+          }
+        }
+        if (in_range) p.lse[lrow] = lse;
+        // O of this tile has been read out: the next P V may overwrite it
+        tc_fence_before();
+        mbar_arrive(bar(L::kOFree + u));
       }
-      if (in_range) p.lse[lrow] = lse;
     }
   }
 
@@ -855,9 +968,14 @@ cudaError_t launch_fwd2(const Problem& pr, const FwdArgs& a, cudaStream_t stream
   if ((e = make_tmap_4d(&tv, a.v, 128, pr.Nk, pr.Hkv, pr.B, a.vs, 64, 128)) != cudaSuccess) return e;
   auto kern = fwd2_kernel<CAUSAL, BF16>;
   static bool attr_set = false;
+  static int n_sms = 0;
   if (!attr_set) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
     attr_set = true;
   }
   FwdParams p = {};
@@ -866,6 +984,7 @@ cudaError_t launch_fwd2(const Problem& pr, const FwdArgs& a, cudaStream_t stream
   p.H = pr.H;
   p.Hkv = pr.Hkv;
   p.G = pr.H / pr.Hkv;
+  p.B_ = pr.B;
   p.Nq = pr.Nq;
   p.Nk = pr.Nk;
   p.off = pr.Nk - pr.Nq;
@@ -877,7 +996,15 @@ cudaError_t launch_fwd2(const Problem& pr, const FwdArgs& a, cudaStream_t stream
   p.o_sh = a.os.h;
   p.o_sn = a.os.n;
   p.err = pr.err;
-  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  // causal order: sections of (batch, head) pairs whose K and V (2 Nk d
+  // 16-bit values per KV head) take about 64 MB of L2 together
+  {
+    const long long kv_head = 4ll * pr.Nk * 128;
+    const long long kv_heads = std::max<long long>(1, (64ll << 20) / kv_head);
+    p.sec_heads = static_cast<int>(std::min<long long>(kv_heads * p.G, 1ll * pr.H * pr.B));
+  }
+  const long long n_units = static_cast<long long>(p.num_q_tiles) * pr.H * pr.B;
+  dim3 grid(static_cast<unsigned>(std::min<long long>(n_units, std::max(n_sms, 1))), 1, 1);
   const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kFwd2Threads, L::kAlloc, stream>>>(tq, tk, tv, p);
   timing_end(slot, stream);

@@ -127,3 +127,50 @@ def test_forward_full_size_sampled(name):
         got_o = torch.stack([o[b, kh * G + g, i] for g, i in rows])
         got_l = torch.stack([lse[b, kh * G + g, i] for g, i in rows])
         check_forward(got_o, got_l, o_ref, lse_ref, f"{name} rows b{b} kh{kh}")
+
+
+# (B, H, Hkv, Nq, Nk, causal): several 256-row units per CTA (300 units), and
+# with Nk = 40000 (20 MB of K and V per KV head) causal (batch, head) pairs
+# split over two sections of the longest-first order
+PERSISTENT = [(3, 20, 5, 1100, 1100, False), (3, 20, 5, 1100, 1100, True),
+              (1, 8, 4, 700, 40000, True), (2, 8, 2, 1500, 1300, True)]
+
+
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk,causal", PERSISTENT)
+def test_forward_every_unit_sampled(B, H, Hkv, Nq, Nk, causal):
+    """The two-query-tile forward walks (batch, head, 256-row block) units in
+    a persistent loop: rows from every unit (first, last and random rows of
+    both 128-row tiles) against the oracle, plus one whole group."""
+    w = Workload("units", B, H, Hkv, Nq, 128, "bf16", causal, 31 + Nq + Nk + B)
+    q, k, v, _ = make_inputs(w, Nk=Nk)
+    o, lse = binding.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal, w.scale)
+    binding.device_status()
+    o, lse = o.cpu(), lse.cpu()
+    G = H // Hkv
+    rng = np.random.default_rng(B * 1000 + Nq)
+
+    def check(got_o, got_l, o_ref, lse_ref, what):
+        # rows that see no key (Nq > Nk under the mask): O = 0 and L = -inf
+        got_l, lse_ref = got_l.double().numpy().copy(), np.asarray(lse_ref).copy()
+        empty = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(got_l), empty), what
+        assert torch.all(got_o[torch.from_numpy(empty)] == 0), what
+        got_l[empty] = 0.0
+        lse_ref[empty] = 0.0
+        check_forward(got_o, got_l, o_ref, lse_ref, what)
+
+    if Nk <= 2000:
+        o_ref, lse_ref = oracle.forward_group(q[0, :G], k[0, 0], v[0, 0], causal, w.scale)
+        check(o[0, :G], lse[0, :G], o_ref, lse_ref, "units whole group b0 kh0")
+    for b in range(B):
+        for kh in range(Hkv):
+            rows = []
+            for g in range(G):
+                for start in range(0, Nq, 128):
+                    end = min(start + 128, Nq)
+                    rows += [(g, start), (g, end - 1), (g, int(rng.integers(start, end)))]
+            o_ref, lse_ref = oracle.forward_rows(q[b, kh * G:(kh + 1) * G], k[b, kh], v[b, kh],
+                                                 rows, causal, w.scale)
+            got_o = torch.stack([o[b, kh * G + g, i] for g, i in rows])
+            got_l = torch.stack([lse[b, kh * G + g, i] for g, i in rows])
+            check(got_o, got_l, o_ref, lse_ref, f"units b{b} kh{kh} {Nq}x{Nk}")
