@@ -40,12 +40,20 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "gqa8k"
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_fwd_kernel.cuh",
-                  "exact_io_aware_20_gb300/csrc/fa_bwd_kernel.cuh",
-                  "exact_io_aware_20_gb300/csrc/fa_bwd_dq_kernel.cuh",
-                  "exact_io_aware_20_gb300/csrc/fa_api.cu",
-                  "exact_io_aware_20_gb300/csrc/block_list.cuh",
-                  "exact_io_aware_20_gb300/csrc/sm103_ptx.cuh"]
+# Sources each timed kernel is built from: a recorded DRAM-traffic figure is
+# used only while these files are unchanged.
+_COMMON_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_api.cu",
+                   "exact_io_aware_20_gb300/csrc/fa_internal.h",
+                   "exact_io_aware_20_gb300/csrc/block_list.cuh",
+                   "exact_io_aware_20_gb300/csrc/sm103_ptx.cuh"]
+KERNEL_SOURCES = {
+    "fwd": ["exact_io_aware_20_gb300/csrc/fa_fwd_kernel.cuh",
+            "exact_io_aware_20_gb300/csrc/fa_fwd.cu"] + _COMMON_SOURCES,
+    "bwd_main": ["exact_io_aware_20_gb300/csrc/fa_bwd_kernel.cuh",
+                 "exact_io_aware_20_gb300/csrc/fa_bwd.cu"] + _COMMON_SOURCES,
+    "bwd_dq": ["exact_io_aware_20_gb300/csrc/fa_bwd_dq_kernel.cuh",
+               "exact_io_aware_20_gb300/csrc/fa_bwd_dq.cu"] + _COMMON_SOURCES,
+}
 
 
 def parse_args():
@@ -88,9 +96,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kind: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -101,7 +109,9 @@ def recorded_traffic(kind: str, workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    if kind not in KERNEL_SOURCES:
+        return None
+    src = kernel_source_hash(kind)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kind and \

@@ -519,8 +519,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 // The row sums are formed on the ALU (no room for the ones columns), and O
 // is divided by the exact sum of the weights.
 //
-// Persistent: one CTA per SM walks a list of units in which (under the
-// mask) the longest come first, taking one unit of every round of gridDim.x
+// Persistent: one CTA per SM walks a list of units ordered by length under
+// the mask (see fwd2_unit), taking one unit of every round of gridDim.x
 // (forwards and backwards in turn, see fwd2_unit_index).  TMEM,
 // barriers and the K/V ring live across units (phase counters continue), the
 // next unit's scores start while the previous unit's epilogue drains O, and
@@ -556,14 +556,18 @@ __device__ __forceinline__ Fwd2Unit fwd2_unit(const FwdParams& p, int x) {
   Fwd2Unit w;
   int bh;
   if (CAUSAL) {
-    // (batch, head) pairs in sections whose K / V fit in L2 together; in a
-    // section the longest 256-row blocks come first, then the next ones, the
-    // section's heads innermost
+    // (batch, head) pairs in sections whose K / V fit in L2 together, the
+    // section's heads innermost.  The last section walks its 256-row blocks
+    // longest first, the one before shortest first, and so on: unit lengths
+    // along the list rise and fall without jumps and end with the shortest,
+    // which keeps the round assignment balanced.
     const int hb = p.H * p.B_;
+    const int n_sec = (hb + p.sec_heads - 1) / p.sec_heads;
     const int per_sec = p.sec_heads * p.num_q_tiles;
     const int sec = x / per_sec, r = x - sec * per_sec;
     const int width = min(p.sec_heads, hb - sec * p.sec_heads);
-    w.blk = p.num_q_tiles - 1 - r / width;
+    const int k = r / width;
+    w.blk = ((n_sec - 1 - sec) & 1) ? k : p.num_q_tiles - 1 - k;
     bh = sec * p.sec_heads + r % width;
   } else {
     // consecutive units are consecutive blocks of one head (shared K / V)
