@@ -1047,52 +1047,60 @@ __device__ __forceinline__ long long view_offset(size_t row, int H, int N, const
   return static_cast<long long>(bh / H) * s.b + static_cast<long long>(bh % H) * s.h + i * s.n;
 }
 
-// D_i = dO_i . O_i (fp32) and a zeroed dQ accumulator row, one warp per row
-// (delta and the accumulator are contiguous; o and dout strided).
+// D_i = dO_i . O_i (fp32) and a zeroed dQ accumulator row (delta and the
+// accumulator are contiguous; o and dout strided).  HBM-bound: D / 8 lanes
+// per row read 16 bytes of each tensor, a warp covers 256 / D rows per pass
+// and makes kPasses passes with every load issued before the first sum, so
+// that enough bytes are in flight to keep HBM busy.
+constexpr int kPrePasses = 4;
+constexpr int kPreWarps = 8;
+template <int D>
+__host__ __device__ constexpr int pre_rows_per_block() { return kPreWarps * (256 / D) * kPrePasses; }
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPreWarps * 32)
 bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                float* __restrict__ delta, float* __restrict__ dq_acc, size_t rows, int H, int N,
                Strides os, Strides dos) {
-  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;   // elements per lane: 2, 4 or 8
-  const uint16_t* orow = o + view_offset(row, H, N, os) + lane * kPer;
-  const uint16_t* drow = dout + view_offset(row, H, N, dos) + lane * kPer;
-  uint32_t ow[kPer / 2], dw[kPer / 2];
-  if constexpr (kPer == 2) {
-    ow[0] = *reinterpret_cast<const uint32_t*>(orow);
-    dw[0] = *reinterpret_cast<const uint32_t*>(drow);
-  } else if constexpr (kPer == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(orow), c = *reinterpret_cast<const uint2*>(drow);
-    ow[0] = a.x; ow[1] = a.y; dw[0] = c.x; dw[1] = c.y;
-  } else {
-    const uint4 a = *reinterpret_cast<const uint4*>(orow), c = *reinterpret_cast<const uint4*>(drow);
-    ow[0] = a.x; ow[1] = a.y; ow[2] = a.z; ow[3] = a.w;
-    dw[0] = c.x; dw[1] = c.y; dw[2] = c.z; dw[3] = c.w;
-  }
-  float acc = 0.f;
+  constexpr int kLanes = D / 8;                  // lanes per row
+  constexpr int kRowsPerPass = 32 / kLanes;      // rows of one warp per pass
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / kLanes, col = (lane % kLanes) * 8;
+  const size_t row0 = static_cast<size_t>(blockIdx.x) * pre_rows_per_block<D>() +
+                      static_cast<size_t>(warp) * kRowsPerPass * kPrePasses + sub;
+  uint4 ov[kPrePasses], dv[kPrePasses];
   #pragma unroll
-  for (int i = 0; i < kPer / 2; ++i) {
-    float2 a, c;
-    if constexpr (BF16) {
-      a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
-      c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[i]));
-    } else {
-      a = __half22float2(*reinterpret_cast<const __half2*>(&ow[i]));
-      c = __half22float2(*reinterpret_cast<const __half2*>(&dw[i]));
+  for (int u = 0; u < kPrePasses; ++u) {
+    const size_t row = row0 + static_cast<size_t>(u) * kRowsPerPass;
+    ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows) {
+      ov[u] = *reinterpret_cast<const uint4*>(o + view_offset(row, H, N, os) + col);
+      dv[u] = *reinterpret_cast<const uint4*>(dout + view_offset(row, H, N, dos) + col);
     }
-    acc = fmaf(a.x, c.x, acc);
-    acc = fmaf(a.y, c.y, acc);
   }
   #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) delta[row] = acc;
-  if (dq_acc == nullptr) return;
-  float* arow = dq_acc + row * D + lane * kPer;
-  #pragma unroll
-  for (int i = 0; i < kPer; i += 2) *reinterpret_cast<float2*>(arow + i) = make_float2(0.f, 0.f);
+  for (int u = 0; u < kPrePasses; ++u) {
+    const size_t row = row0 + static_cast<size_t>(u) * kRowsPerPass;
+    float acc = 0.f;
+    const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+    const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = unpack2<BF16>(ow[i]), c = unpack2<BF16>(dw[i]);
+      acc = fmaf(a.x, c.x, acc);
+      acc = fmaf(a.y, c.y, acc);
+    }
+    #pragma unroll
+    for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows) {
+      if (lane % kLanes == 0) delta[row] = acc;
+      if (dq_acc != nullptr) {
+        float4* arow = reinterpret_cast<float4*>(dq_acc + row * D + col);
+        arow[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        arow[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
 }
 
 // dq = scale * dq_acc (contiguous), converted to the output dtype and
@@ -1124,7 +1132,9 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
   // 1. preprocess
   int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
-  bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  constexpr int kPreRows = pre_rows_per_block<D>();
+  bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + kPreRows - 1) / kPreRows),
+                            kPreWarps * 32, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
       a.deterministic ? nullptr : a.dq_acc, rows, pr.H, pr.Nq, a.os, a.dos);
   timing_end(slot, stream);
