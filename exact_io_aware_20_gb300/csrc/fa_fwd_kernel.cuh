@@ -162,6 +162,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     return sparse ? static_cast<int>(tile_list[j]) : j_base + j;
   };
 
+  // the merge of split partials (launched as this grid's dependent) may start
+  // its launch now; it waits for this grid's completion before reading
+  if (p.splits > 1) grid_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
     for (int s = 0; s < KST; ++s) {
@@ -429,14 +432,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         p.lse_part[split * rows_total + r] = -INFINITY;
       }
     } else if (ok && n_kv == 0) {
-      // no row of this tile sees any key: O = 0, L = -inf
+      // no row of this tile sees any key (of this split's range): O = 0,
+      // L = -inf, as the final result or as this split's partial
       if (row < p.Nq) {
         const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
-                                               h * p.o_sh + row * p.o_sn);
-        #pragma unroll
-        for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
-        p.lse[r] = -INFINITY;
+        if (p.splits > 1) {
+          const size_t rp = split * (static_cast<size_t>(gridDim.z) * p.H * p.Nq) + r;
+          float4* prow = reinterpret_cast<float4*>(p.o_part + rp * D);
+          #pragma unroll
+          for (int i = 0; i < D / 4; ++i) prow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.lse_part[rp] = -INFINITY;
+        } else {
+          uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
+                                                 h * p.o_sh + row * p.o_sn);
+          #pragma unroll
+          for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[r] = -INFINITY;
+        }
       }
     } else if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
       tc_fence_after();
@@ -1017,18 +1029,26 @@ cudaError_t launch_fwd2(const Problem& pr, const FwdArgs& a, cudaStream_t stream
 
 // Merge the per-split partial results of one query row: with L_s the split
 // logsumexps, L = ln sum_s exp(L_s) and O = sum_s exp(L_s - L) O_s.  One warp
-// per row.  A row no split has a key for gets O = 0, L = -inf.
+// per row: lane s holds split s's weight, and the partial rows of up to 8
+// splits are loaded before they are summed (a split without keys for the row
+// left O_s = 0 and L_s = -inf, weight 0).  Launched as the split kernel's
+// programmatic dependent: it waits for the partials here.  A row no split
+// has a key for gets O = 0, L = -inf.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 fwd_combine_splits(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                    uint16_t* __restrict__ o, float* __restrict__ lse, size_t rows, int splits,
                    int H, int Nq, Strides os) {
+  grid_dependency_wait();
   const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   constexpr int kPer = D / 32;
   float m = -INFINITY;
-  for (int sp = 0; sp < splits; ++sp) m = fmaxf(m, lse_part[sp * rows + row]);
+  for (int s0 = 0; s0 < splits; s0 += 32)
+    if (s0 + lane < splits) m = fmaxf(m, lse_part[(s0 + lane) * rows + row]);
+  #pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   // row = (b * H + h) * Nq + i of the output view
   const size_t bh = row / Nq;
   const long long i = static_cast<long long>(row - bh * Nq);
@@ -1044,15 +1064,32 @@ fwd_combine_splits(const float* __restrict__ o_part, const float* __restrict__ l
   #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
   float sum = 0.f;
-  for (int sp = 0; sp < splits; ++sp) {
-    const float ls = lse_part[sp * rows + row];
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - m);
-    sum += w;
-    const float* src = o_part + (sp * rows + row) * D + lane * kPer;
-    #pragma unroll
-    for (int i = 0; i < kPer; ++i) acc[i] = fmaf(w, src[i], acc[i]);
+  for (int s0 = 0; s0 < splits; s0 += 32) {
+    const int n = min(32, splits - s0);
+    const float ls = lane < n ? lse_part[(s0 + lane) * rows + row] : -INFINITY;
+    const float wl = ls == -INFINITY ? 0.f : expf(ls - m);
+    sum += wl;
+    #pragma unroll 8
+    for (int k = 0; k < n; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wl, k);
+      const float* src = o_part + ((s0 + k) * rows + row) * D + lane * kPer;
+      float x[kPer];
+      if constexpr (kPer == 2) {
+        const float2 t = *reinterpret_cast<const float2*>(src);
+        x[0] = t.x; x[1] = t.y;
+      } else {
+        #pragma unroll
+        for (int c = 0; c < kPer; c += 4) {
+          const float4 t = *reinterpret_cast<const float4*>(src + c);
+          x[c] = t.x; x[c + 1] = t.y; x[c + 2] = t.z; x[c + 3] = t.w;
+        }
+      }
+      #pragma unroll
+      for (int c = 0; c < kPer; ++c) acc[c] = fmaf(w, x[c], acc[c]);
+    }
   }
+  #pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   const float inv = 1.f / sum;
   #pragma unroll
   for (int i = 0; i < kPer; i += 2)
@@ -1120,11 +1157,22 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (!SPARSE && p.splits > 1) {
+    // the merge is the split kernel's programmatic dependent: its launch and
+    // first instructions overlap the split kernel's last CTAs
     const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
-    fwd_combine_splits<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        a.o_part, a.lse_part, static_cast<uint16_t*>(a.o), a.lse, rows, p.splits, pr.H, pr.Nq,
-        a.os);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fwd_combine_splits<D, BF16>, static_cast<const float*>(a.o_part),
+                           static_cast<const float*>(a.lse_part), static_cast<uint16_t*>(a.o),
+                           a.lse, rows, p.splits, pr.H, pr.Nq, a.os);
   }
   return e;
 }

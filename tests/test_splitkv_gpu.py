@@ -51,3 +51,21 @@ def test_packed_short_query_and_split_agree(Nq, Nk):
     _check(o1, l1, q, k, v, True, w.scale, "packed fa_fwd_qk")
     assert (o1.float() - o2.float()).abs().max().item() < 4e-3
     assert (l1 - l2).abs().max().item() < 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Nq,Nk", [(1000, 1000), (1000, 300), (700, 2000)])
+def test_splitkv_splits_without_keys(d, Nq, Nk):
+    """Causal with many query rows: the first query tiles see only the first
+    key tiles, so the later splits hold no key for them.  Those splits' partials
+    must carry weight 0 in the merge; the workspace starts filled with a finite
+    non-zero pattern so that an unwritten partial would show."""
+    w = Workload("split-empty", 1, 4, 2, Nq, d, "bf16", True, 41 + Nq + Nk + d)
+    q, k, v, _ = make_inputs(w, Nk=Nk)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for splits in (3, 8):
+        need = int(binding.load().fa_fwd_splitkv_workspace_size(1, 4, 2, Nq, Nk, d, splits))
+        ws = torch.full((max(need, 256),), 0x3F, dtype=torch.uint8, device=DEV)
+        o, lse = binding.forward_splitkv(qd, kd, vd, True, w.scale, splits, workspace=ws)
+        binding.device_status()
+        _check(o, lse, q, k, v, True, w.scale, f"splitkv{splits} empty splits d{d} {Nq}x{Nk}")
