@@ -906,12 +906,19 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tmem_ld32(tS + lane_off + 64 * half + c0, sr);
         tmem_ld_wait();
         reg_fence(sr);
+        // L and D come from shared memory as 16-byte broadcasts (a quarter
+        // of the shared-memory wavefronts of scalar loads)
         #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs,
-                               f2{sL[c0 + c], sL[c0 + c + 1]});
-          P[c0 + c] = ex2_approx(arg.x);
-          P[c0 + c + 1] = ex2_approx(arg.y);
+        for (int c = 0; c < 32; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sL + c0 + c);
+          const f2 a0 = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs,
+                              f2{l4.x, l4.y});
+          const f2 a1 = ffma2(f2{__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])}, cs,
+                              f2{l4.z, l4.w});
+          P[c0 + c] = ex2_approx(a0.x);
+          P[c0 + c + 1] = ex2_approx(a0.y);
+          P[c0 + c + 2] = ex2_approx(a1.x);
+          P[c0 + c + 3] = ex2_approx(a1.y);
         }
         if (masked) {
           #pragma unroll
@@ -940,11 +947,16 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         reg_fence(dr);
         uint32_t w[8];
         #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const f2 diff = fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])},
-                                f2{sD[c0 + 2 * c], sD[c0 + 2 * c + 1]});
-          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]}, diff);
-          w[c] = pack2<BF16>(ds.x, ds.y);
+        for (int c = 0; c < 8; c += 2) {
+          const float4 d4 = *reinterpret_cast<const float4*>(sD + c0 + 2 * c);
+          const f2 diff0 = fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])},
+                                 f2{d4.x, d4.y});
+          const f2 diff1 = fadd2(f2{__uint_as_float(dr[2 * c + 2]), __uint_as_float(dr[2 * c + 3])},
+                                 f2{d4.z, d4.w});
+          const f2 ds0 = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]}, diff0);
+          const f2 ds1 = fmul2(f2{P[c0 + 2 * c + 2], P[c0 + 2 * c + 3]}, diff1);
+          w[c] = pack2<BF16>(ds0.x, ds0.y);
+          w[c + 1] = pack2<BF16>(ds1.x, ds1.y);
         }
         #pragma unroll
         for (int u2 = 0; u2 < 2; ++u2) {
