@@ -609,18 +609,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
 constexpr int kB128Threads = 448;
 
+// DS_SMEM: dS^T is written to shared memory (the operand of the dQ^T
+// product, which reads it as B); otherwise dS^T (16-bit) goes to TMEM over the
+// dP^T columns it was formed from, where dK reads it as the A operand, and
+// its shared-memory tile becomes a third Q stage.
+template <bool DS_SMEM>
 struct B128Layout {
   static constexpr int kTile = 128 * 128 * 2;      // one 128 x 128 16-bit tile
+  static constexpr int kQStages = DS_SMEM ? 2 : 3;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTile;
-  static constexpr int kQOff = 2 * kTile;          // two stages
-  static constexpr int kDOOff = 4 * kTile;         // one stage
-  static constexpr int kDSOff = 5 * kTile;         // dS^T [keys][q]
-  static constexpr int kLDOff = 6 * kTile;         // 8 warps x 2 bufs x {-L*log2e, -D} x 64
+  static constexpr int kQOff = 2 * kTile;          // kQStages stages
+  static constexpr int kDOOff = (2 + kQStages) * kTile;   // one stage
+  static constexpr int kDSOff = kDOOff + kTile;    // dS^T [keys][q] (DS_SMEM only)
+  static constexpr int kLDOff = kDOOff + (DS_SMEM ? 2 : 1) * kTile;  // 8 warps x 2 bufs x {-L*log2e, -D} x 64
   static constexpr int kBarOff = kLDOff + 8 * 2 * 2 * 64 * 4;
-  static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 3, kDOFull = 5, kDOEmpty = 6,
-                       kSFull = 7, kDPFull = 8, kPFull = 9, kDSFull = 10, kDSEmpty = 11,
-                       kDQFull = 12, kDQEmpty = 13, kFinal = 14, kDrain = 15, kNumBars = 16;
+  static constexpr int kKVFull = 0, kQFull = 1, kQEmpty = 4, kDOFull = 7, kDOEmpty = 8,
+                       kSFull = 9, kDPFull = 10, kPFull = 11, kDSFull = 12, kDSEmpty = 13,
+                       kDQFull = 14, kDQEmpty = 15, kFinal = 16, kDrain = 17, kNumBars = 18;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kListCap = 8192;            // (head, query tile) steps under a mask
   static constexpr int kListOff = kMiscOff + 16;
@@ -636,8 +642,10 @@ __global__ void __launch_bounds__(kB128Threads, 1)
 bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const BwdParams p) {
-  using L = B128Layout;
-  constexpr int D = 128, BR = 128;
+  // dense: no dQ product here (the query-outer kernel forms dQ), dS^T in TMEM
+  constexpr bool kDsSmem = SPARSE;
+  using L = B128Layout<kDsSmem>;
+  constexpr int D = 128, BR = 128, QS = L::kQStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -697,7 +705,7 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kKVFull), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QS; ++s) {
       mbar_init(bar(L::kQFull + s), 1);
       mbar_init(bar(L::kQEmpty + s), 1);
     }
@@ -744,8 +752,8 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __syncwarp();
     int q_issued = 0, do_issued = 0;
     for (int t = 0; t < n_steps; ++t) {
-      const int s = t & 1;
-      if (t >= 2 && !wait_uniform(bar(L::kQEmpty + s), ((t >> 1) + 1) & 1, abort)) break;
+      const int s = t % QS;
+      if (t >= QS && !wait_uniform(bar(L::kQEmpty + s), ((t / QS) + 1) & 1, abort)) break;
       int h, q0;
       step_hq(t, h, q0);
       if (elect_one()) {
@@ -768,8 +776,8 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ++do_issued;
     }
     drain_wait(bar(L::kKVFull), 0);
-    for (int t = max(0, q_issued - 2); t < q_issued; ++t)
-      drain_wait(bar(L::kQFull + (t & 1)), (t >> 1) & 1);
+    for (int t = max(0, q_issued - QS); t < q_issued; ++t)
+      drain_wait(bar(L::kQFull + t % QS), (t / QS) & 1);
     if (do_issued > 0) drain_wait(bar(L::kDOFull), (do_issued - 1) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -787,9 +795,9 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint64_t ds_mn = smem_desc_sw128(sbase + L::kDSOff, kBC * 128, 1024);
     // S^T_t = K Q_t^T into the S columns
     auto issue_s = [&](int t) -> bool {
-      if (!wait_uniform(bar(L::kQFull + (t & 1)), (t >> 1) & 1, abort)) return false;
+      if (!wait_uniform(bar(L::kQFull + t % QS), (t / QS) & 1, abort)) return false;
       tc_fence_after();
-      const uint32_t qs = (t & 1) * L::kTile;
+      const uint32_t qs = (t % QS) * L::kTile;
       #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t c = kk >> 2, w = kk & 3;
@@ -815,7 +823,7 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     bool ok = wait_uniform(bar(L::kKVFull), 0, abort);
     if (ok && n_steps > 0) ok = issue_s(0) && issue_dp(0);
     for (int t = 0; ok && t < n_steps; ++t) {
-      const uint32_t qs = (t & 1) * L::kTile;
+      const uint32_t qs = (t % QS) * L::kTile;
       // dV += P^T dO: P^T (16-bit) sits in the first 32 columns of each
       // 64-column half of the S columns (one half per P / dS warp).
       if (!wait_uniform(bar(L::kPFull), t & 1, abort)) break;
@@ -828,23 +836,34 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (t + 1 < n_steps && !issue_s(t + 1)) break;
       if (!wait_uniform(bar(L::kDSFull), t & 1, abort)) break;
       tc_fence_after();
-      if (p.with_dq) {
-        // dQ^T = K^T dS^T over the dP columns (their dP^T has been read)
+      if constexpr (kDsSmem) {
+        if (p.with_dq) {
+          // dQ^T = K^T dS^T over the dP columns (their dP^T has been read)
+          #pragma unroll
+          for (int kk = 0; kk < kBC / 16; ++kk)
+            mma_ss(tdP, desc_add(k_mn, kk * 2048), desc_add(ds_mn, kk * 2048), kIdQ,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(bar(L::kDQFull));
+        }
+        // dK += dS^T Q
         #pragma unroll
-        for (int kk = 0; kk < kBC / 16; ++kk)
-          mma_ss(tdP, desc_add(k_mn, kk * 2048), desc_add(ds_mn, kk * 2048), kIdQ,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(bar(L::kDQFull));
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ss(tdK, desc_add(ds_kmaj, (kk >> 2) * (kBC * 128) + (kk & 3) * 32),
+                 desc_add(q_mn, qs + kk * 2048), kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
+      } else {
+        // dK += dS^T Q, dS^T (16-bit) from TMEM: the first 32 columns of each
+        // 64-column half of the dP columns, as P^T in the S columns
+        #pragma unroll
+        for (int kk = 0; kk < BR / 16; ++kk)
+          mma_ts(tdK, tdP + (kk >> 2) * 64 + (kk & 3) * 8, desc_add(q_mn, qs + kk * 2048), kIdKV,
+                 (t > 0 || kk > 0) ? 1u : 0u);
       }
-      // dK += dS^T Q
-      #pragma unroll
-      for (int kk = 0; kk < BR / 16; ++kk)
-        mma_ss(tdK, desc_add(ds_kmaj, (kk >> 2) * (kBC * 128) + (kk & 3) * 32),
-               desc_add(q_mn, qs + kk * 2048), kIdKV, (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(bar(L::kQEmpty + (t & 1)));
-      mma_commit(bar(L::kDSEmpty));
+      mma_commit(bar(L::kQEmpty + t % QS));
+      if constexpr (kDsSmem) mma_commit(bar(L::kDSEmpty));
       if (t + 1 < n_steps) {
-        if (p.with_dq && !wait_uniform(bar(L::kDQEmpty), t & 1, abort)) break;
+        if (kDsSmem && p.with_dq && !wait_uniform(bar(L::kDQEmpty), t & 1, abort)) break;
+        // in TMEM mode dP^T(t + 1) overwrites dS^T(t) after dK(t) has read it
+        // (products run in issue order)
         if (!issue_dp(t + 1)) break;
       }
     }
@@ -936,7 +955,10 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_arrive(bar(L::kPFull));
       // dS^T = P^T o (dP^T - D) into the swizzled dS^T tile (chunk = half)
       if (!wait_uniform(bar(L::kDPFull), t & 1, abort)) { ok = false; break; }
-      if (t > 0 && !wait_uniform(bar(L::kDSEmpty), (t - 1) & 1, abort)) { ok = false; break; }
+      if (kDsSmem && t > 0 && !wait_uniform(bar(L::kDSEmpty), (t - 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // 16 columns at a time: P (64 values) stays live across the loop
       #pragma unroll
@@ -958,16 +980,27 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           w[c] = pack2<BF16>(ds0.x, ds0.y);
           w[c + 1] = pack2<BF16>(ds1.x, ds1.y);
         }
-        #pragma unroll
-        for (int u2 = 0; u2 < 2; ++u2) {
-          const int u = c0 / 8 + u2;
-          uint4* dst = reinterpret_cast<uint4*>(smem + L::kDSOff + half * (kBC * 128) + r * 128 +
-                                                ((u ^ (r & 7)) * 16));
-          *dst = make_uint4(w[4 * u2], w[4 * u2 + 1], w[4 * u2 + 2], w[4 * u2 + 3]);
+        if constexpr (kDsSmem) {
+          #pragma unroll
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const int u = c0 / 8 + u2;
+            uint4* dst = reinterpret_cast<uint4*>(smem + L::kDSOff + half * (kBC * 128) +
+                                                  r * 128 + ((u ^ (r & 7)) * 16));
+            *dst = make_uint4(w[4 * u2], w[4 * u2 + 1], w[4 * u2 + 2], w[4 * u2 + 3]);
+          }
+        } else {
+          // 16 dS^T values packed into 8 TMEM columns, stored over dP^T
+          // columns [64 half + c0 / 2, + 8): already read (c0 / 2 + 8 <= c0 + 16)
+          tmem_st8(tdP + lane_off + 64 * half + c0 / 2, w);
         }
       }
-      tc_fence_before();
-      fence_proxy_async_smem();
+      if constexpr (kDsSmem) {
+        tc_fence_before();
+        fence_proxy_async_smem();
+      } else {
+        tmem_st_wait();
+        tc_fence_before();
+      }
       mbar_arrive(bar(L::kDSFull));
       if (t + 1 < n_steps) {
         store_ld(t + 1);
@@ -1138,7 +1171,7 @@ int g_num_sms = 0;
 // WIDE: the d = 128 kernel with 128-row steps (bwd128_kernel).
 template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16, bool SPARSE, bool WIDE = false>
 cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  using L = std::conditional_t<WIDE, B128Layout, BwdLayout<D, DH, BR, QST>>;
+  using L = std::conditional_t<WIDE, B128Layout<SPARSE>, BwdLayout<D, DH, BR, QST>>;
   static_assert(!WIDE || (D == 128 && DH == 128 && BR == 128), "wide kernel shape");
   cudaError_t e;
   const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
@@ -1189,6 +1222,8 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.scale_log2 = pr.scale * kLog2e;
   p.err = pr.err;
   p.with_dq = a.deterministic ? 0 : 1;
+  // the dense 128-row kernel forms dK and dV only (dS^T lives in TMEM)
+  if (WIDE && !SPARSE && p.with_dq) return cudaErrorInvalidValue;
   p.mask = a.mask;
   p.dks = a.dks;
   p.dvs = a.dvs;
@@ -1240,7 +1275,7 @@ cudaError_t dispatch_flags(const Problem& pr, const BwdArgs& a, cudaStream_t s) 
 // BR, Q / dO ring stages.
 // d = 128 runs bwd128_kernel (128 query rows per step, two Q stages).
 using Cfg64 = BwdLayout<64, 64, 128, 3>;
-using Cfg128 = B128Layout;
+using Cfg128 = B128Layout<true>;
 using Cfg256 = BwdLayout<256, 128, 64, 1>;
 
 template <bool SPARSE>
