@@ -410,8 +410,8 @@ struct Dq128Layout {
   static constexpr int kBarOff = (4 + KST) * kTile;
   static constexpr int kQDFull = 0, kKFull = 1, kKEmpty = kKFull + KST, kVFull = kKEmpty + KST,
                        kVEmpty = kVFull + 2, kSFull = kVEmpty + 2, kDPFull = kSFull + 2,
-                       kDSFull = kDPFull + 1, kDQDone = kDSFull + 1, kDrain = kDQDone + 1,
-                       kNumBars = kDrain + 1;
+                       kDSFull = kDPFull + 1, kDPRead = kDSFull + 1, kDQDone = kDPRead + 1,
+                       kDrain = kDQDone + 1, kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kListOff = kMiscOff + 16;
   static constexpr int kBytes = kListOff + kDqListCap * 2;
@@ -476,6 +476,7 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     mbar_init(bar(L::kDPFull), 1);
     mbar_init(bar(L::kDSFull), 256);
+    mbar_init(bar(L::kDPRead), 256);
     mbar_init(bar(L::kDQDone), 1);
     mbar_init(bar(L::kDrain), 1);
     *abort = 0;
@@ -579,11 +580,15 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int s = j & 1;
       // the other S buffer: its dS (tile j - 1) was read by dQ_{j-1}, issued earlier
       if (j + 1 < n_kv && !issue_s(j + 1)) break;
+      // dP_{j+1} as soon as the dS warps hold dP_j in registers, so it runs
+      // while they form dS_j
+      if (j + 1 < n_kv) {
+        if (!wait_uniform(bar(L::kDPRead), j & 1, abort)) break;
+        tc_fence_after();
+        if (!issue_dp(j + 1)) break;
+      }
       if (!wait_uniform(bar(L::kDSFull), j & 1, abort)) break;
       tc_fence_after();
-      // the dS warps have read dP_j: the next dP goes first, so they can
-      // start on it while dQ_j runs
-      if (j + 1 < n_kv && !issue_dp(j + 1)) break;
       // dQ += dS_j K_j: dS (16-bit) in the first 32 columns of each 64-column
       // half of S buffer s (one half per dS warp)
       const int sk = j % KST;
@@ -639,17 +644,23 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       if (!wait_uniform(bar(L::kDPFull), j & 1, abort)) { ok = false; break; }
       tc_fence_after();
+      // all 64 dP values of this half into registers, then release the dP
+      // columns for dP_{j+1}
+      uint32_t dr[64];
+      tmem_ld32(tdP + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(tdP + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_ld_wait();
+      reg_fence(dr);
+      tc_fence_before();
+      mbar_arrive(bar(L::kDPRead));
       #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t dr[32];
-        tmem_ld32(tdP + lane_off + 64 * half + c0, dr);
-        tmem_ld_wait();
-        reg_fence(dr);
         uint32_t w[16];
         #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]},
-                              fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])}, cd));
+                              fadd2(f2{__uint_as_float(dr[c0 + 2 * c]),
+                                       __uint_as_float(dr[c0 + 2 * c + 1])}, cd));
           w[c] = pack2<BF16>(ds.x, ds.y);
         }
         // dS (16-bit) over the first 32 columns of this half, already read
