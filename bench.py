@@ -605,6 +605,7 @@ def main():
         "fwd_tflops": round(w.flops_fwd() / (fwd_ms * 1e-3) / 1e12, 1),
         "bwd_tflops": round(w.flops_bwd() / (bwd_ms * 1e-3) / 1e12, 1),
         "kernels": kernels,
+        "exp_rate": exp_rate(w, fwd_ms, kernel_times),
         "roofline": roof,
         "e2e": {"value": round(world * flops_step / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
@@ -621,6 +622,28 @@ def main():
         line["cpu_baseline"] = cpu_baseline(base, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     return 0
+
+
+# exp2 throughput of the GPU used for the secondary (softmax) bound: 32
+# results per clock per SM (the rate at which ncu's XU-pipe utilisation of the
+# forward kernel matches its count of exponentials), 152 SMs, 2.07 GHz.
+EXP_PEAK = 32 * 152 * 2.07e9
+
+
+def exp_rate(w: Workload, fwd_ms: float, kernel_times) -> dict:
+    """Exponentials per second: one per unmasked score in the forward kernel;
+    in the backward the kernels that form P (the main kernel, and at d = 128
+    the query-outer dQ kernel, which forms it again)."""
+    scores = w.B * w.H * w.N * w.N / (2 if w.causal else 1)
+    out = {"peak_per_s": EXP_PEAK, "peak_source": "32/clk/SM x 152 SMs x 2.07 GHz (derived)",
+           "fwd_per_s": round(scores / (fwd_ms * 1e-3), 1)}
+    out["fwd_frac"] = round(out["fwd_per_s"] / EXP_PEAK, 4)
+    for kind in ("bwd_main", "bwd_dq"):
+        ms, n = kernel_times.get(kind, (0.0, 0))
+        if n:
+            out[kind + "_per_s"] = round(scores / (ms / n * 1e-3), 1)
+            out[kind + "_frac"] = round(out[kind + "_per_s"] / EXP_PEAK, 4)
+    return out
 
 
 def step_bytes(w: Workload) -> int:
