@@ -829,10 +829,6 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         ++cs;
         tc_fence_after();
         if (idle) {
-          if (j > 0) {
-            if (!wait_uniform(bar(L::kODone + u), co & 1, abort)) { ok = false; break; }
-            ++co;
-          }
           tc_fence_before();
           mbar_arrive(bar(L::kPFull + u));
           continue;
@@ -894,12 +890,10 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
         l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
         tmem_st_wait();
-        // O_DONE completes once per P V product of this tile; every phase is
-        // consumed here, in order
-        if (j > 0) {
-          if (!wait_uniform(bar(L::kODone + u), co & 1, abort)) { ok = false; break; }
-          ++co;
-        }
+        // O needs no wait before its rescale: S(j) was issued after P V(j-1)
+        // on this tile, and its S_FULL completes only once every earlier
+        // product has (tcgen05.commit tracks all of the issuing thread's prior
+        // products), so P V(j-1) is done and P V(j) waits for this P_FULL
         if (any && j > 0) {
           tc_fence_after();
           #pragma unroll
@@ -934,8 +928,11 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           p.lse[lrow] = -INFINITY;
         }
       } else {
-        if (!wait_uniform(bar(L::kODone + u), co & 1, abort)) { ok = false; break; }
-        ++co;
+        // O_DONE completes once per P V product of the tile and only the
+        // unit's last one is waited for: P V(nk-2) is done (see above), so
+        // the barrier is at that product's phase or one past it
+        co += nk;
+        if (!wait_uniform(bar(L::kODone + u), (co - 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;

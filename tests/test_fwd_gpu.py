@@ -76,6 +76,18 @@ def test_forward_large_scores_f16():
     check_forward(o.cpu(), lse.cpu(), o_ref, lse_ref, "wide scores f16")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_large_scores_two_tile_f16(causal):
+    """The d = 128 two-query-tile kernel under spread-out scores (scale 4,
+    values x3): its running-max rescale of O runs on many key tiles."""
+    w = Workload("wide", 2, 4, 2, 1100, 128, "f16", causal, 19, 3.0)
+    q, k, v, _ = make_inputs(w)
+    o, lse = binding.forward(q.to(DEV), k.to(DEV), v.to(DEV), causal, 4.0)
+    binding.device_status()
+    o_ref, lse_ref = oracle.forward(q, k, v, causal, 4.0)
+    check_forward(o.cpu(), lse.cpu(), o_ref, lse_ref, f"wide scores two-tile causal{causal}")
+
+
 def test_forward_large_scores_bf16():
     """Peaky softmax (scale 3, N(0,1) values) in bf16: the rescale path in bf16.
 
