@@ -769,7 +769,14 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       for (int j = 0; ok && j < w.n_max; ++j) {
         const int g = kt + j, s = g & 1;
         if (!wait_uniform(bar(L::kVFull + s), (g >> 1) & 1, abort)) { ok = false; break; }
-        bool k_ready = false;
+        // K(g + 1) (loaded a stage ahead) before the P waits, so that no wait
+        // sits between P V and the next scores
+        const bool k_ready = j + 1 < w.n_max;
+        if (k_ready &&
+            !wait_uniform(bar(L::kKFull + ((g + 1) & 1)), ((g + 1) >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
         #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (j >= w.n_kv[u]) continue;
@@ -783,14 +790,6 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                    desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(L::kODone + u));
           if (j + 1 < w.n_kv[u]) {
-            if (!k_ready) {
-              if (!wait_uniform(bar(L::kKFull + ((g + 1) & 1)), ((g + 1) >> 1) & 1, abort)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_ready = true;
-            }
             issue_s(u, (g + 1) & 1);
           }
         }
