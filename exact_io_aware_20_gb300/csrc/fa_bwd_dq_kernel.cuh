@@ -475,8 +475,8 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(bar(L::kSFull + s), 1);
     }
     mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kDSFull), 256);
-    mbar_init(bar(L::kDPRead), 256);
+    mbar_init(bar(L::kDSFull), 8);         // one arrival per dS warp
+    mbar_init(bar(L::kDPRead), 8);
     mbar_init(bar(L::kDQDone), 1);
     mbar_init(bar(L::kDrain), 1);
     *abort = 0;
@@ -652,7 +652,7 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_ld_wait();
       reg_fence(dr);
       tc_fence_before();
-      mbar_arrive(bar(L::kDPRead));
+      mbar_arrive_warp(bar(L::kDPRead));
       #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t w[16];
@@ -668,7 +668,7 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::kDSFull));
+      mbar_arrive_warp(bar(L::kDSFull));
     }
     // ------------------------------------------------------------ epilogue
     uint4* out = reinterpret_cast<uint4*>(p.dq + dq_off + 64 * half);

@@ -713,8 +713,8 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(bar(L::kDOEmpty), 1);
     mbar_init(bar(L::kSFull), 1);
     mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kPFull), 256);
-    mbar_init(bar(L::kDSFull), 256);
+    mbar_init(bar(L::kPFull), 8);          // one arrival per P / dS warp
+    mbar_init(bar(L::kDSFull), 8);
     mbar_init(bar(L::kDSEmpty), 1);
     mbar_init(bar(L::kDQFull), 1);
     mbar_init(bar(L::kDQEmpty), 128);
@@ -952,7 +952,7 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::kPFull));
+      mbar_arrive_warp(bar(L::kPFull));
       // dS^T = P^T o (dP^T - D) into the swizzled dS^T tile (chunk = half)
       if (!wait_uniform(bar(L::kDPFull), t & 1, abort)) { ok = false; break; }
       if (kDsSmem && t > 0 && !wait_uniform(bar(L::kDSEmpty), (t - 1) & 1, abort)) {
@@ -1001,7 +1001,7 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tmem_st_wait();
         tc_fence_before();
       }
-      mbar_arrive(bar(L::kDSFull));
+      mbar_arrive_warp(bar(L::kDSFull));
       if (t + 1 < n_steps) {
         store_ld(t + 1);
         __syncwarp();

@@ -639,7 +639,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
       mbar_init(bar(L::kVFull + s), 1);
       mbar_init(bar(L::kVEmpty + s), 1);
       mbar_init(bar(L::kSFull + s), 1);
-      mbar_init(bar(L::kPFull + s), 128);
+      mbar_init(bar(L::kPFull + s), 4);      // one arrival per softmax warp
       mbar_init(bar(L::kODone + s), 1);
       mbar_init(bar(L::kOFree + s), 128);
     }
@@ -829,7 +829,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tc_fence_after();
         if (idle) {
           tc_fence_before();
-          mbar_arrive(bar(L::kPFull + u));
+          mbar_arrive_warp(bar(L::kPFull + u));
           continue;
         }
         const int col0 = j * BC;
@@ -910,7 +910,7 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
           tmem_st_wait();
         }
         tc_fence_before();
-        mbar_arrive(bar(L::kPFull + u));
+        mbar_arrive_warp(bar(L::kPFull + u));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue

@@ -195,6 +195,16 @@ __device__ __forceinline__ uint32_t elect_one() {
   return pred;
 }
 
+// One arrival for a whole (converged) warp: every lane's earlier operations
+// (each lane fences its own tcgen05 or async-proxy work before the call) are
+// ordered before one elected lane's arrive by the warp barrier.  A barrier
+// taking these counts warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if (elect_one()) mbar_arrive(bar);
+  __syncwarp();
+}
+
 // Advance a shared-memory descriptor's start address by `bytes` (a multiple
 // of 16 that keeps the address inside the 256 KiB window).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
