@@ -315,7 +315,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (!wait_uniform(bar(L::kSFull + (j & 1)), (j >> 1) & 1, abort)) { ok = false; break; }
       tc_fence_after();
       if (idle) {
-        if (j > 0 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
+        if (j > 0 && j == n_kv - 1 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_before();
         mbar_arrive(bar(L::kPFull + (j & 1)));
         continue;
@@ -386,11 +389,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int c = 0; c < BC / 64; ++c)
         tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
       tmem_st_wait();
-      // O_DONE completes once per P V product; every phase is consumed here,
-      // in order, so a parity wait can never be confused by a skipped phase.
-      // PV_j cannot start before this thread arrives on P_FULL below, so the
-      // barrier is at most one phase ahead.
-      if (j > 0 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) { ok = false; break; }
+      // O_DONE completes once per P V product.  S(j) was issued after
+      // P V(j-2), and its S_FULL completes only once every earlier product of
+      // the issuing thread has, so here only P V(j-1) can be outstanding and
+      // the barrier is at P V(j-1)'s phase or one past it: a parity wait for
+      // it is exact even when earlier phases were not waited for.  It is
+      // needed before a rescale of O, and on the last tile (so that at the
+      // epilogue only the last product can be outstanding).
+      if (j > 0 && (any || j == n_kv - 1) &&
+          !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) {
+        ok = false;
+        break;
+      }
       if (any && j > 0) {
         // O holds P_0..P_{j-1} V, all complete: rescale it.
         tc_fence_after();
