@@ -635,11 +635,11 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           P[c0 + c + 1] = ex2_approx(arg.y);
         }
         if (masked) {
+          // columns [0, lim) of this chunk are kept (one comparison per score)
+          const int lim = min(p.Nk - col0 - c0, CAUSAL ? row + p.off - col0 - c0 + 1 : 32);
           #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = col0 + c0 + c;
-            if (col >= p.Nk || (CAUSAL && col > row + p.off)) P[c0 + c] = 0.f;
-          }
+          for (int c = 0; c < 32; ++c)
+            if (c >= lim) P[c0 + c] = 0.f;
         }
       }
       if (!wait_uniform(bar(L::kDPFull), j & 1, abort)) { ok = false; break; }

@@ -940,9 +940,12 @@ bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           P[c0 + c + 3] = ex2_approx(a1.y);
         }
         if (masked) {
+          // queries qc0 + c0 + c with c < z see no key kv (z = 32: the key is
+          // past Nk); one comparison per score
+          const int z = kv_out ? 32 : (diag ? min(32, kv - p.off - qc0 - c0) : 0);
           #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (kv_out || (diag && kv > qc0 + c0 + c + p.off)) P[c0 + c] = 0.f;
+            if (c < z) P[c0 + c] = 0.f;
         }
         uint32_t pk[16];
         #pragma unroll

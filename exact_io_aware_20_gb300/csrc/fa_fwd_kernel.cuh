@@ -334,11 +334,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int min_i = packed ? 0 : qt * kBR;
       const bool need_mask = (CAUSAL && col0 + BC - 1 > min_i + p.off) || (col0 + BC > p.Nk);
       if (need_mask) {
+        // columns [0, lim) of the tile are kept (one comparison per score)
+        const int lim = min(p.Nk - col0, CAUSAL ? qi + p.off - col0 + 1 : BC);
         #pragma unroll
-        for (int i = 0; i < BC; ++i) {
-          const int col = col0 + i;
-          if (col >= p.Nk || (CAUSAL && col > qi + p.off)) s[i] = -INFINITY;
-        }
+        for (int i = 0; i < BC; ++i)
+          if (i >= lim) s[i] = -INFINITY;
       }
       // Row max as a tree of three-input maxima (independent partial maxima
       // keep the single warp per sub-partition busy instead of waiting on a
@@ -853,11 +853,12 @@ fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         reg_fence(sr);
         float* s = reinterpret_cast<float*>(sr);
         if (need_mask) {
+          // columns [0, lim) of the tile are kept: key < Nk and (causal)
+          // key <= row + off, one comparison per score
+          const int lim = min(p.Nk - col0, CAUSAL ? row + p.off - col0 + 1 : BC);
           #pragma unroll
-          for (int i = 0; i < BC; ++i) {
-            const int col = col0 + i;
-            if (col >= p.Nk || (CAUSAL && col > row + p.off)) s[i] = -INFINITY;
-          }
+          for (int i = 0; i < BC; ++i)
+            if (i >= lim) s[i] = -INFINITY;
         }
         float mpart[8];
         #pragma unroll
