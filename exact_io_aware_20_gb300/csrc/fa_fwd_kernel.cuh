@@ -1027,6 +1027,7 @@ cudaError_t launch_fwd2(const Problem& pr, const FwdArgs& a, cudaStream_t stream
     p.sec_heads = static_cast<int>(std::min<long long>(kv_heads * p.G, 1ll * pr.H * pr.B));
   }
   const long long n_units = static_cast<long long>(p.num_q_tiles) * pr.H * pr.B;
+  if (n_units >= (1ll << 31)) return cudaErrorInvalidValue;   // unit indices are int
   dim3 grid(static_cast<unsigned>(std::min<long long>(n_units, std::max(n_sms, 1))), 1, 1);
   const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kFwd2Threads, L::kAlloc, stream>>>(tq, tk, tv, p);
