@@ -1,0 +1,191 @@
+"""A model of the persistent two-query-tile forward's barrier protocol,
+checked on random unit sequences and interleavings (no GPU).
+
+It follows the kernel's roles step by step: the TMA producer (Q per unit,
+K / V through two-stage rings), the MMA warp (P V(j) then S(j+1) per tile,
+commits), and the eight softmax warps (S_FULL wait, P_FULL arrival per warp,
+the rescale of O, the epilogue and O_FREE).  Tensor-core products and their
+commits go through one in-order queue, as on the hardware: a commit arrives
+on its barrier only once every product issued before it has completed.
+mbarriers are modelled with their phase/parity semantics.
+
+Checked: every run ends (no wait that can never complete: a protocol
+deadlock or a parity wait aliased by a skipped phase), and whenever a
+softmax warpgroup reads or rescales O (tile u), no P V product on that tile
+is still queued or running -- the property the kernel gets from S_FULL of
+tile j + 1 implying P V(j) has completed, instead of waiting for O_DONE on
+every tile."""
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count, self.pending, self.phase = count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, "more arrivals than the barrier's count"
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def done(self, parity):
+        return (self.phase & 1) != parity
+
+
+def unit_tiles(blk, nq, nk, causal):
+    out = []
+    for u in range(2):
+        first = blk * 256 + 128 * u
+        n = (nk + 127) // 128
+        if first >= nq:
+            n = 0
+        elif causal:
+            last_key = min(first + 128, nq) - 1 + nk - nq
+            n = 0 if last_key < 0 else min(n, last_key // 128 + 1)
+        out.append(n)
+    return out
+
+
+def run(units, seed):
+    rnd = random.Random(seed)
+    B = {n: Bar(1) for n in ("QFull", "QEmpty", "K0F", "K1F", "K0E", "K1E", "V0F", "V1F",
+                              "V0E", "V1E", "S0", "S1", "O0", "O1")}
+    for u in range(2):
+        B[f"P{u}"] = Bar(4)        # one arrival per softmax warp
+        B[f"OF{u}"] = Bar(4)
+    loads = []                     # TMA completions, any order
+    pipe = []                      # tensor-core queue: ("mma", tile) or ("commit", barrier)
+
+    def producer():
+        it = kt = 0
+        for w in units:
+            n_max = max(w)
+
+            def load_kv(j):
+                g = kt + j
+                s = g & 1
+                if g >= 2:
+                    while not B[f"K{s}E"].done(((g >> 1) + 1) & 1):
+                        yield
+                loads.append(f"K{s}F")
+                if g >= 2:
+                    while not B[f"V{s}E"].done(((g >> 1) + 1) & 1):
+                        yield
+                loads.append(f"V{s}F")
+            if n_max > 0:
+                yield from load_kv(0)
+            if it >= 1:
+                while not B["QEmpty"].done((it - 1) & 1):
+                    yield
+            loads.append("QFull")
+            for j in range(1, n_max):
+                yield from load_kv(j)
+            kt += n_max
+            it += 1
+
+    def mma():
+        it = kt = 0
+        cp = [0, 0]
+        of = [0, 0]
+        for w in units:
+            n_max = max(w)
+            while not B["QFull"].done(it & 1):
+                yield
+            if n_max > 0:
+                while not B[f"K{kt & 1}F"].done((kt >> 1) & 1):
+                    yield
+                for u in range(2):
+                    if w[u] > 0:
+                        pipe.append(("mma", None))
+                        pipe.append(("commit", f"S{u}"))
+                pipe.append(("commit", f"K{kt & 1}E"))
+            if n_max <= 1:
+                pipe.append(("commit", "QEmpty"))
+            for u in range(2):
+                if w[u] > 0 and of[u] > 0:
+                    while not B[f"OF{u}"].done((of[u] - 1) & 1):
+                        yield
+                of[u] += 1 if w[u] > 0 else 0
+            for j in range(n_max):
+                g = kt + j
+                s = g & 1
+                while not B[f"V{s}F"].done((g >> 1) & 1):
+                    yield
+                if j + 1 < n_max:
+                    while not B[f"K{(g + 1) & 1}F"].done(((g + 1) >> 1) & 1):
+                        yield
+                for u in range(2):
+                    if j >= w[u]:
+                        continue
+                    while not B[f"P{u}"].done(cp[u] & 1):
+                        yield
+                    cp[u] += 1
+                    pipe.append(("mma", u))            # P V_u(j) writes O_u
+                    pipe.append(("commit", f"O{u}"))
+                    if j + 1 < w[u]:
+                        pipe.append(("mma", None))     # S_u(j + 1)
+                        pipe.append(("commit", f"S{u}"))
+                pipe.append(("commit", f"V{s}E"))
+                if j + 1 < n_max:
+                    pipe.append(("commit", f"K{(g + 1) & 1}E"))
+                if j + 2 == n_max:
+                    pipe.append(("commit", "QEmpty"))
+            kt += n_max
+            it += 1
+
+    def o_busy(u):
+        return any(op == ("mma", u) for op in pipe)
+
+    def softmax(u):
+        cs = co = 0
+        for w in units:
+            nk = w[u]
+            for j in range(nk):
+                while not B[f"S{u}"].done(cs & 1):
+                    yield
+                cs += 1
+                yield
+                if j > 0 and rnd.random() < 0.3:           # a rescale of O
+                    assert not o_busy(u), "O rescaled while a P V on it is in flight"
+                B[f"P{u}"].arrive()
+            if nk > 0:
+                co += nk
+                while not B[f"O{u}"].done((co - 1) & 1):
+                    yield
+                assert not o_busy(u), "O read out while a P V on it is in flight"
+                yield
+                B[f"OF{u}"].arrive()
+
+    roles = [producer(), mma()] + [softmax(u) for u in range(2) for _ in range(4)]
+    alive = list(range(len(roles)))
+    for _ in range(2_000_000):
+        if not alive and not loads and not pipe:
+            return True
+        r = rnd.random()
+        if loads and (r < 0.2 or not alive):
+            B[loads.pop(rnd.randrange(len(loads)))].arrive()
+        elif pipe and (r < 0.45 or not alive):
+            op, arg = pipe.pop(0)                          # in-order completion
+            if op == "commit":
+                B[arg].arrive()
+        elif alive:
+            k = rnd.choice(alive)
+            try:
+                next(roles[k])
+            except StopIteration:
+                alive.remove(k)
+    return False
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_persistent_forward_protocol(seed):
+    rnd = random.Random(seed)
+    nq = rnd.choice([129, 300, 700, 1100, 1500])
+    nk = rnd.choice([nq, 64, 300, 1300])
+    causal = rnd.random() < 0.5
+    nqt = (nq + 255) // 256
+    units = [unit_tiles(rnd.randrange(nqt), nq, nk, causal) for _ in range(rnd.randint(1, 6))]
+    assert run(units, seed), f"protocol stalled: units {units}"
