@@ -410,7 +410,7 @@ struct Dq128Layout {
   static constexpr int kBarOff = (4 + KST) * kTile;
   static constexpr int kQDFull = 0, kKFull = 1, kKEmpty = kKFull + KST, kVFull = kKEmpty + KST,
                        kVEmpty = kVFull + 2, kSFull = kVEmpty + 2, kDPFull = kSFull + 2,
-                       kDSFull = kDPFull + 1, kDPRead = kDSFull + 1, kDQDone = kDPRead + 1,
+                       kDSFull = kDPFull + 1, kDPRead = kDSFull + 2, kDQDone = kDPRead + 1,
                        kDrain = kDQDone + 1, kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kListOff = kMiscOff + 16;
@@ -475,7 +475,11 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(bar(L::kSFull + s), 1);
     }
     mbar_init(bar(L::kDPFull), 1);
-    mbar_init(bar(L::kDSFull), 8);         // one arrival per dS warp
+    // one arrival per dS warp.  DS_FULL alternates between two barriers: a
+    // warp may arrive for tile j + 1 (its dP_{j+1} is issued once every warp
+    // has read dP_j) before a slower one has arrived for tile j
+    mbar_init(bar(L::kDSFull), 8);
+    mbar_init(bar(L::kDSFull + 1), 8);
     mbar_init(bar(L::kDPRead), 8);
     mbar_init(bar(L::kDQDone), 1);
     mbar_init(bar(L::kDrain), 1);
@@ -587,7 +591,7 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_after();
         if (!issue_dp(j + 1)) break;
       }
-      if (!wait_uniform(bar(L::kDSFull), j & 1, abort)) break;
+      if (!wait_uniform(bar(L::kDSFull + (j & 1)), (j >> 1) & 1, abort)) break;
       tc_fence_after();
       // dQ += dS_j K_j: dS (16-bit) in the first 32 columns of each 64-column
       // half of S buffer s (one half per dS warp)
@@ -668,7 +672,7 @@ bwd_dq128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive_warp(bar(L::kDSFull));
+      mbar_arrive_warp(bar(L::kDSFull + (j & 1)));
     }
     // ------------------------------------------------------------ epilogue
     uint4* out = reinterpret_cast<uint4*>(p.dq + dq_off + 64 * half);
