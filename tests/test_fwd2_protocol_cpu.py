@@ -189,3 +189,103 @@ def test_persistent_forward_protocol(seed):
     nqt = (nq + 255) // 256
     units = [unit_tiles(rnd.randrange(nqt), nq, nk, causal) for _ in range(rnd.randint(1, 6))]
     assert run(units, seed), f"protocol stalled: units {units}"
+
+
+def run_one_tile(n, kst, vst, seed):
+    """The one-tile forward (d = 64 / 256, short, split and block-sparse
+    paths): S(j+1) is issued before P V(j), into the other of two score
+    buffers, and the softmax waits for O_DONE only before a rescale of O and
+    on the last tile."""
+    rnd = random.Random(seed)
+    B = {"QFull": Bar(1), "ODone": Bar(1)}
+    for s in range(kst):
+        B[f"KF{s}"], B[f"KE{s}"] = Bar(1), Bar(1)
+    for s in range(vst):
+        B[f"VF{s}"], B[f"VE{s}"] = Bar(1), Bar(1)
+    for s in range(2):
+        B[f"SF{s}"] = Bar(1)
+        B[f"PF{s}"] = Bar(4)           # the model's four softmax warps
+    loads, pipe = [], []
+
+    def producer():
+        loads.append("QFull")
+        for j in range(n):
+            sk, sv = j % kst, j % vst
+            if j >= kst:
+                while not B[f"KE{sk}"].done(((j // kst) + 1) & 1):
+                    yield
+            loads.append(f"KF{sk}")
+            if j >= vst:
+                while not B[f"VE{sv}"].done(((j // vst) + 1) & 1):
+                    yield
+            loads.append(f"VF{sv}")
+
+    def mma():
+        def issue_s(j):
+            while not B[f"KF{j % kst}"].done((j // kst) & 1):
+                yield
+            pipe.append(("mma", f"S{j & 1}"))
+            pipe.append(("commit", f"SF{j & 1}"))
+            pipe.append(("commit", f"KE{j % kst}"))
+        while not B["QFull"].done(0):
+            yield
+        if n > 0:
+            yield from issue_s(0)
+        for j in range(n):
+            if j + 1 < n:
+                yield from issue_s(j + 1)
+            while not B[f"PF{j & 1}"].done((j >> 1) & 1):
+                yield
+            while not B[f"VF{j % vst}"].done((j // vst) & 1):
+                yield
+            pipe.append(("mma", f"S{j & 1}", "O"))       # P V(j): P from buffer j & 1
+            pipe.append(("commit", "ODone"))
+            pipe.append(("commit", f"VE{j % vst}"))
+
+    def busy(region):
+        return any(op[0] == "mma" and region in op[1:] for op in pipe)
+
+    def softmax():
+        for j in range(n):
+            while not B[f"SF{j & 1}"].done((j >> 1) & 1):
+                yield
+            assert not busy(f"S{j & 1}"), "score buffer read while a product uses it"
+            yield
+            rescale = j > 0 and rnd.random() < 0.3
+            if j > 0 and (rescale or j == n - 1):
+                while not B["ODone"].done((j - 1) & 1):
+                    yield
+            if rescale:
+                assert not busy("O"), "O rescaled while a P V is in flight"
+            B[f"PF{j & 1}"].arrive()
+        if n > 0:
+            while not B["ODone"].done((n - 1) & 1):
+                yield
+            assert not busy("O"), "O read out while a P V is in flight"
+
+    roles = [producer(), mma()] + [softmax() for _ in range(4)]
+    alive = list(range(len(roles)))
+    for _ in range(2_000_000):
+        if not alive and not loads and not pipe:
+            return True
+        r = rnd.random()
+        if loads and (r < 0.2 or not alive):
+            B[loads.pop(rnd.randrange(len(loads)))].arrive()
+        elif pipe and (r < 0.45 or not alive):
+            op = pipe.pop(0)
+            if op[0] == "commit":
+                B[op[1]].arrive()
+        elif alive:
+            k = rnd.choice(alive)
+            try:
+                next(roles[k])
+            except StopIteration:
+                alive.remove(k)
+    return False
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_one_tile_forward_protocol(seed):
+    rnd = random.Random(seed)
+    assert run_one_tile(rnd.choice([0, 1, 2, 3, 5, 9]), rnd.choice([2, 3]), rnd.choice([2, 3]),
+                        seed)
