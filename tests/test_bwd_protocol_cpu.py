@@ -62,10 +62,14 @@ def touches(pipe, region):
     return any(op[0] == "mma" and region in op[1:] for op in pipe)
 
 
-def run_key_outer(n, qs, seed):
+def run_key_outer(n, qs, seed, with_dq=False):
+    """with_dq: the block-sparse form, with dS^T in shared memory, dQ^T formed
+    in the dP columns and drained by four dQ warps (DQ_FULL / DQ_EMPTY), and
+    the dS^T tile released by DS_EMPTY."""
     rnd = random.Random(seed)
     B = {"KV": Bar(1), "DOF": Bar(1), "DOE": Bar(1), "SF": Bar(1), "DPF": Bar(1),
-         "Final": Bar(1), "PF": Bar(8), "DSF": Bar(8)}
+         "Final": Bar(1), "PF": Bar(8), "DSF": Bar(8), "DQF": Bar(1), "DQE": Bar(4),
+         "DSE": Bar(1)}
     for s in range(qs):
         B[f"QF{s}"] = Bar(1)
         B[f"QE{s}"] = Bar(1)
@@ -110,9 +114,19 @@ def run_key_outer(n, qs, seed):
                 yield from issue_s(t + 1)
             while not B["DSF"].done(t & 1):
                 yield
-            pipe.append(("mma", "dP", "dK"))          # dK(t) reads dS^T from dP
+            if with_dq:
+                pipe.append(("mma", "dS", "dP"))      # dQ^T(t): dS^T (smem) into the dP columns
+                pipe.append(("commit", "DQF"))
+                pipe.append(("mma", "dS", "dK"))      # dK(t) reads dS^T from shared memory
+            else:
+                pipe.append(("mma", "dP", "dK"))      # dK(t) reads dS^T from dP
             pipe.append(("commit", f"QE{t % qs}"))
+            if with_dq:
+                pipe.append(("commit", "DSE"))
             if t + 1 < n:
+                if with_dq:
+                    while not B["DQE"].done(t & 1):
+                        yield
                 yield from issue_dp(t + 1)
         pipe.append(("commit", "Final"))
 
@@ -125,6 +139,11 @@ def run_key_outer(n, qs, seed):
             B["PF"].arrive()
             while not B["DPF"].done(t & 1):
                 yield
+            if with_dq:
+                if t > 0:
+                    while not B["DSE"].done((t - 1) & 1):
+                        yield
+                assert not touches(pipe, "dS"), "dS^T written while a product reads it"
             assert not touches(pipe, "dP"), "dP read / dS written while a product uses dP"
             yield
             B["DSF"].arrive()
@@ -132,7 +151,16 @@ def run_key_outer(n, qs, seed):
             yield
         assert not touches(pipe, "dV") and not touches(pipe, "dK")
 
-    return simulate([producer(), mma()] + [pwarp() for _ in range(8)], loads, pipe, B, rnd)
+    def dqwarp():
+        for t in range(n if with_dq else 0):
+            while not B["DQF"].done(t & 1):
+                yield
+            assert not touches(pipe, "dP"), "dQ^T read while a product writes the dP columns"
+            yield
+            B["DQE"].arrive()
+
+    roles = [producer(), mma()] + [pwarp() for _ in range(8)] + [dqwarp() for _ in range(4)]
+    return simulate(roles, loads, pipe, B, rnd)
 
 
 def run_query_outer(n, kst, seed):
@@ -218,6 +246,12 @@ def run_query_outer(n, kst, seed):
 def test_key_outer_protocol(seed):
     rnd = random.Random(seed)
     assert run_key_outer(rnd.choice([0, 1, 2, 3, 7, 12]), rnd.choice([2, 3]), seed)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_key_outer_protocol_with_dq(seed):
+    rnd = random.Random(seed)
+    assert run_key_outer(rnd.choice([0, 1, 2, 3, 7, 12]), 2, seed, with_dq=True)
 
 
 @pytest.mark.parametrize("seed", range(30))
