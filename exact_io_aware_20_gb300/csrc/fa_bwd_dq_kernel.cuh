@@ -393,7 +393,8 @@ cudaError_t launch_dq_variant(const Problem& pr, const BwdArgs& a, cudaStream_t 
 // dP (128), dQ (128).  Warps: 0 TMA producer (Q, dO once; K, V rings),
 // 1 MMA issuer, 2..9 dS warps (a query row per thread; warps w and w + 4
 // share a TMEM lane quarter and split the 128 key columns in halves).
-// Issue order per key tile j: S(j+1), [dS(j)] dP(j+1), dQ += dS(j) K_j.
+// Issue order per key tile j: S(j+1), [dP(j) read: DP_READ] dP(j+1),
+// [dS(j) written: DS_FULL, two barriers alternating] dQ += dS(j) K_j.
 // dS stays in TMEM and is the A operand of the dQ product (TS form).
 constexpr int kDq128Threads = 320;
 
