@@ -597,15 +597,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 // cycles, N = 256 takes 126), so with 64-row steps the products S^T, dP^T and
 // dQ^T (N = 64) run at half rate.  With 128-row steps every product has
 // N = 128.  TMEM then holds dV (128 columns), dK (128), S^T (128, P^T written
-// over it in 16 bits) and dP^T (128); dQ^T of a step is written into the dP^T
-// columns once the dS warps have read dP^T, and the next dP^T waits until the
-// dQ warps have read dQ^T out.  Issue order per step t:
+// over it in 16 bits) and dP^T (128).
+// Dense (dK and dV only; dQ comes from the query-outer kernel): the P / dS
+// warps write dS^T in 16 bits over the dP^T columns they have read, dK reads
+// it there (TS form), and the dS^T shared-memory tile becomes a third Q
+// stage.  Issue order per step t:
+//   dV(t), S(t+1), dK(t), dP(t+1)
+// so the exponentials of step t+1 overlap dK(t) and dP(t+1).
+// Block-sparse (dQ accumulated here): dS^T goes to shared memory, dQ^T of a
+// step is written into the dP^T columns once the dS warps have read dP^T,
+// and the next dP^T waits until the dQ warps have read dQ^T out:
 //   dV(t), S(t+1), dQ^T(t), dK(t), dP(t+1)
-// so the exponentials of step t+1 overlap dQ^T(t) and dK(t), and dP(t+1)
-// overlaps the dS of nothing but is ready before P(t+1) is done.
-// Warps: 0 TMA producer (K, V once; Q in two stages, dO in one), 1 MMA
-// issuer, 2..9 P / dS (a key row per thread; warps w and w + 4 share a TMEM
-// lane quarter and split the 128 query columns in halves), 10..13 dQ.
+// Warps: 0 TMA producer (K, V once; Q in three or two stages, dO in one),
+// 1 MMA issuer, 2..9 P / dS (a key row per thread; warps w and w + 4 share a
+// TMEM lane quarter and split the 128 query columns in halves; one arrival
+// per warp on P_FULL and DS_FULL), 10..13 dQ (block-sparse only).
 
 constexpr int kB128Threads = 448;
 
