@@ -68,6 +68,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the forward / backward timings of the other workloads")
     ap.add_argument("--mode", choices=["train", "decode", "blocksparse"], default="train",
                     help="train: fwd+bwd step (the headline); decode: short-query forward; "
                          "blocksparse: fwd+bwd step under a random block mask")
@@ -187,6 +189,76 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": top,
                 "power_w_max": max(power) if power else None, "samples": len(self.rows),
                 "reasons": reasons}
+
+
+class NvmlPoller:
+    """SM clock, power and clock-event reasons read through NVML every few
+    milliseconds (the timed region of the default run lasts well under a
+    second, too short for nvidia-smi's 100 ms sampling).  Read-only queries;
+    None when the NVML library is not present."""
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        import ctypes
+        self.ct = ctypes
+        self.period = period_s
+        self.samples = []
+        self.lib = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) != 0:
+                return
+            self.lib, self.h, self.max_mhz = lib, h, float(mx.value)
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except Exception:
+            self.lib = None
+
+    def _sample(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, ct.c_int(1), ct.byref(clk)) != 0:
+            return
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        self.samples.append((float(clk.value), pw.value / 1000.0, int(rs.value)))
+
+    def __enter__(self):
+        import threading
+        self._stop = threading.Event()
+        if self.lib is not None:
+            def loop():
+                while not self._stop.is_set():
+                    self._sample()
+                    time.sleep(self.period)
+            self._t = threading.Thread(target=loop, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.lib is not None:
+            self._t.join(timeout=2)
+        return False
+
+    def summary(self):
+        if self.lib is None or not self.samples:
+            return None
+        sm = [s[0] for s in self.samples]
+        loaded = [s for s in sm if s > 0.5 * self.max_mhz] or sm
+        reasons = sorted({name for s in self.samples for bit, name in self.REASONS.items()
+                          if s[2] & bit})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(loaded), "power_w_max": max(s[1] for s in self.samples),
+                "samples": len(self.samples), "reasons": reasons, "source": "nvml, 2 ms"}
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -450,7 +522,7 @@ def main():
     # ------------------------------------------------ device-timed region
     binding.timing_enable(4 * args.steps + 8)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local) as clocks, NvmlPoller(local) as nvml:
         barrier()
         torch.cuda.synchronize()
         ev0.record(stream)
@@ -558,6 +630,9 @@ def main():
 
     # ------------------------------------------------ roofline of the dominant kernel
     peaks, peak_src = load_peaks()
+    clk = nvml.summary() or clocks.summary()
+    if nvml.summary() is not None:
+        clk["nvidia_smi"] = clocks.summary()
     dom = max(kernel_times, key=lambda kk: kernel_times[kk][0])
     dom_ms, dom_n = kernel_times[dom]
     per_launch_ms = dom_ms / max(dom_n, 1)
@@ -570,11 +645,11 @@ def main():
             w.flops_fwd() / 2
 
         achieved = fl / (per_launch_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak, why = choose_tensor_peak(peaks, peak_src, clk, ms_total * 1e-3)
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)",
-                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": why,
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
     else:
         rows = w.B * w.H * w.N
         by = rows * w.d * 2 * 2 + rows * 4 + rows * w.d * 4 if dom == "bwd_pre" else \
@@ -615,7 +690,7 @@ def main():
         "fwd_tflops": round(w.flops_fwd() / (fwd_ms * 1e-3) / 1e12, 1),
         "bwd_tflops": round(w.flops_bwd() / (bwd_ms * 1e-3) / 1e12, 1),
         "kernels": kernels,
-        "exp_rate": exp_rate(w, fwd_ms, kernel_times),
+        "exp_rate": exp_rate(w, fwd_ms, kernel_times, binding.measure_ex2_rate(stream)),
         "roofline": roof,
         "e2e": {"value": round(world * flops_step / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
@@ -626,33 +701,175 @@ def main():
                 "serial_ms_per_step": round(ms_e2e_serial, 4),
                 "serial_value": round(world * flops_step / (ms_e2e_serial * 1e-3) / 1e12, 2)},
         "gpu_launches": gpu_launches,
-        "clocks": clocks.summary(),
+        "clocks": clk,
+        "timed_region_s": round(ms_total * 1e-3, 4),
     }
+    if world == 1 and not args.no_per_config:
+        line["bwd_deterministic"] = time_deterministic_bwd(w, q, k, v, o, lse, do, dq, dk, dv, ws,
+                                                           stream, peaks)
+        line["per_config"] = per_config(dev, peaks, peak_src)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(base, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     return 0
 
 
-# exp2 throughput of the GPU used for the secondary (softmax) bound: 32
-# results per clock per SM (the rate at which ncu's XU-pipe utilisation of the
-# forward kernel matches its count of exponentials), 152 SMs, 2.07 GHz.
-EXP_PEAK = 32 * 152 * 2.07e9
+def choose_tensor_peak(peaks, peak_src, clk, region_s):
+    """The dense bf16 peak a kernel timed in this run is held against: the
+    burst figure (a GEMM timed alone at full clock) unless the timed region
+    lasted several seconds and the SM clock under load fell below its maximum,
+    which is the regime of the sustained figure (a GEMM loop of seconds under
+    the power cap)."""
+    sm, mx = (clk or {}).get("sm_mhz"), (clk or {}).get("sm_max_mhz")
+    at_max = sm is not None and mx and sm >= 0.97 * mx
+    if region_s >= 3.0 and sm is not None and not at_max:
+        return peaks["bf16_tflops_sustained"], (
+            f"{peak_src} bf16 sustained: timed region {region_s:.2f} s, median SM clock "
+            f"{sm:.0f} of {mx:.0f} MHz")
+    clock = f"median SM clock {sm:.0f} of {mx:.0f} MHz" if sm is not None else "clock not sampled"
+    return peaks["bf16_tflops"], (
+        f"{peak_src} bf16 burst: timed region {region_s:.3f} s, {clock}")
 
 
-def exp_rate(w: Workload, fwd_ms: float, kernel_times) -> dict:
+def time_deterministic_bwd(w, q, k, v, o, lse, do, dq, dk, dv, ws, stream, peaks, iters=10):
+    """fa_bwd_deterministic on the same workload (query-outer dQ kernel, no
+    atomics): the reproducible alternative to the default backward."""
+    from exact_io_aware_20_gb300 import binding
+
+    def bwd():
+        binding.backward(q, k, v, o, lse, do, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
+                         workspace=ws, stream=stream, deterministic=True)
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        bwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    binding.device_status()
+    ms = e0.elapsed_time(e1) / iters
+    tf = w.flops_bwd() / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tflops": round(tf, 1),
+            "frac_of_burst": round(tf / peaks["bf16_tflops"], 4)}
+
+
+# Forward and backward timings of the other workloads of the measurement plan.
+PER_CONFIG = ["tiny", "gpt_layer", "gpt_layer_causal", "long_seq", "head256"]
+
+
+def fwd_bytes(w: Workload) -> int:
+    """Algorithmic bytes of the forward: Q, K, V read, O and L written."""
+    q = w.B * w.H * w.N * w.d * 2
+    kv = w.B * w.Hkv * w.N * w.d * 2
+    return 2 * q + 2 * kv + w.B * w.H * w.N * 4
+
+
+def bwd_bytes(w: Workload) -> int:
+    """Algorithmic bytes of the backward: Q, K, V, O, dO, L read, dQ, dK, dV written."""
+    q = w.B * w.H * w.N * w.d * 2
+    kv = w.B * w.Hkv * w.N * w.d * 2
+    return 4 * q + 4 * kv + w.B * w.H * w.N * 4
+
+
+def per_config(dev, peaks, peak_src, iters: int = 10):
+    """Forward and backward of each workload timed separately with CUDA
+    events on the launch stream (inputs larger than L2, except the tiny one,
+    whose calls are replayed from CUDA graphs with a write of twice the L2
+    size before each timed call)."""
+    from exact_io_aware_20_gb300 import binding
+    out = {}
+    stream = torch.cuda.Stream(device=dev)     # graphs are captured off the default stream
+    for name in PER_CONFIG:
+        w = WORKLOADS[name]
+        q, k, v, do = (t.to(dev) for t in make_inputs(w))
+        o = torch.empty_like(q)
+        lse = torch.empty(w.B, w.H, w.N, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(binding.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d),
+                         dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()    # the copies above ran on the default stream
+
+        def fwd():
+            binding.forward(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream)
+
+        def bwd():
+            binding.backward(q, k, v, o, lse, do, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
+                             workspace=ws, stream=stream)
+
+        res = {}
+        if name == "tiny":
+            flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+            for part, fn in (("fwd", fwd), ("bwd", bwd)):
+                for _ in range(3):
+                    fn()
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                times = []
+                for _ in range(4 * iters):
+                    with torch.cuda.stream(stream):
+                        flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    with torch.cuda.stream(stream):
+                        g.replay()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                res[part] = statistics.median(times)
+            del flush
+        else:
+            for part, fn in (("fwd", fwd), ("bwd", bwd)):
+                for _ in range(3):
+                    fn()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(iters):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                res[part] = e0.elapsed_time(e1) / iters
+        binding.device_status()
+        entry = {"shape": f"B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d} {w.dtype} "
+                          f"causal={int(w.causal)}"}
+        for part, flops, nbytes in (("fwd", w.flops_fwd(), fwd_bytes(w)),
+                                    ("bwd", w.flops_bwd(), bwd_bytes(w))):
+            ms = res[part]
+            tf = flops / (ms * 1e-3) / 1e12
+            entry[part] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                           "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
+                           "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+            if name == "tiny":
+                entry[part]["us"] = round(ms * 1e3, 2)
+        out[name] = entry
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+    out["notes"] = (f"frac_of_burst against the {peak_src} bf16 burst peak "
+                    f"{peaks['bf16_tflops']} TFLOP/s; gbs = algorithmic bytes (inputs read and "
+                    f"outputs written once) / time; backward = preprocess + main + dQ kernels")
+    return out
+
+
+def exp_rate(w: Workload, fwd_ms: float, kernel_times, peak_per_s: float) -> dict:
     """Exponentials per second: one per unmasked score in the forward kernel;
     in the backward the kernels that form P (the main kernel, and at d = 128
-    the query-outer dQ kernel, which forms it again)."""
+    with the query-outer dQ kernel that one too, which forms it again),
+    against the ex2 rate measured on this GPU in the same run
+    (fa_measure_ex2_rate)."""
     scores = w.B * w.H * w.N * w.N / (2 if w.causal else 1)
-    out = {"peak_per_s": EXP_PEAK, "peak_source": "32/clk/SM x 152 SMs x 2.07 GHz (derived)",
+    out = {"peak_per_s": round(peak_per_s, 1),
+           "peak_source": "measured: fa_measure_ex2_rate (independent ex2.approx chains on every SM)",
            "fwd_per_s": round(scores / (fwd_ms * 1e-3), 1)}
-    out["fwd_frac"] = round(out["fwd_per_s"] / EXP_PEAK, 4)
+    out["fwd_frac"] = round(out["fwd_per_s"] / peak_per_s, 4)
     for kind in ("bwd_main", "bwd_dq"):
         ms, n = kernel_times.get(kind, (0.0, 0))
         if n:
             out[kind + "_per_s"] = round(scores / (ms / n * 1e-3), 1)
-            out[kind + "_frac"] = round(out[kind + "_per_s"] / EXP_PEAK, 4)
+            out[kind + "_frac"] = round(out[kind + "_per_s"] / peak_per_s, 4)
     return out
 
 

@@ -45,6 +45,7 @@ SIGNATURES = {
     "fa_get_device_status": (_i, [_vp]),
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_selftest_expired_wait": (_i, [_i, _vp]),
+    "fa_measure_ex2_rate": (_i, [ctypes.POINTER(ctypes.c_double), _vp]),
     "fa_timing_enable": (_i, [_i]),
     "fa_timing_read": (_i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
@@ -260,6 +261,14 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None
 def device_status(stream=None):
     """Synchronise the stream and raise if a kernel reported a bounded-wait timeout."""
     _check(fa_get_device_status(stream), "fa_get_device_status")
+
+
+def measure_ex2_rate(stream=None) -> float:
+    """Exponentials per second of the device's ex2 unit (fa_measure_ex2_rate)."""
+    out = ctypes.c_double(0.0)
+    _check(load().fa_measure_ex2_rate(ctypes.byref(out), _stream_ptr(stream)),
+           "fa_measure_ex2_rate")
+    return out.value
 
 
 def timing_enable(capacity: int):

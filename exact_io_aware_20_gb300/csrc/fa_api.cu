@@ -129,6 +129,23 @@ cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int cols, int rows,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int cols, int rows, int planes,
+                             int box_cols, int box_rows) {
+  std::call_once(g_encode_once, load_encoder);
+  if (g_encode_err != cudaSuccess) return g_encode_err;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4,
+                           static_cast<cuuint64_t>(cols) * rows * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
 struct TimingState {
   std::mutex mu;
@@ -170,6 +187,24 @@ __global__ void expired_wait_kernel(unsigned int* err, uint64_t limit_ns) {
     const bool completed = mbar_wait_limit(smem_u32(&never_done), 0, &abort_flag, limit_ns);
     if (!completed && abort_flag == 2) atomicOr(err, kErrTimeout);
   }
+}
+
+// Throughput of the exponential unit: every thread runs eight independent
+// chains x <- 2^(-x) (values stay in [1/2, 1]) through ex2.approx, the
+// instruction the softmax warps use; the chains' results are kept alive
+// through a store that never happens for these inputs.
+__global__ void __launch_bounds__(256) ex2_rate_kernel(float* sink, int iters) {
+  float x[8];
+  #pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = -1e-3f * static_cast<float>((threadIdx.x + i) & 63);
+  for (int it = 0; it < iters; ++it) {
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = ex2_approx(-x[i]);
+  }
+  float s = 0.f;
+  #pragma unroll
+  for (int i = 0; i < 8; ++i) s += x[i];
+  if (s < 0.f) sink[blockIdx.x] = s;
 }
 
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -472,12 +507,8 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
   float* delta = static_cast<float*>(workspace);
   float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         (rows * sizeof(float) + 255) / 256 * 256);
-  // dQ strategy, chosen by measurement on GB300: at d = 128 the query-outer
-  // kernel (S and dP formed again, no atomics) is faster than adding every
-  // key tile's contribution into the fp32 accumulator, whose reductions bound
-  // the key-outer kernel; at d = 64 and 256 the atomic path is faster.  Under
-  // a block mask the atomic path is kept unless reproducibility is asked for.
-  if (d == 128 && mask == nullptr) deterministic = 1;
+  // dQ strategy: atomic adds into the fp32 accumulator unless
+  // reproducibility is asked for.
   fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};
   if (mask != nullptr) a.mask = *mask;
   if (strd != nullptr) {
@@ -510,7 +541,11 @@ extern "C" int fa_get_device_status(fa_stream_t stream) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(fa::g_device_error, &zero, sizeof(zero));
     if (e != cudaSuccess) return fa::cuda_fail(e, "clear device error word");
-    return FA_ERR_TIMEOUT;
+    if (word & fa::kErrTimeout) return FA_ERR_TIMEOUT;
+    std::snprintf(fa::g_cuda_msg, sizeof(fa::g_cuda_msg),
+                  "a kernel found its dynamic shared memory base misaligned (error word %#x)",
+                  word);
+    return FA_ERR_CUDA;
   }
   return FA_OK;
 }
@@ -582,4 +617,37 @@ extern "C" int fa_selftest_expired_wait(int limit_us, fa_stream_t stream) {
       err, static_cast<uint64_t>(limit_us) * 1000ull);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FA_OK : fa::cuda_fail(e, "selftest launch");
+}
+
+extern "C" int fa_measure_ex2_rate(double* exps_per_s, fa_stream_t stream) {
+  if (!exps_per_s) return FA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int st = fa::check_device(&err);
+  if (st != FA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int blocks = 8 * fa::num_sms(), threads = 256, iters = 4096;
+  cudaEvent_t e0, e1;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e != cudaSuccess) return fa::cuda_fail(e, "cudaEventCreate");
+  if ((e = cudaEventCreate(&e1)) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return fa::cuda_fail(e, "cudaEventCreate");
+  }
+  double best = 0.0;
+  for (int rep = 0; rep < 4 && e == cudaSuccess; ++rep) {
+    cudaEventRecord(e0, s);
+    fa::ex2_rate_kernel<<<blocks, threads, 0, s>>>(nullptr, iters);
+    cudaEventRecord(e1, s);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    if (e == cudaSuccess && rep > 0 && ms > 0.f)   // the first run is a warm-up
+      best = std::max(best, 8.0 * blocks * threads * static_cast<double>(iters) / (ms * 1e-3));
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return fa::cuda_fail(e, "ex2 rate kernel");
+  *exps_per_s = best;
+  return FA_OK;
 }

@@ -92,6 +92,12 @@ struct BwdArgs {
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int cols, int rows, int heads,
                          int batch, const Strides& st, int box_cols, int box_rows);
 
+// Encode a 3-D tiled tensor map over a contiguous fp32 [planes][rows][cols]
+// array with a box of box_cols x box_rows of one plane and no swizzle;
+// coordinates (col, row, plane).
+cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int cols, int rows, int planes,
+                             int box_cols, int box_rows);
+
 // Diagnostics timing (see fa_timing_enable in fa.h): returns a slot to pass
 // to timing_end, or -1 when timing is off or out of event pairs.
 int timing_begin(int kind, cudaStream_t stream);
@@ -101,6 +107,8 @@ cudaError_t launch_fwd(const Problem& p, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_blocksparse(const Problem& p, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);
+// d = 128, dense, dQ by atomic adds: the fused five-product kernel.
+cudaError_t launch_bwd_fused(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 // Deterministic dQ (query-outer, no atomics); needs D in a.delta.
 cudaError_t launch_bwd_dq(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);

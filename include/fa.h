@@ -25,9 +25,12 @@
  * of the tile size is handled inside the kernels); H % Hkv == 0.
  *
  * Ownership: the caller allocates every buffer (device memory) and keeps it
- * alive until the work on `stream` has finished.  The library allocates no
- * device memory; the backward pass takes its scratch from the caller's
- * `workspace`.
+ * alive until the work on `stream` has finished.  The library makes no
+ * allocation when called; the backward pass takes its scratch from the
+ * caller's `workspace` (fa_bwd_noalloc excepted: it uses a fixed array the
+ * library holds on every device that loads it).  The library caches, per
+ * device, the address of its device-side error word: after cudaDeviceReset
+ * the library must not be used again in the same process.
  *
  * Semantics: every call only enqueues work on `stream` (NULL is the legacy
  * default stream) and returns; nothing is synchronised.  Outputs are
@@ -121,11 +124,12 @@ size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  * heads that share each key/value head).  workspace must be a device buffer
  * of at least fa_bwd_workspace_size(...) bytes, 256-byte aligned; its
  * contents on entry do not matter and are garbage on exit.
- * dQ strategy (chosen by measurement): at d = 128 dQ comes from the
- * query-outer kernel of fa_bwd_deterministic, which is the faster one there
- * (every output is then bitwise reproducible); at d = 64 and 256 each key
- * tile's contribution is added to an fp32 accumulator with atomic adds, the
- * pages' scheme, whose summation order varies from run to run.
+ * dQ strategy (chosen by measurement): each key tile's contribution is added
+ * to an fp32 accumulator in the workspace, the pages' scheme; at d = 128 one
+ * fused kernel forms all five products of a tile and hands each dQ tile to
+ * the tensor memory accelerator as bulk reduce-adds.  The order of those
+ * additions varies from run to run, so dQ is reproducible only up to fp32
+ * rounding; fa_bwd_deterministic gives the same bits on every run.
  */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
@@ -175,7 +179,11 @@ int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void
  * share the one array: calls whose work overlaps on the GPU (two streams,
  * two threads) race and must be ordered by the caller.  The first call on a
  * device looks up the array's address with that device current, so make it
- * before any stream capture.
+ * before any stream capture.  That address is kept for the life of the
+ * process: after cudaDeviceReset (or anything else that destroys the
+ * device's primary context) this entry point must not be called again in the
+ * same process.  Devices with an ordinal of 64 or more are not served
+ * (FA_ERR_UNSUPPORTED).
  */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -281,6 +289,18 @@ const char *fa_strerror(int status);
  * the CUDA context stays usable.  Returns an fa_status for the launch.
  */
 int fa_selftest_expired_wait(int limit_us, fa_stream_t stream);
+
+/*
+ * Diagnostics: measures the throughput of the GPU's exponential unit
+ * (ex2.approx, the instruction the softmax steps use for every score), the
+ * secondary bound of the attention kernels ("FlashAttention-2: Faster
+ * Attention with Better Parallelism and Work Partitioning", paper digest,
+ * section 2 Q1: the non-matmul work).  Runs a kernel of independent ex2
+ * chains on every SM of the current device, synchronises `stream`, and
+ * writes the exponentials per second (best of three timed runs) to
+ * *exps_per_s.  Returns an fa_status.
+ */
+int fa_measure_ex2_rate(double *exps_per_s, fa_stream_t stream);
 
 enum fa_kernel_kind {
   FA_KERNEL_FWD = 0,         /* the forward kernel */

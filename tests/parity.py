@@ -60,3 +60,22 @@ def check_grads(pairs, what=""):
     bad = {k: v for k, v in errs.items() if v > GRAD_REL_L2}
     assert not bad, f"{what}: gradient rel_l2 over {GRAD_REL_L2}: {errs}"
     return errs
+
+
+def check_grads_tiled(pairs, tile=128, what=""):
+    """Each (name, x, ref) of shape [heads, rows, d]: the rel_L2 bound of the
+    gradients applied to every (head, 128-row tile) block on its own, so that
+    one wrong tile cannot hide inside the norm of the whole tensor."""
+    worst = {}
+    for name, x, ref in pairs:
+        x, ref = to_np(x), to_np(ref)
+        assert x.shape == ref.shape and x.ndim == 3, (name, x.shape, ref.shape)
+        w = 0.0
+        for h in range(x.shape[0]):
+            for r0 in range(0, x.shape[1], tile):
+                e = rel_l2(x[h, r0:r0 + tile], ref[h, r0:r0 + tile])
+                assert e <= GRAD_REL_L2, f"{what}: {name} head {h} rows {r0}.. rel_l2 {e:.3e}"
+                w = max(w, e)
+        worst[name] = w
+    record(what + " (worst tile)", **{f"{k}_rel_l2": v for k, v in worst.items()})
+    return worst

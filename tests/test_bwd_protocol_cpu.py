@@ -36,7 +36,9 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def simulate(roles, loads, pipe, B, rnd):
+def simulate(roles, loads, pipe, B, rnd, content=None):
+    """content: optional dict, TMEM region -> label of the product that last
+    wrote it (products given as ("mma", reads, writes, label))."""
     alive = list(range(len(roles)))
     for _ in range(2_000_000):
         if not alive and not loads and not pipe:
@@ -48,6 +50,8 @@ def simulate(roles, loads, pipe, B, rnd):
             op = pipe.pop(0)
             if op[0] == "commit":
                 B[op[1]].arrive()
+            elif content is not None and len(op) == 4:
+                content[op[2]] = op[3]
         elif alive:
             k = rnd.choice(alive)
             try:
@@ -258,3 +262,125 @@ def test_key_outer_protocol_with_dq(seed):
 def test_query_outer_protocol(seed):
     rnd = random.Random(seed)
     assert run_query_outer(rnd.choice([0, 1, 2, 3, 7, 12]), rnd.choice([2, 3]), seed)
+
+
+
+def run_fused(n, seed, readout_wait=True):
+    """The fused d = 128 kernel (all five products, dQ added to the fp32
+    accumulator): the key-outer protocol with two Q stages, dQ^T formed in
+    the dP columns and read out by four dQ warps (DQ_FULL, then one DQ_EMPTY
+    arrival per warp before dP^T(t+1) may overwrite the columns); their
+    staging and bulk reduce-add are ordered among themselves by named
+    barriers and touch no barrier here.  Besides the checks of the other
+    models, each read of dQ^T must find the product of the same step in the
+    dP columns.  readout_wait=False plants a mistake: the dQ warps read
+    without waiting for DQ_FULL."""
+    rnd = random.Random(seed)
+    B = {"KV": Bar(1), "DOF": Bar(1), "DOE": Bar(1), "SF": Bar(1), "DPF": Bar(1),
+         "Final": Bar(1), "PF": Bar(8), "DSF": Bar(8), "DQF": Bar(1), "DQE": Bar(4),
+         "DSE": Bar(1)}
+    qs = 2
+    for s_ in range(qs):
+        B[f"QF{s_}"] = Bar(1)
+        B[f"QE{s_}"] = Bar(1)
+    loads, pipe = [], []
+
+    def producer():
+        loads.append("KV")
+        for t in range(n):
+            s_ = t % qs
+            if t >= qs:
+                while not B[f"QE{s_}"].done(((t // qs) + 1) & 1):
+                    yield
+            loads.append(f"QF{s_}")
+            if t >= 1:
+                while not B["DOE"].done((t - 1) & 1):
+                    yield
+            loads.append("DOF")
+
+    def mma():
+        def issue_s(t):
+            while not B[f"QF{t % qs}"].done((t // qs) & 1):
+                yield
+            pipe.append(("mma", "S"))
+            pipe.append(("commit", "SF"))
+
+        def issue_dp(t):
+            while not B["DOF"].done(t & 1):
+                yield
+            pipe.append(("mma", "dP"))
+            pipe.append(("commit", "DPF"))
+        while not B["KV"].done(0):
+            yield
+        if n > 0:
+            yield from issue_s(0)
+            yield from issue_dp(0)
+        for t in range(n):
+            while not B["PF"].done(t & 1):
+                yield
+            pipe.append(("mma", "S", "dV"))
+            pipe.append(("commit", "DOE"))
+            if t + 1 < n:
+                yield from issue_s(t + 1)
+            while not B["DSF"].done(t & 1):
+                yield
+            pipe.append(("mma", "dS", "dP", ("dQ", t)))   # dQ^T(t) into the dP columns
+            pipe.append(("commit", "DQF"))
+            pipe.append(("mma", "dS", "dK"))
+            pipe.append(("commit", f"QE{t % qs}"))
+            pipe.append(("commit", "DSE"))
+            if t + 1 < n:
+                while not B["DQE"].done(t & 1):
+                    yield
+                yield from issue_dp(t + 1)
+        pipe.append(("commit", "Final"))
+
+    def pwarp():
+        for t in range(n):
+            while not B["SF"].done(t & 1):
+                yield
+            assert not touches(pipe, "S")
+            yield
+            B["PF"].arrive()
+            while not B["DPF"].done(t & 1):
+                yield
+            if t > 0:
+                while not B["DSE"].done((t - 1) & 1):
+                    yield
+            assert not touches(pipe, "dS") and not touches(pipe, "dP")
+            yield
+            B["DSF"].arrive()
+        while not B["Final"].done(0):
+            yield
+        assert not touches(pipe, "dV") and not touches(pipe, "dK")
+
+    def dqwarp():
+        for t in range(n):
+            if readout_wait:
+                while not B["DQF"].done(t & 1):
+                    yield
+            assert not touches(pipe, "dP"), "dQ^T read while a product writes the dP columns"
+            assert content.get("dP") == ("dQ", t), "dQ^T read before the product that forms it"
+            yield
+            B["DQE"].arrive()
+
+    content = {}
+    return simulate([producer(), mma()] + [pwarp() for _ in range(8)] +
+                    [dqwarp() for _ in range(4)], loads, pipe, B, rnd, content)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fused_protocol(seed):
+    rnd = random.Random(seed)
+    assert run_fused(rnd.choice([0, 1, 2, 3, 4, 7, 12]), seed)
+
+
+def test_fused_model_catches_a_missing_readout_wait():
+    caught = 0
+    for seed in range(40):
+        try:
+            run_fused(6, seed, readout_wait=False)
+        except AssertionError as e:
+            assert "dQ^T read" in str(e), e
+            caught += 1
+    assert caught > 0

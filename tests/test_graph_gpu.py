@@ -42,9 +42,9 @@ def test_graph_replay_matches_eager(d, causal):
         torch.cuda.synchronize()
         binding.device_status()
         for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), got, (o, lse, dq, dk, dv)):
-            if name == "dq" and d != 128:
-                # d = 64, 256: dQ accumulated with fp32 atomic adds, whose order
-                # varies: equal up to a bf16 rounding step
+            if name == "dq":
+                # dQ accumulated with fp32 atomic adds, whose order varies:
+                # equal up to a bf16 rounding step
                 assert torch.allclose(a.float(), b.float(), rtol=1e-2, atol=1e-3), name
             else:
                 assert torch.equal(a, b), name

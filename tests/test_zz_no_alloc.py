@@ -44,3 +44,21 @@ def test_noalloc_rejects_problems_above_its_scratch():
     st = binding.load().fa_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                        B, H, Hkv, N, d, 1, 0.088, binding.FA_BF16, None)
     assert st == binding.FA_ERR_WORKSPACE
+
+
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs a second GPU")
+def test_noalloc_on_a_second_device():
+    """The scratch address is looked up per device, with that device current:
+    a call under device 1 gives fa_bwd's gradients there."""
+    w = Workload("noalloc_dev1", 1, 4, 2, 300, 128, "bf16", True, 44)
+    dev = torch.device("cuda", 1)
+    with torch.cuda.device(dev):
+        q, k, v, do = make_inputs(w, dev)
+        o, lse = binding.forward(q, k, v, w.causal, w.scale)
+        dq_ref, dk_ref, dv_ref = binding.backward(q, k, v, o, lse, do, w.causal, w.scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        st = binding.fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, w.B, w.H, w.Hkv, w.N, w.d,
+                                    w.causal, w.scale, binding.FA_BF16)
+        assert st == binding.FA_OK, binding.strerror(st)
+        binding.device_status()
+        check_grads([("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)], "noalloc dev1")
