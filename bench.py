@@ -50,8 +50,9 @@ _COMMON_SOURCES = ["exact_io_aware_20_gb300/csrc/fa_api.cu",
 KERNEL_SOURCES = {
     "fwd": ["exact_io_aware_20_gb300/csrc/fa_fwd_kernel.cuh",
             "exact_io_aware_20_gb300/csrc/fa_fwd.cu"] + _COMMON_SOURCES,
-    "bwd_main": ["exact_io_aware_20_gb300/csrc/fa_bwd_kernel.cuh",
-                 "exact_io_aware_20_gb300/csrc/fa_bwd.cu"] + _COMMON_SOURCES,
+    "bwd_main": ["exact_io_aware_20_gb300/csrc/fa_bwd_fused_kernel.cuh",
+                 "exact_io_aware_20_gb300/csrc/fa_bwd_fused.cu",
+                 "exact_io_aware_20_gb300/csrc/fa_bwd_kernel.cuh"] + _COMMON_SOURCES,
     "bwd_dq": ["exact_io_aware_20_gb300/csrc/fa_bwd_dq_kernel.cuh",
                "exact_io_aware_20_gb300/csrc/fa_bwd_dq.cu"] + _COMMON_SOURCES,
 }

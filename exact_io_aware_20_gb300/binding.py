@@ -29,6 +29,7 @@ SIGNATURES = {
     "fa_bwd_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                        _i, _i, _vp, _sz, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_bwd_workspace_size_for": (_sz, [_i, _i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i,
                     _vp, _sz, _vp]),
     "fa_bwd_deterministic": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
@@ -115,6 +116,10 @@ def fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, dtype, stream=None) 
 
 def fa_bwd_workspace_size(B, H, Hkv, N, d) -> int:
     return int(load().fa_bwd_workspace_size(B, H, Hkv, N, d))
+
+
+def fa_bwd_workspace_size_for(B, H, Hkv, Nq, d, deterministic) -> int:
+    return int(load().fa_bwd_workspace_size_for(B, H, Hkv, Nq, d, int(bool(deterministic))))
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, d, causal, scale, dtype, workspace,
@@ -204,7 +209,7 @@ def backward_strided(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = fa_bwd_workspace_size(B, H, Hkv, Nq, d)
+    need = fa_bwd_workspace_size_for(B, H, Hkv, Nq, d, deterministic)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _check(load().fa_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
@@ -241,7 +246,7 @@ def backward(q, k, v, o, lse, dout, causal: bool, scale: float, dq=None, dk=None
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = fa_bwd_workspace_size(B, H, Hkv, Nq, d)
+    need = fa_bwd_workspace_size_for(B, H, Hkv, Nq, d, deterministic)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -342,7 +347,7 @@ def backward_blocksparse(q, k, v, o, lse, dout, block_mask, causal: bool, scale:
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = fa_bwd_workspace_size(B, H, Hkv, Nq, d)
+    need = fa_bwd_workspace_size_for(B, H, Hkv, Nq, d, deterministic)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _check(load().fa_bwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),

@@ -207,9 +207,10 @@ __global__ void __launch_bounds__(256) ex2_rate_kernel(float* sink, int iters) {
   if (s < 0.f) sink[blockIdx.x] = s;
 }
 
-size_t bwd_workspace_bytes(int B, int H, int N, int d) {
+size_t bwd_workspace_bytes(int B, int H, int N, int d, int deterministic) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
+  if (deterministic) return delta;   // dQ is written directly, no accumulator
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
   return delta + acc;
 }
@@ -409,7 +410,15 @@ extern "C" int fa_fwd_strided(const void* q, const void* k, const void* v, void*
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
   Problem pr;
   if (fa::validate(B, H, Hkv, N, N, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
-  return fa::bwd_workspace_bytes(B, H, N, d);
+  return fa::bwd_workspace_bytes(B, H, N, d, 0);
+}
+
+extern "C" size_t fa_bwd_workspace_size_for(int B, int H, int Hkv, int Nq, int d,
+                                            int deterministic) {
+  Problem pr;
+  if (deterministic != 0 && deterministic != 1) return 0;
+  if (fa::validate(B, H, Hkv, Nq, Nq, d, 0, 1.0f, FA_BF16, &pr) != FA_OK) return 0;
+  return fa::bwd_workspace_bytes(B, H, Nq, d, deterministic);
 }
 
 namespace fa {
@@ -499,14 +508,17 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
       !fa::aligned(dout, 16) || !fa::aligned(dq, 16) || !fa::aligned(dk, 16) ||
       !fa::aligned(dv, 16) || !fa::aligned(lse, 4))
     return FA_ERR_INVALID_ARG;
-  const size_t need = fa::bwd_workspace_bytes(B, H, Nq, d);
+  // scratch of the path that runs: D, and the fp32 dQ accumulator unless
+  // dQ is formed by the query-outer kernel
+  const size_t need = fa::bwd_workspace_bytes(B, H, Nq, d, deterministic);
   if (!workspace || workspace_bytes < need || !fa::aligned(workspace, 256))
     return FA_ERR_WORKSPACE;
   if ((st = fa::check_device(&pr.err)) != FA_OK) return st;
   const size_t rows = static_cast<size_t>(B) * H * Nq;
   float* delta = static_cast<float*>(workspace);
-  float* acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        (rows * sizeof(float) + 255) / 256 * 256);
+  float* acc = deterministic ? nullptr
+                            : reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                       (rows * sizeof(float) + 255) / 256 * 256);
   // dQ strategy: atomic adds into the fp32 accumulator unless
   // reproducibility is asked for.
   fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};

@@ -329,12 +329,11 @@ bwd128_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
       const f2 cs = {p.scale_log2, p.scale_log2};
       const int qc0 = q0 + 64 * half;              // first query of this half
       float P[64];
-      #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t sr[32];
-        tmem_ld32(tS + lane_off + 64 * half + c0, sr);
-        tmem_ld_wait();
-        reg_fence(sr);
+      // 32 columns at a time, the second chunk's TMEM load in flight while
+      // the first is exponentiated
+      auto p_chunk = [&](const uint32_t (&sr)[32], int c0) {
+        // L and D come from shared memory as 16-byte broadcasts (a quarter
+        // of the shared-memory wavefronts of scalar loads)
         #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(sL + c0 + c);
@@ -360,6 +359,18 @@ bwd128_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(P[c0 + 2 * c], P[c0 + 2 * c + 1]);
         // P^T over the first 32 columns of this half, already read
         tmem_st16(tS + lane_off + 64 * half + c0 / 2, pk);
+      };
+      {
+        const uint32_t src = tS + lane_off + 64 * half;
+        uint32_t sa[32], sb[32];
+        tmem_ld32(src, sa);
+        tmem_ld_wait();
+        reg_fence(sa);
+        tmem_ld32(src + 32, sb);
+        p_chunk(sa, 0);
+        tmem_ld_wait();
+        reg_fence(sb);
+        p_chunk(sb, 32);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -368,12 +379,9 @@ bwd128_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!wait_uniform(bar(L::kDPFull), t & 1, abort)) { ok = false; break; }
       if (t > 0 && !wait_uniform(bar(L::kDSEmpty), (t - 1) & 1, abort)) { ok = false; break; }
       tc_fence_after();
-      #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        uint32_t dr[16];
-        tmem_ld16(tdP + lane_off + 64 * half + c0, dr);
-        tmem_ld_wait();
-        reg_fence(dr);
+      // 16 columns at a time, the TMEM load of the next chunk in flight while
+      // the current one is computed (P, 64 values, stays live throughout)
+      auto ds_chunk = [&](const uint32_t (&dr)[16], int c0) {
         uint32_t w[8];
         #pragma unroll
         for (int c = 0; c < 8; c += 2) {
@@ -394,6 +402,26 @@ bwd128_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                 ((u ^ (r & 7)) * 16));
           *dst = make_uint4(w[4 * u2], w[4 * u2 + 1], w[4 * u2 + 2], w[4 * u2 + 3]);
         }
+      };
+      {
+        const uint32_t src = tdP + lane_off + 64 * half;
+        uint32_t da[16], db[16];
+        tmem_ld16(src, da);
+        tmem_ld_wait();
+        reg_fence(da);
+        tmem_ld16(src + 16, db);
+        ds_chunk(da, 0);
+        tmem_ld_wait();
+        reg_fence(db);
+        tmem_ld16(src + 32, da);
+        ds_chunk(db, 16);
+        tmem_ld_wait();
+        reg_fence(da);
+        tmem_ld16(src + 48, db);
+        ds_chunk(da, 32);
+        tmem_ld_wait();
+        reg_fence(db);
+        ds_chunk(db, 48);
       }
       tc_fence_before();
       fence_proxy_async_smem();

@@ -19,11 +19,15 @@
 // only the (head, query tile) steps whose mask block with its key tile is
 // kept; a key tile with no step gets dK = dV = 0.
 //
-// Three kernels: preprocess (D and a zeroed fp32 dQ accumulator), the main
-// kernel below, and a conversion of the accumulator to the output dtype
-// (with the softmax scale applied).
+// Three kernels: preprocess (D and a zeroed fp32 dQ accumulator), a main
+// kernel, and a conversion of the accumulator to the output dtype (with the
+// softmax scale applied).  The main kernels here: bwd_kernel (d = 64 and
+// 256) and bwd128_kernel (d = 128: the key-outer half of the reproducible
+// backward, and the block-sparse backward).  The default dense d = 128
+// backward runs the fused kernel of fa_bwd_fused_kernel.cuh, which uses the
+// preprocess and conversion kernels of this file.
 //
-// Main kernel, one CTA per (batch, key/value head, 128-key tile[, half of
+// bwd_kernel, one CTA per (batch, key/value head, 128-key tile[, half of
 // d when d = 256]); 10 warps:
 //   warp 0      TMA producer: K and V once, then (Q_i, dO_i) tiles;
 //   warp 1      MMA issuer (tcgen05, fp32 accumulators in TMEM);
@@ -36,10 +40,11 @@
 //               accumulator in global memory (red.global.add).
 // S^T and dP^T are computed with keys on the TMEM lanes (M = 128) so the
 // dK/dV accumulators and the score tiles share one layout.  Two tile shapes:
-//   d = 64:       128 query rows per step; dQ = dS K (query rows on lanes).
-//   d = 128, 256: 64 query rows per step; dQ^T = K^T dS^T (d on lanes).
-//   d = 256 is split over two CTAs by output half of d (S^T and dP^T are
-//   computed by both), because dK + dV for all 256 columns would fill TMEM.
+//   d = 64:  128 query rows per step; dQ = dS K (query rows on lanes).
+//   d = 256: 64 query rows per step; dQ^T = K^T dS^T (d on lanes), split
+//            over two CTAs by output half of d (S^T and dP^T are computed by
+//            both), because dK + dV for all 256 columns would fill TMEM.
+// (bwd128_kernel, below, has its own description.)
 #pragma once
 
 #include <type_traits>

@@ -113,8 +113,8 @@ cudaError_t launch_bwd_fused(const Problem& p, const BwdArgs& a, cudaStream_t st
 cudaError_t launch_bwd_dq(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 
-// Bytes of backward scratch for a problem (delta + dq accumulator, each
-// rounded up to 256 bytes).
-size_t bwd_workspace_bytes(int B, int H, int N, int d);
+// Bytes of backward scratch for a problem: delta, and unless deterministic
+// the fp32 dq accumulator, each rounded up to 256 bytes.
+size_t bwd_workspace_bytes(int B, int H, int N, int d, int deterministic);
 
 }  // namespace fa

@@ -61,7 +61,7 @@ enum fa_status {
   FA_ERR_UNSUPPORTED = 2, /* head dim, dtype or device (not sm_103) not supported */
   FA_ERR_CUDA = 3,        /* a CUDA call failed; fa_strerror(FA_ERR_CUDA) has its text */
   FA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (from fa_get_device_status) */
-  FA_ERR_WORKSPACE = 5    /* backward workspace missing or smaller than fa_bwd_workspace_size */
+  FA_ERR_WORKSPACE = 5    /* backward workspace missing, misaligned or too small for the path */
 };
 
 /*
@@ -112,18 +112,30 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int 
 /*
  * Bytes of device scratch fa_bwd needs for this shape: the fp32 row vector
  * D = rowsum(dO o O) [B][H][N] and an fp32 dQ accumulator [B][H][N][d]
- * (N = the query length).
- * Returns 0 for invalid sizes.
+ * (N = the query length), each rounded up to 256 bytes.  This is enough for
+ * every backward entry point.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
+
+/*
+ * Bytes of scratch the backward path selected by `deterministic` needs
+ * (0 or 1, as in fa_bwd_qk): with deterministic = 1 dQ is written directly by
+ * the query-outer kernel and only D is needed (B * H * Nq * 4 bytes, rounded
+ * up to 256); with 0 D and the fp32 dQ accumulator (fa_bwd_workspace_size).
+ * fa_bwd, fa_bwd_qk, fa_bwd_deterministic, fa_bwd_strided and
+ * fa_bwd_blocksparse check their workspace_bytes against this size for the
+ * path they run.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size_for(int B, int H, int Hkv, int Nq, int d, int deterministic);
 
 /*
  * Backward pass of the forward above, for the same arguments.  o and lse are
  * the forward's outputs; dout is the upstream gradient dO.  Writes dq
  * [B][H][N][d], dk and dv [B][Hkv][N][d] (dtype; dk/dv summed over the query
  * heads that share each key/value head).  workspace must be a device buffer
- * of at least fa_bwd_workspace_size(...) bytes, 256-byte aligned; its
- * contents on entry do not matter and are garbage on exit.
+ * of at least fa_bwd_workspace_size(...) bytes (= fa_bwd_workspace_size_for
+ * with deterministic = 0), 256-byte aligned; its contents on entry do not
+ * matter and are garbage on exit.
  * dQ strategy (chosen by measurement): each key tile's contribution is added
  * to an fp32 accumulator in the workspace, the pages' scheme; at d = 128 one
  * fused kernel forms all five products of a tile and hands each dQ tile to
@@ -140,8 +152,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
  * Backward pass of fa_fwd_qk: separate query and key lengths, the same mask.
  * dq [B][H][Nq][d], dk, dv [B][Hkv][Nk][d].  deterministic = 1 selects the
  * reproducible dQ path of fa_bwd_deterministic for every head dim, 0 the
- * choice of fa_bwd.  The workspace is fa_bwd_workspace_size(B, H, Hkv, Nq, d)
- * bytes.
+ * choice of fa_bwd.  The workspace is fa_bwd_workspace_size_for(B, H, Hkv,
+ * Nq, d, deterministic) bytes.
  */
 int fa_bwd_qk(const void *q, const void *k, const void *v, const void *o, const float *lse,
               const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int Nq,
@@ -157,8 +169,9 @@ int fa_bwd_qk(const void *q, const void *k, const void *v, const void *o, const 
  * dQ in a query-outer kernel that owns each query tile and walks the key
  * tiles in a fixed order (two extra products per tile: S and dP are formed
  * again); dK and dV come from the same key-outer kernel as in fa_bwd, in a
- * mode without dQ.  Same arguments, layouts and workspace as fa_bwd; every
- * output is the same bits on every run.
+ * mode without dQ.  Same arguments and layouts as fa_bwd; the workspace
+ * needs only fa_bwd_workspace_size_for(..., deterministic = 1) bytes (D);
+ * every output is the same bits on every run.
  */
 int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
                          const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
@@ -214,7 +227,8 @@ int fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *
                    const fa_strides *strides, fa_stream_t stream);
 
 /* strides[8]: q, k, v, o, dout, dq, dk, dv.  Otherwise as fa_bwd_qk (the
- * workspace is fa_bwd_workspace_size(B, H, Hkv, Nq, d) bytes). */
+ * workspace is fa_bwd_workspace_size_for(B, H, Hkv, Nq, d, deterministic)
+ * bytes). */
 int fa_bwd_strided(const void *q, const void *k, const void *v, const void *o, const float *lse,
                    const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int Nq,
                    int Nk, int d, int causal, float scale, int dtype, const fa_strides *strides,

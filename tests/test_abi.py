@@ -49,6 +49,33 @@ def test_workspace_size(lib):
     assert binding.fa_bwd_workspace_size(B, H, 2, N, 96) == 0
 
 
+def test_workspace_size_for_the_path(lib):
+    """The deterministic path needs only D (dQ is written directly); the
+    default path D and the fp32 dQ accumulator, which is the upper bound."""
+    B, H, N = 2, 32, 8192
+    delta = -(-B * H * N * 4 // 256) * 256
+    for d in (64, 128, 256):
+        assert binding.fa_bwd_workspace_size_for(B, H, 8, N, d, True) == delta
+        assert binding.fa_bwd_workspace_size_for(B, H, 8, N, d, False) == \
+            binding.fa_bwd_workspace_size(B, H, 8, N, d)
+    assert binding.load().fa_bwd_workspace_size_for(B, H, 8, N, 128, 2) == 0
+    assert binding.fa_bwd_workspace_size_for(B, H, 3, N, 128, True) == 0
+
+
+def test_backward_rejects_a_workspace_too_small_for_its_path(lib):
+    """With only D's bytes the default (accumulating) path is refused before
+    anything is enqueued; the deterministic path accepts them (checked on the
+    GPU in test_bwd_gpu.py)."""
+    B, H, Hkv, N, d = 1, 4, 4, 256, 128
+    only_d = binding.fa_bwd_workspace_size_for(B, H, Hkv, N, d, True)
+    st = lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv, N, d, 1,
+                    0.088, binding.FA_BF16, FAKE, only_d, None)
+    assert st == binding.FA_ERR_WORKSPACE
+    st = lib.fa_bwd_deterministic(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv,
+                                  N, d, 1, 0.088, binding.FA_BF16, FAKE, only_d - 256, None)
+    assert st == binding.FA_ERR_WORKSPACE
+
+
 FAKE = 1 << 20   # never dereferenced: every case below fails validation first
 
 

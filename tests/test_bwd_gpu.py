@@ -70,6 +70,24 @@ def test_backward_dk_dv_deterministic_and_workspace_contents_ignored():
     assert (r1[0].float() - r2[0].float()).abs().max().item() < 1e-2
 
 
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_backward_with_exactly_the_workspace_of_its_path(deterministic):
+    """d = 128: the deterministic path runs in D's bytes alone, the default
+    path in D plus the accumulator; both against the oracle."""
+    w = Workload("ws", 1, 8, 2, 700, 128, "bf16", True, 21)
+    q, k, v, do = make_inputs(w)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = binding.forward(qd, kd, vd, w.causal, w.scale)
+    need = binding.fa_bwd_workspace_size_for(w.B, w.H, w.Hkv, w.N, w.d, deterministic)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    dq, dk, dv = binding.backward(qd, kd, vd, o, lse, dod, w.causal, w.scale, workspace=ws,
+                                  deterministic=deterministic)
+    binding.device_status()
+    dq_r, dk_r, dv_r = oracle.backward(q, k, v, do, w.causal, w.scale)
+    check_grads([("dq", dq.cpu(), dq_r), ("dk", dk.cpu(), dk_r), ("dv", dv.cpu(), dv_r)],
+                f"exact workspace det{deterministic}")
+
+
 FULL = ["gpt_layer", "gpt_layer_causal", "long_seq", "head256", "gqa8k"]
 
 
