@@ -58,6 +58,35 @@ KERNEL_SOURCES = {
 }
 
 
+# Small shapes for profiler captures (--mode case): one kernel of each kind
+# on a few hundred MB, larger than L2.  name -> (workload, deterministic backward)
+PROFILE_CASES = {
+    "gqa8k_b1": (WORKLOADS["gqa8k"].with_(B=1), False),
+    "gpt_layer_b2": (WORKLOADS["gpt_layer"].with_(B=2), False),
+    "d64": (Workload("d64", 1, 16, 16, 4096, 64, "bf16", False, 7), False),
+    "head256_b1": (WORKLOADS["head256"].with_(B=1), False),
+    "head256_b1_det": (WORKLOADS["head256"].with_(B=1), True),
+}
+
+
+def run_case(args):
+    """One forward and two backward calls of a small shape: the launches a
+    profiler capture selects from (-k <kernel> -s <launches to skip> -c 1)."""
+    torch.cuda.set_device(0)
+    from exact_io_aware_20_gb300 import binding
+    binding.load()
+    w, det = PROFILE_CASES[args.case]
+    q, k, v, do = make_inputs(w, "cuda")
+    o, lse = binding.forward(q, k, v, w.causal, w.scale)
+    for _ in range(2):
+        binding.backward(q, k, v, o, lse, do, w.causal, w.scale, deterministic=det)
+    binding.device_status()
+    print(json.dumps({"case": args.case, "shape": f"B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d} "
+                                                 f"{w.dtype} causal={int(w.causal)}",
+                      "deterministic": det}), flush=True)
+    return 0
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -71,9 +100,12 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the forward / backward timings of the other workloads")
-    ap.add_argument("--mode", choices=["train", "decode", "blocksparse"], default="train",
+    ap.add_argument("--mode", choices=["train", "decode", "blocksparse", "case"], default="train",
                     help="train: fwd+bwd step (the headline); decode: short-query forward; "
-                         "blocksparse: fwd+bwd step under a random block mask")
+                         "blocksparse: fwd+bwd step under a random block mask; case: one "
+                         "forward and two backward calls of a --case, for profiler captures")
+    ap.add_argument("--case", default="gqa8k_b1", choices=sorted(PROFILE_CASES),
+                    help="case: the shape to run (see PROFILE_CASES)")
     ap.add_argument("--density", type=float, default=0.25,
                     help="blocksparse: fraction of 128x128 blocks kept")
     ap.add_argument("--decode-nq", type=int, default=1)
@@ -483,6 +515,8 @@ def main():
         return run_decode(args)
     if args.mode == "blocksparse":
         return run_blocksparse(args)
+    if args.mode == "case":
+        return run_case(args)
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
