@@ -855,6 +855,16 @@ def per_config(dev, peaks, peak_src, iters: int = 10):
                     torch.cuda.synchronize()
                     times.append(e0.elapsed_time(e1))
                 res[part] = statistics.median(times)
+                # eager calls back to back through the Python binding (host
+                # argument checks, cached tensor maps, launches): their
+                # average spacing on the GPU timeline
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(200):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                res[part + "_eager"] = e0.elapsed_time(e1) / 200
             del flush
         else:
             for part, fn in (("fwd", fwd), ("bwd", bwd)):
@@ -880,6 +890,7 @@ def per_config(dev, peaks, peak_src, iters: int = 10):
                            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
             if name == "tiny":
                 entry[part]["us"] = round(ms * 1e3, 2)
+                entry[part]["eager_us"] = round(res[part + "_eager"] * 1e3, 2)
         out[name] = entry
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()

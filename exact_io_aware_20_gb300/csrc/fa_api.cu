@@ -112,8 +112,67 @@ int validate(int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float sca
 
 }  // namespace
 
+namespace {
+// Encoded tensor maps, kept per (base address, shape, strides, box): encoding
+// is a driver call of about a microsecond, and a training loop passes the
+// same buffers call after call.  A fixed number of entries, replaced round
+// robin; the map itself holds only the address and the geometry, so an entry
+// is valid on any device.
+struct TmapKey {
+  int kind;                      // 0: 16-bit 4-D view, 1: fp32 3-D array
+  const void* base;
+  long long dims[4], strides[3];
+  int box[2];
+  bool operator==(const TmapKey& o) const {
+    return kind == o.kind && base == o.base && box[0] == o.box[0] && box[1] == o.box[1] &&
+           std::memcmp(dims, o.dims, sizeof(dims)) == 0 &&
+           std::memcmp(strides, o.strides, sizeof(strides)) == 0;
+  }
+};
+constexpr int kTmapCacheSize = 128;
+struct TmapCache {
+  std::mutex mu;
+  TmapKey key[kTmapCacheSize];
+  CUtensorMap map[kTmapCacheSize];
+  int used = 0, next = 0;
+};
+TmapCache g_tmaps;
+
+bool tmap_lookup(const TmapKey& k, CUtensorMap* out) {
+  std::lock_guard<std::mutex> lk(g_tmaps.mu);
+  for (int i = 0; i < g_tmaps.used; ++i)
+    if (g_tmaps.key[i] == k) {
+      *out = g_tmaps.map[i];
+      return true;
+    }
+  return false;
+}
+
+void tmap_store(const TmapKey& k, const CUtensorMap& m) {
+  std::lock_guard<std::mutex> lk(g_tmaps.mu);
+  const int slot = g_tmaps.next;
+  g_tmaps.key[slot] = k;
+  g_tmaps.map[slot] = m;
+  g_tmaps.next = (slot + 1) % kTmapCacheSize;
+  if (g_tmaps.used < kTmapCacheSize) ++g_tmaps.used;
+}
+}  // namespace
+
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int cols, int rows, int heads,
                          int batch, const Strides& st, int box_cols, int box_rows) {
+  TmapKey key{};
+  key.kind = 0;
+  key.base = base;
+  key.dims[0] = cols;
+  key.dims[1] = rows;
+  key.dims[2] = heads;
+  key.dims[3] = batch;
+  key.strides[0] = st.n;
+  key.strides[1] = st.h;
+  key.strides[2] = st.b;
+  key.box[0] = box_cols;
+  key.box[1] = box_rows;
+  if (tmap_lookup(key, map)) return cudaSuccess;
   std::call_once(g_encode_once, load_encoder);
   if (g_encode_err != cudaSuccess) return g_encode_err;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -126,11 +185,22 @@ cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, int cols, int rows,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  tmap_store(key, *map);
+  return cudaSuccess;
 }
 
 cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int cols, int rows, int planes,
                              int box_cols, int box_rows) {
+  TmapKey key{};
+  key.kind = 1;
+  key.base = base;
+  key.dims[0] = cols;
+  key.dims[1] = rows;
+  key.dims[2] = planes;
+  key.box[0] = box_cols;
+  key.box[1] = box_rows;
+  if (tmap_lookup(key, map)) return cudaSuccess;
   std::call_once(g_encode_once, load_encoder);
   if (g_encode_err != cudaSuccess) return g_encode_err;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -143,7 +213,9 @@ cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int cols, int 
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  tmap_store(key, *map);
+  return cudaSuccess;
 }
 
 namespace {
