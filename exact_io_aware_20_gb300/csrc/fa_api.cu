@@ -284,7 +284,7 @@ size_t bwd_workspace_bytes(int B, int H, int N, int d, int deterministic) {
   const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
   if (deterministic) return delta;   // dQ is written directly, no accumulator
   const size_t acc = (rows * d * sizeof(float) + 255) / 256 * 256;
-  return delta + acc;
+  return delta + acc + kBwdSchedBytes;   // + the persistent kernel's work counter
 }
 
 }  // namespace fa
@@ -591,9 +591,14 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
   float* acc = deterministic ? nullptr
                             : reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                        (rows * sizeof(float) + 255) / 256 * 256);
+  unsigned int* units =
+      deterministic ? nullptr
+                    : reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(acc) +
+                                                      (rows * d * sizeof(float) + 255) / 256 * 256);
   // dQ strategy: atomic adds into the fp32 accumulator unless
   // reproducibility is asked for.
   fa::BwdArgs a{q, k, v, o, lse, dout, dq, dk, dv, delta, acc, deterministic};
+  a.units = units;
   if (mask != nullptr) a.mask = *mask;
   if (strd != nullptr) {
     a.qs = strd[0];

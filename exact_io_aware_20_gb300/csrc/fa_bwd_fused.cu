@@ -17,7 +17,7 @@ cudaError_t launch_fused(const Problem& pr, const BwdArgs& a, cudaStream_t strea
   bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + kPreRows - 1) / kPreRows),
                             kPreWarps * 32, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta, a.dq_acc,
-      rows, pr.H, pr.Nq, a.os, a.dos);
+      rows, pr.H, pr.Nq, a.os, a.dos, a.units);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 2. the fused kernel
@@ -29,6 +29,9 @@ cudaError_t launch_fused(const Problem& pr, const BwdArgs& a, cudaStream_t strea
   CUtensorMap tacc;   // the fp32 dQ accumulator [B * H][Nq][128], boxes of 32 rows
   if ((e = make_tmap_f32_3d(&tacc, a.dq_acc, D, pr.Nq, pr.B * pr.H, D, 32)) != cudaSuccess)
     return e;
+  CUtensorMap tdk, tdv;   // outputs, stored as the K / V tiles are loaded
+  if ((e = make_tmap_4d(&tdk, a.dk, D, pr.Nk, pr.Hkv, pr.B, a.dks, 64, kBC)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tdv, a.dv, D, pr.Nk, pr.Hkv, pr.B, a.dvs, 64, kBC)) != cudaSuccess) return e;
   auto kern = bwd128_fused_kernel<CAUSAL, BF16>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -64,22 +67,32 @@ cudaError_t launch_fused(const Problem& pr, const BwdArgs& a, cudaStream_t strea
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (g_num_sms <= 0) g_num_sms = 148;
   }
-  // Heavy-first order (the longest key tiles of every group dispatched
-  // first) when one CTA holds more than a fifth of an SM's share of the
-  // work; otherwise key tiles fastest, so the CTAs of a group share its Q
-  // and dO in L2.
+  // Unit order.  Heavy first (the longest key tiles of every group first)
+  // when one unit holds more than a fifth of an SM's share of the work;
+  // otherwise key tiles fastest, so the units of a group run together and
+  // share its Q and dO in L2, with the last groups (about two units per CTA)
+  // taken longest key tile first under the mask so the launch does not end
+  // on one long unit.
+  p.n_groups = pr.Hkv * pr.B;
+  p.n_kv_tiles = n_kv_tiles;
+  const long long n_units = static_cast<long long>(n_kv_tiles) * p.n_groups;
+  if (n_units > (1ll << 30)) return cudaErrorInvalidValue;
+  p.n_units = static_cast<int>(n_units);
+  p.units = a.units;
+  const int n_ctas = static_cast<int>(std::min<long long>(n_units, g_num_sms));
   p.heavy_first = 0;
-  if (CAUSAL && n_kv_tiles <= 65535) {
+  p.tail_groups = 0;
+  if (CAUSAL) {
     double total = 0.0;
     for (int j = 0; j < n_kv_tiles; ++j) total += p.n_q_tiles - std::max(0, j * kBC - p.off) / BR;
-    total *= static_cast<double>(p.G) * pr.Hkv * pr.B;
+    total *= static_cast<double>(p.G) * p.n_groups;
     const double longest = static_cast<double>(p.G) * p.n_q_tiles;
     p.heavy_first = longest > 0.2 * total / g_num_sms ? 1 : 0;
+    if (!p.heavy_first)
+      p.tail_groups = std::min(p.n_groups, (2 * n_ctas + n_kv_tiles - 1) / n_kv_tiles);
   }
-  const dim3 grid = p.heavy_first ? dim3(pr.Hkv * pr.B, n_kv_tiles, 1)
-                                  : dim3(n_kv_tiles, pr.Hkv, pr.B);
   slot = timing_begin(FA_KERNEL_BWD_MAIN, stream);
-  kern<<<grid, kFusedThreads, FusedLayout::kAlloc, stream>>>(tq, tk, tv, tdo, tacc, p);
+  kern<<<n_ctas, kFusedThreads, FusedLayout::kAlloc, stream>>>(tq, tk, tv, tdo, tacc, tdk, tdv, p);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 3. dq = scale * accumulator, in the output dtype
@@ -96,7 +109,8 @@ cudaError_t launch_fused(const Problem& pr, const BwdArgs& a, cudaStream_t strea
 }  // namespace
 
 cudaError_t launch_bwd_fused(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
-  if (pr.d != 128 || a.mask.ptr != nullptr || a.deterministic) return cudaErrorInvalidValue;
+  if (pr.d != 128 || a.mask.ptr != nullptr || a.deterministic || a.units == nullptr)
+    return cudaErrorInvalidValue;
   if (pr.causal)
     return pr.bf16 ? launch_fused<true, true>(pr, a, stream) : launch_fused<true, false>(pr, a, stream);
   return pr.bf16 ? launch_fused<false, true>(pr, a, stream) : launch_fused<false, false>(pr, a, stream);

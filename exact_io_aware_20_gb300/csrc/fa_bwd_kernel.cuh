@@ -125,6 +125,11 @@ struct BwdParams {
   BlockMask mask;    // block-sparse: only the kept blocks' steps
   Strides dks, dvs;  // element strides of dk, dv
   unsigned int* err;
+  // persistent fused kernel: work counter (zero at launch), units = key
+  // tiles x groups, groups = (batch, kv head) pairs, and how many of the last
+  // groups are taken heavy first in the key-tile-fastest order
+  unsigned int* units;
+  int n_units, n_kv_tiles, n_groups, tail_groups;
 };
 
 template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16, bool SPARSE>
@@ -1107,7 +1112,8 @@ __device__ __forceinline__ long long view_offset(size_t row, int H, int N, const
 }
 
 // D_i = dO_i . O_i (fp32) and a zeroed dQ accumulator row (delta and the
-// accumulator are contiguous; o and dout strided).  HBM-bound: D / 8 lanes
+// accumulator are contiguous; o and dout strided), and the persistent
+// kernel's work counter set to zero when one is given.  HBM-bound: D / 8 lanes
 // per row read 16 bytes of each tensor, a warp covers 256 / D rows per pass
 // and makes kPasses passes with every load issued before the first sum, so
 // that enough bytes are in flight to keep HBM busy.
@@ -1120,11 +1126,12 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kPreWarps * 32)
 bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                float* __restrict__ delta, float* __restrict__ dq_acc, size_t rows, int H, int N,
-               Strides os, Strides dos) {
+               Strides os, Strides dos, unsigned int* __restrict__ units) {
   constexpr int kLanes = D / 8;                  // lanes per row
   constexpr int kRowsPerPass = 32 / kLanes;      // rows of one warp per pass
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / kLanes, col = (lane % kLanes) * 8;
+  if (units != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *units = 0u;   // work counter
   const size_t row0 = static_cast<size_t>(blockIdx.x) * pre_rows_per_block<D>() +
                       static_cast<size_t>(warp) * kRowsPerPass * kPrePasses + sub;
   uint4 ov[kPrePasses], dv[kPrePasses];
@@ -1195,7 +1202,7 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + kPreRows - 1) / kPreRows),
                             kPreWarps * 32, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
-      a.deterministic ? nullptr : a.dq_acc, rows, pr.H, pr.Nq, a.os, a.dos);
+      a.deterministic ? nullptr : a.dq_acc, rows, pr.H, pr.Nq, a.os, a.dos, nullptr);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // 2. main kernel

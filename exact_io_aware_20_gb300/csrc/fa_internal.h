@@ -80,6 +80,7 @@ struct BwdArgs {
   float* dq_acc;   // [B, H, Nq, d] fp32 scratch (unused when deterministic)
   int deterministic;   // dQ from the query-outer kernel, without atomics
   BlockMask mask = {};  // block-sparse
+  unsigned int* units = nullptr;   // work counter of the persistent d = 128 kernel (scratch)
   // element strides of q, k, v, o, dout, dq, dk, dv (set by the caller); the
   // scratch (delta, dq_acc) and lse are always contiguous
   Strides qs = {}, ks = {}, vs = {}, os = {}, dos = {}, dqs = {}, dks = {}, dvs = {};
@@ -114,7 +115,9 @@ cudaError_t launch_bwd_dq(const Problem& p, const BwdArgs& a, cudaStream_t strea
 cudaError_t launch_bwd_dq_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 
 // Bytes of backward scratch for a problem: delta, and unless deterministic
-// the fp32 dq accumulator, each rounded up to 256 bytes.
+// the fp32 dq accumulator (each rounded up to 256 bytes) and kBwdSchedBytes
+// for the work counter of the persistent d = 128 kernel.
+constexpr size_t kBwdSchedBytes = 256;
 size_t bwd_workspace_bytes(int B, int H, int N, int d, int deterministic);
 
 }  // namespace fa

@@ -140,6 +140,28 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 4-D tiled store of one shared-memory box to global memory, in the
+// bulk-async group of the issuing thread (rows outside the tensor are not
+// written); coordinates c0 (innermost) .. c3, c0 16-byte aligned and none
+// negative.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// Fetch one box of a 4-D tensor into L2 (no shared memory written, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                   int c3) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

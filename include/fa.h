@@ -112,7 +112,8 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int 
 /*
  * Bytes of device scratch fa_bwd needs for this shape: the fp32 row vector
  * D = rowsum(dO o O) [B][H][N] and an fp32 dQ accumulator [B][H][N][d]
- * (N = the query length), each rounded up to 256 bytes.  This is enough for
+ * (N = the query length), each rounded up to 256 bytes, then 256 bytes for
+ * the work counter of the persistent d = 128 kernel.  This is enough for
  * every backward entry point.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
@@ -121,7 +122,8 @@ size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  * Bytes of scratch the backward path selected by `deterministic` needs
  * (0 or 1, as in fa_bwd_qk): with deterministic = 1 dQ is written directly by
  * the query-outer kernel and only D is needed (B * H * Nq * 4 bytes, rounded
- * up to 256); with 0 D and the fp32 dQ accumulator (fa_bwd_workspace_size).
+ * up to 256); with 0 D, the fp32 dQ accumulator and the work counter
+ * (fa_bwd_workspace_size).
  * fa_bwd, fa_bwd_qk, fa_bwd_deterministic, fa_bwd_strided and
  * fa_bwd_blocksparse check their workspace_bytes against this size for the
  * path they run.  Returns 0 for invalid sizes.
