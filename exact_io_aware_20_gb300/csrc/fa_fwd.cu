@@ -4,7 +4,7 @@
 
 namespace fa {
 
-int fwd_key_tile(int d) { return d == 256 ? 64 : 128; }
+int fwd_key_tile(int) { return 128; }
 
 cudaError_t launch_fwd(const Problem& pr, const FwdArgs& a, cudaStream_t stream) {
   if (a.mask.ptr != nullptr) return launch_fwd_blocksparse(pr, a, stream);

@@ -60,10 +60,18 @@ struct FwdLayout {
   // every row into 16 extra TMEM columns (the row sum l_r without ALU work).
   static constexpr bool kOnes = D <= 128;
   static constexpr int kOnesCols = kOnes ? 16 : 0;
-  static constexpr int kVStage = kKVBytes + (kOnes ? BC * 128 : 0);
+  // d = 256: a whole 128-key K or V tile is 64 KB, so the rings hold smaller
+  // pieces, each with its own barriers: K in 64-column chunks (the pieces
+  // S = Q K^T consumes one after another along d) and V in halves of BC / 2
+  // keys (the pieces P V consumes along the keys).  KST and VST then count
+  // pieces, and a slot is freed as soon as the products reading it are done.
+  static constexpr bool kChunked = D > 128 && BC == 128;
+  static constexpr int kKSlot = kChunked ? BC * 128 : kKVBytes;
+  static constexpr int kVHalf = (BC / 2) * D * 2;
+  static constexpr int kVStage = kChunked ? kVHalf : kKVBytes + (kOnes ? BC * 128 : 0);
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBytes;
-  static constexpr int kVOff = kKOff + KST * kKVBytes;
+  static constexpr int kVOff = kKOff + KST * kKSlot;
   static constexpr int kBarOff = kVOff + VST * kVStage;
   // barrier indices
   static constexpr int kQFull = 0;
@@ -85,7 +93,7 @@ struct FwdLayout {
   static constexpr uint32_t kS0 = 0, kS1 = BC, kO = 2 * BC;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kO + D + kOnesCols <= kTmemCols, "TMEM budget");
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kAllocDense <= 227 * 1024, "shared memory budget");
 };
 
 struct FwdParams {
@@ -221,7 +229,37 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     __syncwarp();
     int k_issued = 0, v_issued = 0;
-    for (int j = 0; j < n_kv; ++j) {
+    if constexpr (L::kChunked) {
+      // Two lanes, each with its own ring, so that neither ring's wait holds
+      // up the other's loads: lane 0 streams the K chunks, lane 1 the V
+      // halves (with one ring walked in order, a V half waiting for P V(j)
+      // would hold back K(j + 2), which S(j + 2) needs before P V(j + 1)).
+      if (lane == 0) {
+        for (int ck = 0; ck < n_kv * L::kNch; ++ck) {
+          const int s = ck % KST;
+          if (ck >= KST && !mbar_wait(bar(L::kKEmpty + s), ((ck / KST) + 1) & 1, abort)) break;
+          mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKSlot);
+          tma_load_4d(sbase + L::kKOff + s * L::kKSlot, &tm_k, bar(L::kKFull + s),
+                      (ck % L::kNch) * 64, key_tile(ck / L::kNch) * BC, kh, b);
+          ++k_issued;
+        }
+      } else if (lane == 1) {
+        for (int vh = 0; vh < n_kv * 2; ++vh) {
+          const int sv = vh % VST;
+          if (vh >= VST && !mbar_wait(bar(L::kVEmpty + sv), ((vh / VST) + 1) & 1, abort)) break;
+          mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kVHalf);
+          #pragma unroll
+          for (int c = 0; c < L::kNch; ++c)
+            tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * ((BC / 2) * 128), &tm_v,
+                        bar(L::kVFull + sv), c * 64, key_tile(vh / 2) * BC + (vh & 1) * (BC / 2), kh, b);
+          ++v_issued;
+        }
+      }
+      __syncwarp();
+      k_issued = __shfl_sync(0xffffffffu, k_issued, 0);
+      v_issued = __shfl_sync(0xffffffffu, v_issued, 1);
+    }
+    for (int j = 0; !L::kChunked && j < n_kv; ++j) {
       const int s = j % KST;
       if (j >= KST && !wait_uniform(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) break;
       if (elect_one()) {
@@ -261,7 +299,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
     const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
     const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
+    // a V half: 64-column chunks of BC / 2 keys each
+    const uint64_t v_desc_half = smem_desc_sw128(sbase + L::kVOff, (BC / 2) * 128, 1024);
     auto issue_s = [&](int j) -> bool {
+      if constexpr (L::kChunked) {
+        // one chunk of K (64 columns of d) at a time, each slot freed as soon
+        // as its four products are done
+        const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
+        #pragma unroll 1
+        for (int c = 0; c < L::kNch; ++c) {
+          const int ck = j * L::kNch + c, s = ck % KST;
+          if (!wait_uniform(bar(L::kKFull + s), (ck / KST) & 1, abort)) return false;
+          tc_fence_after();
+          const uint64_t ks = desc_add(k_desc, s * L::kKSlot);
+          #pragma unroll
+          for (int w = 0; w < 4; ++w)
+            mma_ss(d_tmem, desc_add(q_desc, c * (kBR * 128) + w * 32), desc_add(ks, w * 32), kIdS,
+                   (c > 0 || w > 0) ? 1u : 0u);
+          mma_commit(bar(L::kKEmpty + s));
+        }
+        mma_commit(bar(L::kSFull + (j & 1)));
+        return true;
+      }
       const int s = j % KST;
       if (!wait_uniform(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
       tc_fence_after();
@@ -282,6 +341,29 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     for (int j = 0; ok && j < n_kv; ++j) {
       if (j + 1 < n_kv && !issue_s(j + 1)) break;
       if (!wait_uniform(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
+      if constexpr (L::kChunked) {
+        // P V over one half of the keys at a time
+        const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
+        bool vok = true;
+        #pragma unroll 1
+        for (int hv = 0; hv < 2; ++hv) {
+          const int vh = 2 * j + hv, sv = vh % VST;
+          if (!wait_uniform(bar(L::kVFull + sv), (vh / VST) & 1, abort)) {
+            vok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vs = desc_add(v_desc_half, sv * L::kVStage);
+          #pragma unroll
+          for (int w = 0; w < BC / 32; ++w)
+            mma_ts(tO, a_tmem + (hv * (BC / 32) + w) * 8, desc_add(vs, w * 2048), kIdO,
+                   (j > 0 || hv > 0 || w > 0) ? 1u : 0u);
+          mma_commit(bar(L::kVEmpty + sv));
+        }
+        if (!vok) break;
+        mma_commit(bar(L::kODone));
+        continue;
+      }
       const int sv = j % VST;
       if (!wait_uniform(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
       tc_fence_after();
@@ -1111,10 +1193,14 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   CUtensorMap tq, tk, tv;
   cudaError_t e;
   if ((e = make_tmap_4d(&tk, a.k, D, pr.Nk, pr.Hkv, pr.B, a.ks, 64, BC)) != cudaSuccess) return e;
-  if ((e = make_tmap_4d(&tv, a.v, D, pr.Nk, pr.Hkv, pr.B, a.vs, 64, BC)) != cudaSuccess) return e;
+  // V in halves of BC / 2 keys when the rings hold pieces of tiles
+  if ((e = make_tmap_4d(&tv, a.v, D, pr.Nk, pr.Hkv, pr.B, a.vs, 64, L::kChunked ? BC / 2 : BC)) !=
+      cudaSuccess)
+    return e;
   auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST, SPARSE>;
   // without a block mask the list is never touched and not allocated
   constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -1207,7 +1293,10 @@ cudaError_t launch_fwd_for(const Problem& pr, const FwdArgs& a, cudaStream_t str
   switch (pr.d) {
     case 64: return dispatch_flags<64, 128, 3, 3, SPARSE>(pr, a, stream);
     case 128: return dispatch_flags<128, 128, 2, 2, SPARSE>(pr, a, stream);
-    case 256: return dispatch_flags<256, 64, 2, 2, SPARSE>(pr, a, stream);
+    // d = 256: 128-key tiles through rings of pieces (six K chunks and two
+    // V halves; four K chunks with a block mask, whose key-tile list also
+    // needs shared memory)
+    case 256: return dispatch_flags<256, 128, SPARSE ? 4 : 6, 2, SPARSE>(pr, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -145,7 +145,7 @@ def test_splitkv_workspace_checks(lib):
     (dict(mask_heads=3), binding.FA_ERR_INVALID_ARG),      # neither 1 nor H
     (dict(mask_heads=0), binding.FA_ERR_INVALID_ARG),
     (dict(Nk=8193 * 128), binding.FA_ERR_INVALID_ARG),     # forward key-tile list
-    (dict(d=256, Nk=8193 * 64), binding.FA_ERR_INVALID_ARG),
+    (dict(d=256, Nk=8193 * 128), binding.FA_ERR_INVALID_ARG),   # 128-key tiles at every d
     (dict(q=FAKE + 2), binding.FA_ERR_INVALID_ARG),
     (dict(d=80), binding.FA_ERR_UNSUPPORTED),
 ])

@@ -191,11 +191,15 @@ def test_persistent_forward_protocol(seed):
     assert run(units, seed), f"protocol stalled: units {units}"
 
 
-def run_one_tile(n, kst, vst, seed):
+def run_one_tile(n, kst, vst, seed, kp=1, vp=1):
     """The one-tile forward (d = 64 / 256, short, split and block-sparse
     paths): S(j+1) is issued before P V(j), into the other of two score
     buffers, and the softmax waits for O_DONE only before a rescale of O and
-    on the last tile."""
+    on the last tile.  kp, vp: pieces per K and V tile (d = 256: four
+    64-column chunks of K, two halves of V); the rings then hold kst and vst
+    pieces, each freed by a commit after the products that read it.  Every
+    product checks, when it runs, that the ring slots it reads hold the
+    pieces of its own tile."""
     rnd = random.Random(seed)
     B = {"QFull": Bar(1), "ODone": Bar(1)}
     for s in range(kst):
@@ -205,28 +209,48 @@ def run_one_tile(n, kst, vst, seed):
     for s in range(2):
         B[f"SF{s}"] = Bar(1)
         B[f"PF{s}"] = Bar(4)           # the model's four softmax warps
-    loads, pipe = [], []
+    loads, pipe, slot = [], [], {}
+
+    def k_pieces(j):
+        for c in range(kp):
+            ck = j * kp + c
+            if ck >= kst:
+                while not B[f"KE{ck % kst}"].done(((ck // kst) + 1) & 1):
+                    yield
+            loads.append((f"KF{ck % kst}", f"K{ck % kst}", (j, c)))
+
+    def v_pieces(j):
+        for h in range(vp):
+            vh = j * vp + h
+            if vh >= vst:
+                while not B[f"VE{vh % vst}"].done(((vh // vst) + 1) & 1):
+                    yield
+            loads.append((f"VF{vh % vst}", f"V{vh % vst}", (j, h)))
 
     def producer():
-        loads.append("QFull")
+        # whole tiles: one lane walks K and V in turn; pieces: the K ring
+        # here, the V ring in producer_v (another lane)
+        loads.append(("QFull", None, None))
         for j in range(n):
-            sk, sv = j % kst, j % vst
-            if j >= kst:
-                while not B[f"KE{sk}"].done(((j // kst) + 1) & 1):
-                    yield
-            loads.append(f"KF{sk}")
-            if j >= vst:
-                while not B[f"VE{sv}"].done(((j // vst) + 1) & 1):
-                    yield
-            loads.append(f"VF{sv}")
+            yield from k_pieces(j)
+            if kp == 1:
+                yield from v_pieces(j)
+
+    def producer_v():
+        if kp > 1:
+            for j in range(n):
+                yield from v_pieces(j)
 
     def mma():
         def issue_s(j):
-            while not B[f"KF{j % kst}"].done((j // kst) & 1):
-                yield
-            pipe.append(("mma", f"S{j & 1}"))
+            for c in range(kp):
+                ck = j * kp + c
+                while not B[f"KF{ck % kst}"].done((ck // kst) & 1):
+                    yield
+                pipe.append(("mma", f"S{j & 1}"))
+                pipe.append(("check", f"K{ck % kst}", (j, c)))   # what the product read
+                pipe.append(("commit", f"KE{ck % kst}"))
             pipe.append(("commit", f"SF{j & 1}"))
-            pipe.append(("commit", f"KE{j % kst}"))
         while not B["QFull"].done(0):
             yield
         if n > 0:
@@ -236,11 +260,14 @@ def run_one_tile(n, kst, vst, seed):
                 yield from issue_s(j + 1)
             while not B[f"PF{j & 1}"].done((j >> 1) & 1):
                 yield
-            while not B[f"VF{j % vst}"].done((j // vst) & 1):
-                yield
-            pipe.append(("mma", f"S{j & 1}", "O"))       # P V(j): P from buffer j & 1
+            for h in range(vp):
+                vh = j * vp + h
+                while not B[f"VF{vh % vst}"].done((vh // vst) & 1):
+                    yield
+                pipe.append(("mma", f"S{j & 1}", "O"))       # P V(j): P from buffer j & 1
+                pipe.append(("check", f"V{vh % vst}", (j, h)))
+                pipe.append(("commit", f"VE{vh % vst}"))
             pipe.append(("commit", "ODone"))
-            pipe.append(("commit", f"VE{j % vst}"))
 
     def busy(region):
         return any(op[0] == "mma" and region in op[1:] for op in pipe)
@@ -263,18 +290,23 @@ def run_one_tile(n, kst, vst, seed):
                 yield
             assert not busy("O"), "O read out while a P V is in flight"
 
-    roles = [producer(), mma()] + [softmax() for _ in range(4)]
+    roles = [producer(), producer_v(), mma()] + [softmax() for _ in range(4)]
     alive = list(range(len(roles)))
     for _ in range(2_000_000):
         if not alive and not loads and not pipe:
             return True
         r = rnd.random()
         if loads and (r < 0.2 or not alive):
-            B[loads.pop(rnd.randrange(len(loads)))].arrive()
+            bar, key, val = loads.pop(rnd.randrange(len(loads)))
+            if key is not None:
+                slot[key] = val
+            B[bar].arrive()
         elif pipe and (r < 0.45 or not alive):
             op = pipe.pop(0)
             if op[0] == "commit":
                 B[op[1]].arrive()
+            elif op[0] == "check":
+                assert slot.get(op[1]) == op[2], "a product read a ring slot holding another piece"
         elif alive:
             k = rnd.choice(alive)
             try:
@@ -289,3 +321,12 @@ def test_one_tile_forward_protocol(seed):
     rnd = random.Random(seed)
     assert run_one_tile(rnd.choice([0, 1, 2, 3, 5, 9]), rnd.choice([2, 3]), rnd.choice([2, 3]),
                         seed)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_one_tile_forward_protocol_in_pieces(seed):
+    """d = 256: K in four chunks through a ring of four to six, V in two
+    halves through a ring of two or three, each ring loaded by its own lane."""
+    rnd = random.Random(seed)
+    assert run_one_tile(rnd.choice([0, 1, 2, 3, 5, 9]), rnd.choice([4, 5, 6]), rnd.choice([2, 3]),
+                        seed, kp=4, vp=2)
