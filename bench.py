@@ -727,6 +727,7 @@ def main():
         "kernels": kernels,
         "exp_rate": exp_rate(w, fwd_ms, kernel_times, binding.measure_ex2_rate(stream)),
         "roofline": roof,
+        "dq_reduce": dq_reduce(w, kernel_times, stream),
         "e2e": {"value": round(world * flops_step / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -917,6 +918,34 @@ def exp_rate(w: Workload, fwd_ms: float, kernel_times, peak_per_s: float) -> dic
             out[kind + "_per_s"] = round(scores / (ms / n * 1e-3), 1)
             out[kind + "_frac"] = round(out[kind + "_per_s"] / peak_per_s, 4)
     return out
+
+
+def dq_reduce_bytes(w: Workload) -> int:
+    """Bytes the d = 128 main kernel adds into the fp32 dQ accumulator: one
+    128-row x d tile per (key tile, query tile, head) step it walks (under the
+    mask only the query tiles at or below each key tile's diagonal)."""
+    n_t = (w.N + 127) // 128
+    steps = sum(n_t - (jt if w.causal else 0) for jt in range(n_t)) * w.H * w.B
+    return steps * 128 * w.d * 4
+
+
+def dq_reduce(w: Workload, kernel_times, stream):
+    """The resource that bounds the d = 128 backward main kernel: the SMs'
+    outflow of fp32 reduce-adds (each step's 64 KB dQ tile), as bytes per
+    second over the kernel's time against the rate measured on this GPU in
+    the same run (fa_measure_reduce_rate, 128 MiB of targets like the
+    accumulator)."""
+    ms, n = kernel_times.get("bwd_main", (0.0, 0))
+    if w.d != 128 or not n:
+        return None
+    scratch = torch.empty(128 << 20, dtype=torch.uint8, device="cuda")
+    peak = binding.measure_reduce_rate(scratch, stream)
+    del scratch
+    by = dq_reduce_bytes(w)
+    achieved = by / (ms / n * 1e-3)
+    return {"kernel": "bwd_main", "bytes_per_launch": by, "achieved_tbs": round(achieved / 1e12, 3),
+            "peak_tbs": round(peak / 1e12, 3), "frac": round(achieved / peak, 4),
+            "peak_source": "measured: fa_measure_reduce_rate (16 KB bulk reduce-adds, one CTA per SM)"}
 
 
 def step_bytes(w: Workload) -> int:

@@ -47,6 +47,7 @@ SIGNATURES = {
     "fa_strerror": (ctypes.c_char_p, [_i]),
     "fa_selftest_expired_wait": (_i, [_i, _vp]),
     "fa_measure_ex2_rate": (_i, [ctypes.POINTER(ctypes.c_double), _vp]),
+    "fa_measure_reduce_rate": (_i, [_vp, _sz, ctypes.POINTER(ctypes.c_double), _vp]),
     "fa_timing_enable": (_i, [_i]),
     "fa_timing_read": (_i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
 }
@@ -273,6 +274,17 @@ def measure_ex2_rate(stream=None) -> float:
     out = ctypes.c_double(0.0)
     _check(load().fa_measure_ex2_rate(ctypes.byref(out), _stream_ptr(stream)),
            "fa_measure_ex2_rate")
+    return out.value
+
+
+def measure_reduce_rate(scratch: torch.Tensor, stream=None) -> float:
+    """Bytes per second of fp32 bulk reduce-adds from every SM into `scratch`
+    (a device tensor of at least 1 MiB; fa_measure_reduce_rate)."""
+    out = ctypes.c_double(0.0)
+    _check(load().fa_measure_reduce_rate(ctypes.c_void_p(scratch.data_ptr()),
+                                         scratch.numel() * scratch.element_size(),
+                                         ctypes.byref(out), _stream_ptr(stream)),
+           "fa_measure_reduce_rate")
     return out.value
 
 

@@ -279,6 +279,28 @@ __global__ void __launch_bounds__(256) ex2_rate_kernel(float* sink, int iters) {
   if (s < 0.f) sink[blockIdx.x] = s;
 }
 
+// 16 KB fp32 tiles of shared memory (zeros) added into `dst` by 1-D bulk
+// reduce-adds from one thread per CTA, two in flight: the outflow of
+// reduction traffic an SM sustains, which bounds the atomic dQ strategy.
+__global__ void __launch_bounds__(128) reduce_rate_kernel(float* dst, int tiles, int rounds) {
+  extern __shared__ __align__(128) float zeros[];
+  for (int i = threadIdx.x; i < 2 * 4096; i += 128) zeros[i] = 0.f;
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t base = smem_u32(zeros);
+    for (int it = 0; it < rounds; ++it) {
+      const int tile = static_cast<int>((static_cast<long long>(blockIdx.x) * 7 + it * 13ll) % tiles);
+      asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 16384;"
+                   ::"l"(dst + static_cast<size_t>(tile) * 4096), "r"(base + (it & 1) * 16384)
+                   : "memory");
+      bulk_commit_group();
+      bulk_wait_read_one_left();
+    }
+    bulk_wait_all();
+  }
+}
+
 size_t bwd_workspace_bytes(int B, int H, int N, int d, int deterministic) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t delta = (rows * sizeof(float) + 255) / 256 * 256;
@@ -706,6 +728,43 @@ extern "C" int fa_selftest_expired_wait(int limit_us, fa_stream_t stream) {
       err, static_cast<uint64_t>(limit_us) * 1000ull);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FA_OK : fa::cuda_fail(e, "selftest launch");
+}
+
+extern "C" int fa_measure_reduce_rate(void* scratch, size_t scratch_bytes, double* bytes_per_s,
+                                      fa_stream_t stream) {
+  if (!bytes_per_s || !scratch || scratch_bytes < (1u << 20) || !fa::aligned(scratch, 256))
+    return FA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int st = fa::check_device(&err);
+  if (st != FA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long tiles_ll = static_cast<long long>(scratch_bytes / 16384);
+  const int tiles = static_cast<int>(std::min<long long>(tiles_ll, 1 << 30));
+  const int blocks = fa::num_sms(), rounds = 400;
+  cudaEvent_t e0, e1;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e != cudaSuccess) return fa::cuda_fail(e, "cudaEventCreate");
+  if ((e = cudaEventCreate(&e1)) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return fa::cuda_fail(e, "cudaEventCreate");
+  }
+  double best = 0.0;
+  for (int rep = 0; rep < 4 && e == cudaSuccess; ++rep) {
+    cudaEventRecord(e0, s);
+    fa::reduce_rate_kernel<<<blocks, 128, 2 * 16384, s>>>(static_cast<float*>(scratch), tiles, rounds);
+    cudaEventRecord(e1, s);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    if (e == cudaSuccess && rep > 0 && ms > 0.f)   // the first run is a warm-up
+      best = std::max(best, 16384.0 * blocks * rounds / (ms * 1e-3));
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return fa::cuda_fail(e, "reduce rate kernel");
+  *bytes_per_s = best;
+  return FA_OK;
 }
 
 extern "C" int fa_measure_ex2_rate(double* exps_per_s, fa_stream_t stream) {

@@ -318,6 +318,22 @@ int fa_selftest_expired_wait(int limit_us, fa_stream_t stream);
  */
 int fa_measure_ex2_rate(double *exps_per_s, fa_stream_t stream);
 
+/*
+ * Diagnostics: measures how many bytes per second of fp32 reduce-adds the
+ * SMs of the current device push into global memory together (one CTA per
+ * SM, 16 KB bulk reduce-adds of shared-memory tiles, two in flight per SM),
+ * the resource that bounds the backward's dQ accumulation (dQ is
+ * accumulated across key/value tiles with atomic adds: "FlashAttention-2:
+ * Faster Attention with Better Parallelism and Work Partitioning", paper
+ * digest, section 2 Q2, improvement 2).  scratch: device buffer of
+ * scratch_bytes (at least 1 MiB, 256-byte aligned) the tiles are added into;
+ * zeros are added, so finite contents are unchanged.  Synchronises `stream`
+ * and writes the best of three timed runs to *bytes_per_s.  Returns an
+ * fa_status (FA_ERR_INVALID_ARG for a missing, small or misaligned buffer).
+ */
+int fa_measure_reduce_rate(void *scratch, size_t scratch_bytes, double *bytes_per_s,
+                           fa_stream_t stream);
+
 enum fa_kernel_kind {
   FA_KERNEL_FWD = 0,         /* the forward kernel */
   FA_KERNEL_BWD_PRE = 1,     /* backward preprocess: D and the zeroed dQ accumulator */

@@ -34,6 +34,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert isinstance(getattr(lib, name), ctypes._CFuncPtr), name
 
 
+def test_measure_reduce_rate_rejects_bad_buffers(lib):
+    """Refused on the host, before any launch: no buffer, less than 1 MiB,
+    or not 256-byte aligned."""
+    out = ctypes.c_double(0.0)
+    for ptr, size in ((None, 1 << 24), (FAKE, (1 << 20) - 16), (FAKE + 16, 1 << 24)):
+        st = lib.fa_measure_reduce_rate(ptr, size, ctypes.byref(out), None)
+        assert st == binding.FA_ERR_INVALID_ARG, (ptr, size)
+    assert lib.fa_measure_reduce_rate(FAKE, 1 << 24, None, None) == binding.FA_ERR_INVALID_ARG
+
+
 def test_strerror(lib):
     for st in range(6):
         assert binding.strerror(st)

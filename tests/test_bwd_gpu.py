@@ -112,3 +112,12 @@ def test_backward_full_size_group(name):
                            ("dv", dv[b, kh][None], dv_r[None])], 128, what + " bwd tiles")
     for t in (dq, dk, dv):
         assert torch.isfinite(t.float()).all()
+
+
+def test_reduce_rate_diagnostic():
+    """fa_measure_reduce_rate: a plausible rate (0.5 to 50 TB/s over all SMs)
+    and finite scratch contents left unchanged (zeros are added)."""
+    scratch = torch.full((8 << 20,), 1.5, dtype=torch.float32, device="cuda")
+    rate = binding.measure_reduce_rate(scratch)
+    assert 5e11 < rate < 5e13, rate
+    assert bool((scratch == 1.5).all())
