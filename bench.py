@@ -935,6 +935,7 @@ def dq_reduce(w: Workload, kernel_times, stream):
     second over the kernel's time against the rate measured on this GPU in
     the same run (fa_measure_reduce_rate, 128 MiB of targets like the
     accumulator)."""
+    from exact_io_aware_20_gb300 import binding
     ms, n = kernel_times.get("bwd_main", (0.0, 0))
     if w.d != 128 or not n:
         return None
