@@ -279,7 +279,8 @@ def measure_ex2_rate(stream=None) -> float:
 
 def measure_reduce_rate(scratch: torch.Tensor, stream=None) -> float:
     """Bytes per second of fp32 bulk reduce-adds from every SM into `scratch`
-    (a device tensor of at least 1 MiB; fa_measure_reduce_rate)."""
+    (a device tensor of at least 1 MiB, 256-byte aligned; zeros are added:
+    fa_measure_reduce_rate)."""
     out = ctypes.c_double(0.0)
     _check(load().fa_measure_reduce_rate(ctypes.c_void_p(scratch.data_ptr()),
                                          scratch.numel() * scratch.element_size(),

@@ -327,7 +327,8 @@ int fa_measure_ex2_rate(double *exps_per_s, fa_stream_t stream);
  * Faster Attention with Better Parallelism and Work Partitioning", paper
  * digest, section 2 Q2, improvement 2).  scratch: device buffer of
  * scratch_bytes (at least 1 MiB, 256-byte aligned) the tiles are added into;
- * zeros are added, so finite contents are unchanged.  Synchronises `stream`
+ * zeros are added, so its values are unchanged (a negative zero may become
+ * a positive one).  Synchronises `stream`
  * and writes the best of three timed runs to *bytes_per_s.  Returns an
  * fa_status (FA_ERR_INVALID_ARG for a missing, small or misaligned buffer).
  */
