@@ -350,7 +350,25 @@ def cpu_baseline(w: Workload, target_seconds: float):
     dt = run_oracle_sample(w, q, k, v, do, seg)
     flops = pairs * 4.0 * w.d * 3.5      # metric FLOPs of these pairs: fwd + 2.5x bwd
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "seconds": round(dt, 3), "sample": describe(seg, pairs, w) + f", {threads} threads"}
+            "seconds": round(dt, 3), "cpu": cpu_model(),
+            "sample": describe(seg, pairs, w) + f", {threads} threads"}
+
+
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm
+    implementer / part codes), with the number of logical CPUs."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            for line in f:
+                if ":" in line:
+                    key, val = (s.strip() for s in line.split(":", 1))
+                    fields.setdefault(key, val)
+    except OSError:
+        return "unknown"
+    name = fields.get("model name") or " ".join(
+        f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields) or "unknown"
+    return f"{name}, {os.cpu_count()} logical CPUs"
 
 
 # ---------------------------------------------------------------- reference arm
@@ -380,7 +398,7 @@ def run_reference(args):
                                f"{w.dtype} causal={int(w.causal)}",
                    "sample_per_step": describe(seg, pairs, w)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "per step: " + describe(seg, pairs, w)},
+                         "cpu": cpu_model(), "sample": "per step: " + describe(seg, pairs, w)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -560,13 +578,18 @@ def main():
     with ClockSampler(local) as clocks, NvmlPoller(local) as nvml:
         barrier()
         torch.cuda.synchronize()
+        step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ev0.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             step()
+            step_evs[i].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier()
     binding.device_status()
+    # each step's own time (the line's value is over the whole region)
+    step_ms = [ev0.elapsed_time(step_evs[0])] + \
+        [step_evs[i - 1].elapsed_time(step_evs[i]) for i in range(1, args.steps)]
     kernel_times = binding.timing_read()
     binding.timing_enable(0)
     ms_total = ev0.elapsed_time(ev1)
@@ -711,6 +734,8 @@ def main():
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
+        "ms_per_step_median": round(statistics.median(step_ms), 4),
+        "ms_per_step_min": round(min(step_ms), 4),
         "config": {"workload": f"{w.name}: B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d} "
                                f"{w.dtype} causal={int(w.causal)}, N(0,1) inputs, seed {w.seed}",
                    "step": "fa_fwd + fa_bwd (O, L, dQ, dK, dV)",
