@@ -442,28 +442,42 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const bool diag = CAUSAL && (q0 + p.off < kv0 + kBC);   // tile crosses the diagonal
       const bool masked = __any_sync(0xffffffffu, kv_out || diag);
       const f2 cs = {p.scale_log2, p.scale_log2};
-      float P[BR];
+      // 128 query columns (d = 64): the weights stay in registers as the
+      // 16-bit pairs written to TMEM (64 registers, not 128 in fp32, which
+      // spilled), and dS uses those rounded weights, as dV does
+      constexpr bool kPackP = BR > 64;
+      float P[kPackP ? 1 : BR];
+      uint32_t Pk[kPackP ? BR / 2 : 1];
       #pragma unroll
       for (int c0 = 0; c0 < BR; c0 += 32) {
         uint32_t sr[32];
         tmem_ld32(tS + lane_off + c0, sr);
         tmem_ld_wait();
         reg_fence(sr);
+        float Pc[32];
         #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs,
                                f2{sL[c0 + c], sL[c0 + c + 1]});
-          P[c0 + c] = ex2_approx(arg.x);
-          P[c0 + c + 1] = ex2_approx(arg.y);
+          Pc[c] = ex2_approx(arg.x);
+          Pc[c + 1] = ex2_approx(arg.y);
         }
         if (masked) {
           #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (kv_out || (diag && kv > q0 + c0 + c + p.off)) P[c0 + c] = 0.f;
+            if (kv_out || (diag && kv > q0 + c0 + c + p.off)) Pc[c] = 0.f;
         }
         uint32_t pk[16];
         #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(P[c0 + 2 * c], P[c0 + 2 * c + 1]);
+        for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(Pc[2 * c], Pc[2 * c + 1]);
+        #pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if constexpr (kPackP) {
+            if ((c & 1) == 0) Pk[(c0 + c) / 2] = pk[c / 2];
+          } else {
+            P[c0 + c] = Pc[c];
+          }
+        }
         // P^T (16-bit) goes over the first BR/2 columns of the S^T tile,
         // which this thread has already read.
         tmem_st16(tS + lane_off + c0 / 2, pk);
@@ -488,7 +502,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         for (int c = 0; c < 16; ++c) {
           const f2 diff = fadd2(f2{__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])},
                                 f2{sD[c0 + 2 * c], sD[c0 + 2 * c + 1]});
-          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]}, diff);
+          f2 pv;
+          if constexpr (kPackP) {
+            const float2 u2 = unpack2<BF16>(Pk[c0 / 2 + c]);
+            pv = f2{u2.x, u2.y};
+          } else {
+            pv = f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]};
+          }
+          const f2 ds = fmul2(pv, diff);
           w[c] = pack2<BF16>(ds.x, ds.y);
         }
         #pragma unroll
