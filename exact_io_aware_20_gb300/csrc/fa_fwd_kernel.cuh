@@ -20,9 +20,12 @@
 // only the key tiles of its kept mask blocks, from a list built in shared
 // memory before the warps split up.
 //
-// GB300 design (not the pages' A100 design): one CTA per 128-row query tile,
-// warp-specialised:
-//   warp 0      TMA producer: Q once, then K_j / V_j through two smem rings;
+// GB300 design (not the pages' A100 design): a work unit is one 128-row
+// query tile (of one split of the keys, head, batch); a persistent grid of one
+// CTA per SM walks the units (one CTA per unit with a block mask), TMEM, the
+// barriers and the K / V rings living across units; warp-specialised:
+//   warp 0      TMA producer: each unit's Q, then K_j through a smem ring;
+//   warp 6      TMA producer: V_j through a second ring;
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM score buffers,
 //               O += P_j V_j with P_j read from TMEM (tcgen05 "TS" form);
 //   warps 2..5  softmax: one query row per thread, read S_j from TMEM, mask,
@@ -46,7 +49,7 @@ namespace fa {
 namespace {
 
 constexpr int kBR = 128;             // query rows per tile (= MMA M)
-constexpr int kThreads = 192;        // 6 warps
+constexpr int kThreads = 224;        // 7 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -75,7 +78,8 @@ struct FwdLayout {
   static constexpr int kBarOff = kVOff + VST * kVStage;
   // barrier indices
   static constexpr int kQFull = 0;
-  static constexpr int kKFull = 1;
+  static constexpr int kQEmpty = 1;
+  static constexpr int kKFull = 2;
   static constexpr int kKEmpty = kKFull + KST;
   static constexpr int kVFull = kKEmpty + KST;
   static constexpr int kVEmpty = kVFull + VST;
@@ -134,40 +138,65 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = p.splits > 1 ? static_cast<int>(blockIdx.x) % p.splits : 0;
-  const int xt = p.splits > 1 ? static_cast<int>(blockIdx.x) / p.splits : static_cast<int>(blockIdx.x);
-  const int qt = CAUSAL ? (p.num_q_tiles - 1 - xt) : xt;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int kh = h / p.G;
   const bool packed = p.mask_rows != p.Nq;
-  int n_kv = (p.Nk + BC - 1) / BC;
-  if (CAUSAL) {
-    // last key any row of this tile may see (bottom-right aligned mask);
-    // negative when every row of the tile sees none (only if Nq > Nk)
-    const int max_i = packed ? p.mask_rows - 1 : min((qt + 1) * kBR, p.Nq) - 1;
-    const int last_key = max_i + p.off;
-    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
-  }
-  // key tiles [j_base, j_base + n_kv) of this CTA
-  const int j_base = split * p.tiles_per_split;
-  if (p.splits > 1) n_kv = max(0, min(n_kv, j_base + p.tiles_per_split) - j_base);
+  // Work units (split, query tile, head, batch), numbered with the split
+  // fastest, then query tiles (under the mask the longest first), heads,
+  // batches.  Without a block mask the grid is persistent: CTA c takes unit
+  // k * G + c in even rounds k and k * G + G - 1 - c in odd ones (G = grid
+  // size), so that over two rounds of longest-first units every CTA gets
+  // about the same work.  With a block mask every CTA takes one unit.
+  const int ux = p.num_q_tiles * p.splits;
+  const long long n_units = static_cast<long long>(ux) * p.H * p.B_;
+  auto unit_of = [&](int k) -> long long {
+    if (SPARSE) return k == 0 ? static_cast<long long>(blockIdx.x) : -1;
+    const long long G = gridDim.x;
+    const long long u = k * G + ((k & 1) ? G - 1 - blockIdx.x : blockIdx.x);
+    return u < n_units ? u : -1;
+  };
+  struct Unit {
+    int split, qt, h, b, n_kv, j_base;
+  };
+  auto decode = [&](long long u) {
+    Unit w;
+    const int bx = static_cast<int>(u % ux);
+    const long long hb = u / ux;
+    w.h = static_cast<int>(hb % p.H);
+    w.b = static_cast<int>(hb / p.H);
+    w.split = p.splits > 1 ? bx % p.splits : 0;
+    const int xt = p.splits > 1 ? bx / p.splits : bx;
+    w.qt = CAUSAL ? (p.num_q_tiles - 1 - xt) : xt;
+    int n = (p.Nk + BC - 1) / BC;
+    if (CAUSAL) {
+      // last key any row of this tile may see (bottom-right aligned mask);
+      // negative when every row of the tile sees none (only if Nq > Nk)
+      const int max_i = packed ? p.mask_rows - 1 : min((w.qt + 1) * kBR, p.Nq) - 1;
+      const int last_key = max_i + p.off;
+      n = last_key < 0 ? 0 : min(n, last_key / BC + 1);
+    }
+    // key tiles [j_base, j_base + n) of this split
+    w.j_base = w.split * p.tiles_per_split;
+    if (p.splits > 1) n = max(0, min(n, w.j_base + p.tiles_per_split) - w.j_base);
+    w.n_kv = n;
+    return w;
+  };
   constexpr bool sparse = SPARSE;
   if (sparse && warp == 2) {
     // key tiles of the kept blocks in this query tile's mask row, within n_kv
+    const Unit w = decode(unit_of(0));
     constexpr int kSub = kMaskBlock / BC;
-    const int mh = p.mask.heads == 1 ? 0 : h;
+    const int mh = p.mask.heads == 1 ? 0 : w.h;
     const unsigned char* mrow =
-        p.mask.ptr + (static_cast<size_t>(mh) * p.mask.nbr + qt) * p.mask.nbc;
-    const int lim = n_kv;
+        p.mask.ptr + (static_cast<size_t>(mh) * p.mask.nbr + w.qt) * p.mask.nbc;
+    const int lim = w.n_kv;
     const int cnt = compact_steps<kSub>(
         p.mask.nbc, [&](int e) { return mrow[e] != 0; },
         [&](int e, int sub) { const int j = e * kSub + sub; return j < lim ? j : -1; },
         tile_list, kFwdListCap);
     if (lane == 0) *list_count = min(cnt, kFwdListCap);
   }
-  // key tile of step j
-  auto key_tile = [&](int j) -> int {
-    return sparse ? static_cast<int>(tile_list[j]) : j_base + j;
+  // key tile of step j of unit w
+  auto key_tile = [&](const Unit& w, int j) -> int {
+    return sparse ? static_cast<int>(tile_list[j]) : w.j_base + j;
   };
 
   // the merge of split partials (launched as this grid's dependent) may start
@@ -175,6 +204,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   if (p.splits > 1) grid_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
+    mbar_init(bar(L::kQEmpty), 1);
     for (int s = 0; s < KST; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kKEmpty + s), 1);
@@ -197,7 +227,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     tmem_relinquish();
   }
   if constexpr (L::kOnes) {
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
       // the ones chunks (any layout of all-ones is all-ones), written once
       const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
       for (int sv = 0; sv < VST; ++sv) {
@@ -211,89 +241,121 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (sparse) n_kv = *list_count;
+  // the unit's key tiles: the kept list under a block mask
+  auto unit_at = [&](int k, Unit& w) -> bool {
+    const long long u = unit_of(k);
+    if (u < 0) return false;
+    w = decode(u);
+    if (sparse) w.n_kv = *list_count;
+    return true;
+  };
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS0 = tmem + L::kS0, tS1 = tmem + L::kS1, tO = tmem + L::kO;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop; one elected lane issues the copies.
+    // ------------------------------------------------------------ producer: Q, K
+    // Each unit's Q tile (once the previous unit's last S product has
+    // completed), then its K tiles through the K ring; the V ring has a warp
+    // of its own (warp 6), so that neither stream's waits hold up the
+    // other's loads (in one thread, in order, a V slot waiting for P V(j)
+    // would hold back K(j + 2), which S(j + 2) needs before the MMA warp
+    // issues P V(j + 1)).  The whole warp runs the loop, one elected lane
+    // issues the copies.
     if (elect_one()) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
-      #pragma unroll
-      for (int c = 0; c < L::kNch; ++c)
-        tma_load_4d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, qt * kBR, h, b);
     }
     __syncwarp();
-    int k_issued = 0, v_issued = 0;
-    if constexpr (L::kChunked) {
-      // Two lanes, each with its own ring, so that neither ring's wait holds
-      // up the other's loads: lane 0 streams the K chunks, lane 1 the V
-      // halves (with one ring walked in order, a V half waiting for P V(j)
-      // would hold back K(j + 2), which S(j + 2) needs before P V(j + 1)).
-      if (lane == 0) {
-        for (int ck = 0; ck < n_kv * L::kNch; ++ck) {
-          const int s = ck % KST;
-          if (ck >= KST && !mbar_wait(bar(L::kKEmpty + s), ((ck / KST) + 1) & 1, abort)) break;
-          mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKSlot);
-          tma_load_4d(sbase + L::kKOff + s * L::kKSlot, &tm_k, bar(L::kKFull + s),
-                      (ck % L::kNch) * 64, key_tile(ck / L::kNch) * BC, kh, b);
-          ++k_issued;
-        }
-      } else if (lane == 1) {
-        for (int vh = 0; vh < n_kv * 2; ++vh) {
-          const int sv = vh % VST;
-          if (vh >= VST && !mbar_wait(bar(L::kVEmpty + sv), ((vh / VST) + 1) & 1, abort)) break;
-          mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kVHalf);
-          #pragma unroll
-          for (int c = 0; c < L::kNch; ++c)
-            tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * ((BC / 2) * 128), &tm_v,
-                        bar(L::kVFull + sv), c * 64, key_tile(vh / 2) * BC + (vh & 1) * (BC / 2), kh, b);
-          ++v_issued;
-        }
-      }
-      __syncwarp();
-      k_issued = __shfl_sync(0xffffffffu, k_issued, 0);
-      v_issued = __shfl_sync(0xffffffffu, v_issued, 1);
-    }
-    for (int j = 0; !L::kChunked && j < n_kv; ++j) {
-      const int s = j % KST;
-      if (j >= KST && !wait_uniform(bar(L::kKEmpty + s), ((j / KST) + 1) & 1, abort)) break;
+    int issued = 0, q_issued = 0;   // K pieces, Q tiles
+    bool ok = true;
+    Unit w;
+    for (int k = 0; ok && unit_at(k, w); ++k) {
+      if (k >= 1 && !wait_uniform(bar(L::kQEmpty), (k - 1) & 1, abort)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKVBytes);
+        mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
         #pragma unroll
         for (int c = 0; c < L::kNch; ++c)
-          tma_load_4d(sbase + L::kKOff + s * L::kKVBytes + c * (BC * 128), &tm_k,
-                      bar(L::kKFull + s), c * 64, key_tile(j) * BC, kh, b);
+          tma_load_4d(sbase + L::kQOff + c * (kBR * 128), &tm_q, bar(L::kQFull), c * 64, w.qt * kBR,
+                      w.h, w.b);
       }
       __syncwarp();
-      ++k_issued;
-      const int sv = j % VST;
-      if (j >= VST && !wait_uniform(bar(L::kVEmpty + sv), ((j / VST) + 1) & 1, abort)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
-        #pragma unroll
-        for (int c = 0; c < L::kNch; ++c)
-          tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
-                      bar(L::kVFull + sv), c * 64, key_tile(j) * BC, kh, b);
+      ++q_issued;
+      const int kh = w.h / p.G;
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        #pragma unroll 1
+        for (int c = 0; c < (L::kChunked ? L::kNch : 1); ++c) {
+          const int s = issued % KST;
+          if (issued >= KST && !wait_uniform(bar(L::kKEmpty + s), ((issued / KST) + 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKSlot);
+            if constexpr (L::kChunked) {
+              tma_load_4d(sbase + L::kKOff + s * L::kKSlot, &tm_k, bar(L::kKFull + s), c * 64,
+                          key_tile(w, j) * BC, kh, w.b);
+            } else {
+              #pragma unroll
+              for (int cc = 0; cc < L::kNch; ++cc)
+                tma_load_4d(sbase + L::kKOff + s * L::kKSlot + cc * (BC * 128), &tm_k,
+                            bar(L::kKFull + s), cc * 64, key_tile(w, j) * BC, kh, w.b);
+            }
+          }
+          __syncwarp();
+          ++issued;
+        }
       }
-      __syncwarp();
-      ++v_issued;
     }
     // Never leave the CTA with copies in flight: wait for every load issued
     // (they have completed already on the normal path).
-    drain_wait(bar(L::kQFull), 0);
-    for (int j = max(0, k_issued - KST); j < k_issued; ++j)
-      drain_wait(bar(L::kKFull + j % KST), (j / KST) & 1);
-    for (int j = max(0, v_issued - VST); j < v_issued; ++j)
-      drain_wait(bar(L::kVFull + j % VST), (j / VST) & 1);
+    if (q_issued > 0) drain_wait(bar(L::kQFull), (q_issued - 1) & 1);
+    for (int i = max(0, issued - KST); i < issued; ++i)
+      drain_wait(bar(L::kKFull + i % KST), (i / KST) & 1);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ producer: V
+    int issued = 0;
+    bool ok = true;
+    Unit w;
+    for (int k = 0; ok && unit_at(k, w); ++k) {
+      const int kh = w.h / p.G;
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        #pragma unroll 1
+        for (int hv = 0; hv < (L::kChunked ? 2 : 1); ++hv) {
+          const int sv = issued % VST;
+          if (issued >= VST && !wait_uniform(bar(L::kVEmpty + sv), ((issued / VST) + 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            if constexpr (L::kChunked) {
+              mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kVHalf);
+              #pragma unroll
+              for (int c = 0; c < L::kNch; ++c)
+                tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * ((BC / 2) * 128), &tm_v,
+                            bar(L::kVFull + sv), c * 64, key_tile(w, j) * BC + hv * (BC / 2), kh, w.b);
+            } else {
+              mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
+              #pragma unroll
+              for (int c = 0; c < L::kNch; ++c)
+                tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
+                            bar(L::kVFull + sv), c * 64, key_tile(w, j) * BC, kh, w.b);
+            }
+          }
+          __syncwarp();
+          ++issued;
+        }
+      }
+    }
+    for (int i = max(0, issued - VST); i < issued; ++i)
+      drain_wait(bar(L::kVFull + i % VST), (i / VST) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Warp-wide; each tcgen05 instruction is issued by one elected lane.
-    // Descriptors are built once and advanced by constant offsets.
+    // Descriptors are built once and advanced by constant offsets.  Global
+    // step g counts the CTA's key tiles over all its units: it indexes the
+    // score buffers and the K / V rings, and the parities of S_FULL, P_FULL
+    // and O_DONE.
     constexpr uint32_t kIdS = idesc_f16(kBR, BC, BF16 ? 1 : 0, 0, 0);
     constexpr uint32_t kIdO = idesc_f16(kBR, D + L::kOnesCols, BF16 ? 1 : 0, 0, 1);
     const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
@@ -301,14 +363,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, BC * 128, 1024);
     // a V half: 64-column chunks of BC / 2 keys each
     const uint64_t v_desc_half = smem_desc_sw128(sbase + L::kVOff, (BC / 2) * 128, 1024);
-    auto issue_s = [&](int j) -> bool {
+    auto issue_s = [&](int g) -> bool {
+      const uint32_t d_tmem = (g & 1) ? tS1 : tS0;
       if constexpr (L::kChunked) {
         // one chunk of K (64 columns of d) at a time, each slot freed as soon
         // as its four products are done
-        const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
         #pragma unroll 1
         for (int c = 0; c < L::kNch; ++c) {
-          const int ck = j * L::kNch + c, s = ck % KST;
+          const int ck = g * L::kNch + c, s = ck % KST;
           if (!wait_uniform(bar(L::kKFull + s), (ck / KST) & 1, abort)) return false;
           tc_fence_after();
           const uint64_t ks = desc_add(k_desc, s * L::kKSlot);
@@ -318,231 +380,258 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                    (c > 0 || w > 0) ? 1u : 0u);
           mma_commit(bar(L::kKEmpty + s));
         }
-        mma_commit(bar(L::kSFull + (j & 1)));
+        mma_commit(bar(L::kSFull + (g & 1)));
         return true;
       }
-      const int s = j % KST;
-      if (!wait_uniform(bar(L::kKFull + s), (j / KST) & 1, abort)) return false;
+      const int s = g % KST;
+      if (!wait_uniform(bar(L::kKFull + s), (g / KST) & 1, abort)) return false;
       tc_fence_after();
-      const uint32_t d_tmem = (j & 1) ? tS1 : tS0;
-      const uint64_t ks = desc_add(k_desc, s * L::kKVBytes);
+      const uint64_t ks = desc_add(k_desc, s * L::kKSlot);
       #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t c = kk >> 2, w = kk & 3;
         mma_ss(d_tmem, desc_add(q_desc, c * (kBR * 128) + w * 32),
                desc_add(ks, c * (BC * 128) + w * 32), kIdS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(bar(L::kSFull + (j & 1)));
+      mma_commit(bar(L::kSFull + (g & 1)));
       mma_commit(bar(L::kKEmpty + s));
       return true;
     };
-    bool ok = wait_uniform(bar(L::kQFull), 0, abort);
-    if (ok && n_kv > 0) ok = issue_s(0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      if (j + 1 < n_kv && !issue_s(j + 1)) break;
-      if (!wait_uniform(bar(L::kPFull + (j & 1)), (j >> 1) & 1, abort)) break;
-      if constexpr (L::kChunked) {
-        // P V over one half of the keys at a time
-        const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
-        bool vok = true;
-        #pragma unroll 1
-        for (int hv = 0; hv < 2; ++hv) {
-          const int vh = 2 * j + hv, sv = vh % VST;
-          if (!wait_uniform(bar(L::kVFull + sv), (vh / VST) & 1, abort)) {
-            vok = false;
-            break;
+    // The step index that selects ring slots and score buffers (and so the
+    // MMA descriptors) is read from lane 0 where it is used: the compiler
+    // then knows it is the same in every lane and keeps the descriptor
+    // arithmetic on the uniform datapath; computed from the unit loop it
+    // did not, and each key tile's products took ~10% longer to issue
+    // (head256 forward 355 -> 380 us).
+    bool ok = true;
+    int g = 0;                 // key tiles so far
+    Unit w;
+    for (int k = 0; ok && unit_at(k, w); ++k) {
+      const int n = w.n_kv;
+      ok = wait_uniform(bar(L::kQFull), k & 1, abort);
+      if (ok && n > 0) ok = issue_s(__shfl_sync(0xffffffffu, g, 0));
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          if (!issue_s(__shfl_sync(0xffffffffu, g + j + 1, 0))) { ok = false; break; }
+        } else {
+          mma_commit(bar(L::kQEmpty));     // the unit's last S has been issued
+        }
+        if (!wait_uniform(bar(L::kPFull + ((g + j) & 1)), ((g + j) >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        // O += P V (the first of a unit overwrites O: every softmax thread
+        // reads the previous unit's O out, and waits for the loads, before
+        // it turns to this unit's scores, so P_FULL of this tile implies O
+        // is free).
+        const int gj = __shfl_sync(0xffffffffu, g + j, 0);
+        const uint32_t a_tmem = (gj & 1) ? tS1 : tS0;
+        if constexpr (L::kChunked) {
+          // one half of the keys at a time
+          #pragma unroll 1
+          for (int hv = 0; hv < 2; ++hv) {
+            const int vh = 2 * gj + hv, sv = vh % VST;
+            if (!wait_uniform(bar(L::kVFull + sv), (vh / VST) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vs = desc_add(v_desc_half, sv * L::kVStage);
+            #pragma unroll
+            for (int w2 = 0; w2 < BC / 32; ++w2)
+              mma_ts(tO, a_tmem + (hv * (BC / 32) + w2) * 8, desc_add(vs, w2 * 2048), kIdO,
+                     (j > 0 || hv > 0 || w2 > 0) ? 1u : 0u);
+            mma_commit(bar(L::kVEmpty + sv));
           }
+          if (!ok) break;
+          mma_commit(bar(L::kODone));
+        } else {
+          const int sv = gj % VST;
+          if (!wait_uniform(bar(L::kVFull + sv), (gj / VST) & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t vs = desc_add(v_desc_half, sv * L::kVStage);
+          const uint64_t vs = desc_add(v_desc, sv * L::kVStage);
           #pragma unroll
-          for (int w = 0; w < BC / 32; ++w)
-            mma_ts(tO, a_tmem + (hv * (BC / 32) + w) * 8, desc_add(vs, w * 2048), kIdO,
-                   (j > 0 || hv > 0 || w > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BC / 16; ++kk)
+            mma_ts(tO, a_tmem + kk * 8, desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(L::kODone));
           mma_commit(bar(L::kVEmpty + sv));
         }
-        if (!vok) break;
-        mma_commit(bar(L::kODone));
-        continue;
       }
-      const int sv = j % VST;
-      if (!wait_uniform(bar(L::kVFull + sv), (j / VST) & 1, abort)) break;
-      tc_fence_after();
-      const uint32_t a_tmem = (j & 1) ? tS1 : tS0;
-      const uint64_t vs = desc_add(v_desc, sv * L::kVStage);
-      #pragma unroll
-      for (int kk = 0; kk < BC / 16; ++kk)
-        mma_ts(tO, a_tmem + kk * 8, desc_add(vs, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(bar(L::kODone));
-      mma_commit(bar(L::kVEmpty + sv));
+      if (!ok) break;
+      if (n == 0) mma_commit(bar(L::kQEmpty));
+      g += n;
     }
     // Every MMA issued above completes before TMEM is released.
     mma_commit(bar(L::kDrain));
     drain_wait(bar(L::kDrain), 0);
   } else {
-    // ------------------------------------------------------------ softmax
+    // ------------------------------------------------------------ softmax (warps 2..5)
     const int quarter = warp & 3;                 // TMEM lanes this warp may access
     const int r_tile = quarter * 32 + lane;
-    const int row = qt * kBR + r_tile;
-    const int qi = row % p.mask_rows;             // query index of this row for the mask
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
     bool ok = true;
-    // A warp whose 32 rows all lie past the last query row (short or packed
-    // queries) only keeps the barrier protocol: its Q rows are zero-filled,
-    // so its scores are 0 and the P it leaves in TMEM is 0, and its rows are
-    // never stored.
-    const bool idle = qt * kBR + quarter * 32 >= p.Nq;
-    for (int j = 0; j < n_kv; ++j) {
-      const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
-      if (!wait_uniform(bar(L::kSFull + (j & 1)), (j >> 1) & 1, abort)) { ok = false; break; }
-      tc_fence_after();
-      if (idle) {
-        if (j > 0 && j == n_kv - 1 && !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) {
+    int g = 0;
+    Unit w;
+    for (int k = 0; ok && unit_at(k, w); ++k) {
+      const int n_kv = w.n_kv, qt = w.qt, h = w.h, b = w.b, split = w.split;
+      const int row = qt * kBR + r_tile;
+      const int qi = row % p.mask_rows;             // query index of this row for the mask
+      float m_ref = -INFINITY, l = 0.f, l_r = 0.f;
+      // A warp whose 32 rows all lie past the last query row (short or packed
+      // queries) only keeps the barrier protocol: its Q rows are zero-filled,
+      // so its scores are 0 and the P it leaves in TMEM is 0, and its rows are
+      // never stored.
+      const bool idle = qt * kBR + quarter * 32 >= p.Nq;
+      for (int j = 0; j < n_kv; ++j) {
+        // read from lane 0: a known warp-uniform TMEM address (see the MMA warp)
+        const int gj = __shfl_sync(0xffffffffu, g + j, 0);
+        const uint32_t tS = ((gj & 1) ? tS1 : tS0) + lane_off;
+        if (!wait_uniform(bar(L::kSFull + (gj & 1)), (gj >> 1) & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        if (idle) {
+          if (j > 0 && j == n_kv - 1 && !wait_uniform(bar(L::kODone), (gj - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_before();
+          mbar_arrive(bar(L::kPFull + (gj & 1)));
+          continue;
+        }
+        uint32_t sr[BC];
+        #pragma unroll
+        for (int c = 0; c < BC / 32; ++c)
+          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_ld_wait();
+        reg_fence(sr);
+        float* s = reinterpret_cast<float*>(sr);
+        const int col0 = key_tile(w, j) * BC;
+        const int min_i = packed ? 0 : qt * kBR;
+        const bool need_mask = (CAUSAL && col0 + BC - 1 > min_i + p.off) || (col0 + BC > p.Nk);
+        if (need_mask) {
+          // columns [0, lim) of the tile are kept (one comparison per score)
+          const int lim = min(p.Nk - col0, CAUSAL ? qi + p.off - col0 + 1 : BC);
+          #pragma unroll
+          for (int i = 0; i < BC; ++i)
+            if (i >= lim) s[i] = -INFINITY;
+        }
+        // Row max as a tree of three-input maxima (independent partial maxima
+        // keep the single warp per sub-partition busy instead of waiting on a
+        // 127-long dependent chain).
+        static_assert(BC % 16 == 0, "row max tree covers 16 columns per step");
+        float mpart[8];
+        #pragma unroll
+        for (int u = 0; u < 8; ++u) mpart[u] = fmaxf(s[2 * u], s[2 * u + 1]);
+        #pragma unroll
+        for (int i = 16; i < BC; i += 16) {
+          #pragma unroll
+          for (int u = 0; u < 8; ++u) mpart[u] = fmax3(mpart[u], s[i + 2 * u], s[i + 2 * u + 1]);
+        }
+        const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
+                               fmaxf(mpart[6], mpart[7]));
+        const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        const bool any = __any_sync(0xffffffffu, need);
+        float alpha = 1.f;
+        if (any) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          l *= alpha;
+          l_r *= alpha;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        uint32_t pk[BC / 2];
+        // Exponent arguments two at a time (packed FMA); four independent
+        // partial sums of each kind (exact, and of the rounded weights).
+        f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        float rs_r[4] = {0.f, 0.f, 0.f, 0.f};
+        const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
+        #pragma unroll
+        for (int i = 0; i < BC / 2; ++i) {
+          const f2 arg = ffma2(f2{s[2 * i], s[2 * i + 1]}, cs, cm);
+          const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
+          pk[i] = pack2<BF16>(pe.x, pe.y);
+          rs[i & 3] = fadd2(rs[i & 3], pe);
+          // l_r sums the rounded weights the P V product uses, so the final
+          // division of O normalises exactly those weights; L uses the exact l.
+          // With the ones chunk the tensor core forms l_r next to O instead.
+          if constexpr (!L::kOnes) rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
+        }
+        const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+        l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
+        l_r += (rs_r[0] + rs_r[1]) + (rs_r[2] + rs_r[3]);
+        #pragma unroll
+        for (int c = 0; c < BC / 64; ++c)
+          tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
+        tmem_st_wait();
+        // O_DONE completes once per P V product.  S(g) was issued after
+        // P V(g-2), and its S_FULL completes only once every earlier product
+        // of the issuing thread has, so here only P V(g-1) can be outstanding
+        // and the barrier is at P V(g-1)'s phase or one past it: a parity
+        // wait for it is exact even when earlier phases were not waited for.
+        // It is needed before a rescale of O, and on the last tile (so that
+        // at the epilogue only the last product can be outstanding).  The
+        // first tile of a unit has no earlier product on O to wait for.
+        if (j > 0 && (any || j == n_kv - 1) &&
+            !wait_uniform(bar(L::kODone), (gj - 1) & 1, abort)) {
           ok = false;
           break;
         }
+        if (any && j > 0) {
+          // O holds P_0..P_{j-1} V, all complete: rescale it.
+          tc_fence_after();
+          #pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t o2[64];
+            tmem_ld32(tO + lane_off + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
+            tmem_ld32(tO + lane_off + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
+            tmem_ld_wait();
+            reg_fence(o2);
+            #pragma unroll
+            for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
+            tmem_st32(tO + lane_off + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
+            tmem_st32(tO + lane_off + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
+          }
+          if constexpr (L::kOnes) {
+            uint32_t lr[16];
+            tmem_ld16(tO + lane_off + D, lr);
+            tmem_ld_wait();
+            reg_fence(lr);
+            #pragma unroll
+            for (int i = 0; i < 16; ++i) lr[i] = __float_as_uint(__uint_as_float(lr[i]) * alpha);
+            tmem_st16(tO + lane_off + D, lr);
+          }
+          tmem_st_wait();
+        }
         tc_fence_before();
-        mbar_arrive(bar(L::kPFull + (j & 1)));
+        mbar_arrive(bar(L::kPFull + (gj & 1)));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      const size_t rows_total = static_cast<size_t>(p.B_) * p.H * p.Nq;
+      const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
+      const bool in_range = row < p.Nq;
+      if (n_kv == 0) {
+        // no row of this tile sees any key (of this split's range): O = 0,
+        // L = -inf, as the final result or as this split's partial
+        if (in_range) {
+          const size_t r = row_base + row;
+          if (p.splits > 1) {
+            const size_t rp = split * rows_total + r;
+            float4* prow = reinterpret_cast<float4*>(p.o_part + rp * D);
+            #pragma unroll
+            for (int i = 0; i < D / 4; ++i) prow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.lse_part[rp] = -INFINITY;
+          } else {
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
+                                                   h * p.o_sh + row * p.o_sn);
+            #pragma unroll
+            for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[r] = -INFINITY;
+          }
+        }
         continue;
       }
-      uint32_t sr[BC];
-      #pragma unroll
-      for (int c = 0; c < BC / 32; ++c)
-        tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_ld_wait();
-      reg_fence(sr);
-      float* s = reinterpret_cast<float*>(sr);
-      const int col0 = key_tile(j) * BC;
-      const int min_i = packed ? 0 : qt * kBR;
-      const bool need_mask = (CAUSAL && col0 + BC - 1 > min_i + p.off) || (col0 + BC > p.Nk);
-      if (need_mask) {
-        // columns [0, lim) of the tile are kept (one comparison per score)
-        const int lim = min(p.Nk - col0, CAUSAL ? qi + p.off - col0 + 1 : BC);
-        #pragma unroll
-        for (int i = 0; i < BC; ++i)
-          if (i >= lim) s[i] = -INFINITY;
-      }
-      // Row max as a tree of three-input maxima (independent partial maxima
-      // keep the single warp per sub-partition busy instead of waiting on a
-      // 127-long dependent chain).
-      static_assert(BC % 16 == 0, "row max tree covers 16 columns per step");
-      float mpart[8];
-      #pragma unroll
-      for (int u = 0; u < 8; ++u) mpart[u] = fmaxf(s[2 * u], s[2 * u + 1]);
-      #pragma unroll
-      for (int i = 16; i < BC; i += 16) {
-        #pragma unroll
-        for (int u = 0; u < 8; ++u) mpart[u] = fmax3(mpart[u], s[i + 2 * u], s[i + 2 * u + 1]);
-      }
-      const float mx = fmax3(fmax3(mpart[0], mpart[1], mpart[2]), fmax3(mpart[3], mpart[4], mpart[5]),
-                             fmaxf(mpart[6], mpart[7]));
-      const float m_new = fmaxf(m_ref, mx * p.scale_log2);
-      const bool need = m_new > m_ref + kRescaleThreshold;
-      const bool any = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (any) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-        l *= alpha;
-        l_r *= alpha;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      uint32_t pk[BC / 2];
-      // Exponent arguments two at a time (packed FMA); four independent
-      // partial sums of each kind (exact, and of the rounded weights).
-      f2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-      float rs_r[4] = {0.f, 0.f, 0.f, 0.f};
-      const f2 cs = {p.scale_log2, p.scale_log2}, cm = {-m_use, -m_use};
-      #pragma unroll
-      for (int i = 0; i < BC / 2; ++i) {
-        const f2 arg = ffma2(f2{s[2 * i], s[2 * i + 1]}, cs, cm);
-        const f2 pe = {ex2_approx(arg.x), ex2_approx(arg.y)};
-        pk[i] = pack2<BF16>(pe.x, pe.y);
-        rs[i & 3] = fadd2(rs[i & 3], pe);
-        // l_r sums the rounded weights the P V product uses, so the final
-        // division of O normalises exactly those weights; L uses the exact l.
-        // With the ones chunk the tensor core forms l_r next to O instead.
-        if constexpr (!L::kOnes) rs_r[i & 3] = add_packed<BF16>(rs_r[i & 3], pk[i]);
-      }
-      const f2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
-      l += (rs01.x + rs01.y) + (rs23.x + rs23.y);
-      l_r += (rs_r[0] + rs_r[1]) + (rs_r[2] + rs_r[3]);
-      #pragma unroll
-      for (int c = 0; c < BC / 64; ++c)
-        tmem_st32(tS + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * c]));
-      tmem_st_wait();
-      // O_DONE completes once per P V product.  S(j) was issued after
-      // P V(j-2), and its S_FULL completes only once every earlier product of
-      // the issuing thread has, so here only P V(j-1) can be outstanding and
-      // the barrier is at P V(j-1)'s phase or one past it: a parity wait for
-      // it is exact even when earlier phases were not waited for.  It is
-      // needed before a rescale of O, and on the last tile (so that at the
-      // epilogue only the last product can be outstanding).
-      if (j > 0 && (any || j == n_kv - 1) &&
-          !wait_uniform(bar(L::kODone), (j - 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      if (any && j > 0) {
-        // O holds P_0..P_{j-1} V, all complete: rescale it.
-        tc_fence_after();
-        #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t o2[64];
-          tmem_ld32(tO + lane_off + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&o2[0]));
-          tmem_ld32(tO + lane_off + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&o2[32]));
-          tmem_ld_wait();
-          reg_fence(o2);
-          #pragma unroll
-          for (int i = 0; i < 64; ++i) o2[i] = __float_as_uint(__uint_as_float(o2[i]) * alpha);
-          tmem_st32(tO + lane_off + 64 * c, *reinterpret_cast<const uint32_t(*)[32]>(&o2[0]));
-          tmem_st32(tO + lane_off + 64 * c + 32, *reinterpret_cast<const uint32_t(*)[32]>(&o2[32]));
-        }
-        if constexpr (L::kOnes) {
-          uint32_t lr[16];
-          tmem_ld16(tO + lane_off + D, lr);
-          tmem_ld_wait();
-          reg_fence(lr);
-          #pragma unroll
-          for (int i = 0; i < 16; ++i) lr[i] = __float_as_uint(__uint_as_float(lr[i]) * alpha);
-          tmem_st16(tO + lane_off + D, lr);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(L::kPFull + (j & 1)));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && p.splits > 1 && n_kv == 0) {
-      // this split holds no key of these rows: partial O = 0, L = -inf
-      if (row < p.Nq) {
-        const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
-        const size_t rows_total = static_cast<size_t>(gridDim.z) * p.H * p.Nq;
-        float4* orow = reinterpret_cast<float4*>(p.o_part + (split * rows_total + r) * D);
-        #pragma unroll
-        for (int i = 0; i < D / 4; ++i) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.lse_part[split * rows_total + r] = -INFINITY;
-      }
-    } else if (ok && n_kv == 0) {
-      // no row of this tile sees any key (of this split's range): O = 0,
-      // L = -inf, as the final result or as this split's partial
-      if (row < p.Nq) {
-        const size_t r = (static_cast<size_t>(b) * p.H + h) * p.Nq + row;
-        if (p.splits > 1) {
-          const size_t rp = split * (static_cast<size_t>(gridDim.z) * p.H * p.Nq) + r;
-          float4* prow = reinterpret_cast<float4*>(p.o_part + rp * D);
-          #pragma unroll
-          for (int i = 0; i < D / 4; ++i) prow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          p.lse_part[rp] = -INFINITY;
-        } else {
-          uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
-                                                 h * p.o_sh + row * p.o_sn);
-          #pragma unroll
-          for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[r] = -INFINITY;
-        }
-      }
-    } else if (ok && wait_uniform(bar(L::kODone), (n_kv - 1) & 1, abort)) {
+      if (!wait_uniform(bar(L::kODone), (g + n_kv - 1) & 1, abort)) { ok = false; break; }
       tc_fence_after();
       if constexpr (L::kOnes) {
         uint32_t lr[16];
@@ -553,11 +642,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       }
       const float inv_l = l_r > 0.f ? 1.f / l_r : 0.f;
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-      const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
-      const bool in_range = row < p.Nq;
       if (p.splits > 1) {
         // partial result of this key range, combined by fwd_combine_splits
-        const size_t rows_total = static_cast<size_t>(gridDim.z) * p.H * p.Nq;
         const size_t r = split * rows_total + row_base + (in_range ? row : 0);
         float4* orow = reinterpret_cast<float4*>(p.o_part + r * D);
         #pragma unroll
@@ -576,26 +662,27 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
         if (in_range) p.lse_part[r] = lse;
       } else {
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
-                                             h * p.o_sh + (in_range ? row : 0) * p.o_sn);
-      #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o1[32];
-        tmem_ld32(tO + lane_off + 32 * c, o1);
-        tmem_ld_wait();
-        reg_fence(o1);
-        uint32_t w[16];
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + b * p.o_sb +
+                                               h * p.o_sh + (in_range ? row : 0) * p.o_sn);
         #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l, __uint_as_float(o1[2 * i + 1]) * inv_l);
-        if (in_range) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o1[32];
+          tmem_ld32(tO + lane_off + 32 * c, o1);
+          tmem_ld_wait();
+          reg_fence(o1);
+          uint32_t wv[16];
           #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            orow[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 16; ++i)
+            wv[i] = pack2<BF16>(__uint_as_float(o1[2 * i]) * inv_l, __uint_as_float(o1[2 * i + 1]) * inv_l);
+          if (in_range) {
+            #pragma unroll
+            for (int i = 0; i < 4; ++i)
+              orow[c * 4 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+          }
         }
+        if (in_range) p.lse[row_base + row] = lse;
       }
-      if (in_range) p.lse[row_base + row] = lse;
-      }
+      g += n_kv;
     }
   }
 
@@ -1223,6 +1310,7 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   p.num_q_tiles = (p.Nq + kBR - 1) / kBR;
   p.scale_log2 = pr.scale * 1.4426950408889634f;
   p.err = pr.err;
+  p.B_ = pr.B;
   const int n_kv_tiles = (pr.Nk + BC - 1) / BC;
   p.splits = 1;
   p.tiles_per_split = n_kv_tiles;
@@ -1245,7 +1333,19 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   p.o_sh = ov.h;
   p.o_sn = ov.n;
   if ((e = make_tmap_4d(&tq, a.q, D, p.Nq, p.H, pr.B, qv, 64, kBR)) != cudaSuccess) return e;
-  dim3 grid(p.num_q_tiles * p.splits, p.H, pr.B);
+  // persistent: one CTA per SM walking the units (one CTA per unit with a
+  // block mask, whose key-tile list is built per CTA)
+  static int n_sms = 0;
+  if (n_sms == 0) {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+  }
+  const long long n_units = static_cast<long long>(p.num_q_tiles) * p.splits * p.H * pr.B;
+  if (n_units >= (1ll << 31)) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(SPARSE ? n_units : std::min<long long>(n_units, std::max(n_sms, 1))),
+                  1, 1);
   const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
   timing_end(slot, stream);

@@ -191,17 +191,29 @@ def test_persistent_forward_protocol(seed):
     assert run(units, seed), f"protocol stalled: units {units}"
 
 
-def run_one_tile(n, kst, vst, seed, kp=1, vp=1):
+def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
     """The one-tile forward (d = 64 / 256, short, split and block-sparse
-    paths): S(j+1) is issued before P V(j), into the other of two score
-    buffers, and the softmax waits for O_DONE only before a rescale of O and
-    on the last tile.  kp, vp: pieces per K and V tile (d = 256: four
-    64-column chunks of K, two halves of V); the rings then hold kst and vst
-    pieces, each freed by a commit after the products that read it.  Every
-    product checks, when it runs, that the ring slots it reads hold the
-    pieces of its own tile."""
+    paths), persistent: one CTA walks the units of `units` (their key-tile
+    counts, 0 allowed) one after another.  Per key tile: S(g+1) is issued
+    before P V(g), into the other of two score buffers, and the softmax waits
+    for O_DONE only before a rescale of O and on the last tile of a unit.  Per
+    unit: Q is loaded once the previous unit's last S has completed (Q_EMPTY,
+    committed after that S is issued); its first P V overwrites O with no
+    wait of its own, since every softmax warp reads the previous unit's O out
+    before it arrives on P_FULL for this unit's first tile (the model checks
+    that the read-out finds the unit's last product).  kp, vp: pieces per K and V tile (d = 256: four 64-column
+    chunks of K, two halves of V); the rings then hold kst and vst pieces.
+    Q and K are loaded by one producer lane, V by another, each with its own
+    waits.
+    Global indices (tiles over all units) give the parities.  Every product
+    checks, when it runs, that Q and the ring slots it reads hold its own
+    unit's and tile's pieces and that it reads the P of its own tile; the
+    epilogue that O holds the unit's last product.  plant: None or a mistake
+    ("no_qempty_wait", "early_qempty", "early_p_full": a softmax warp arrives
+    on P_FULL of a unit's first tile before its read-out of the previous
+    unit's O)."""
     rnd = random.Random(seed)
-    B = {"QFull": Bar(1), "ODone": Bar(1)}
+    B = {"QFull": Bar(1), "QEmpty": Bar(1), "ODone": Bar(1)}
     for s in range(kst):
         B[f"KF{s}"], B[f"KE{s}"] = Bar(1), Bar(1)
     for s in range(vst):
@@ -209,104 +221,127 @@ def run_one_tile(n, kst, vst, seed, kp=1, vp=1):
     for s in range(2):
         B[f"SF{s}"] = Bar(1)
         B[f"PF{s}"] = Bar(4)           # the model's four softmax warps
-    loads, pipe, slot = [], [], {}
+    loads, pipe, content = [], [], {}
 
-    def k_pieces(j):
-        for c in range(kp):
-            ck = j * kp + c
-            if ck >= kst:
-                while not B[f"KE{ck % kst}"].done(((ck // kst) + 1) & 1):
-                    yield
-            loads.append((f"KF{ck % kst}", f"K{ck % kst}", (j, c)))
+    def wait(name, parity):
+        while not B[name].done(parity):
+            yield
 
-    def v_pieces(j):
-        for h in range(vp):
-            vh = j * vp + h
-            if vh >= vst:
-                while not B[f"VE{vh % vst}"].done(((vh // vst) + 1) & 1):
-                    yield
-            loads.append((f"VF{vh % vst}", f"V{vh % vst}", (j, h)))
-
-    def producer():
-        # whole tiles: one lane walks K and V in turn; pieces: the K ring
-        # here, the V ring in producer_v (another lane)
-        loads.append(("QFull", None, None))
-        for j in range(n):
-            yield from k_pieces(j)
-            if kp == 1:
-                yield from v_pieces(j)
-
-    def producer_v():
-        if kp > 1:
+    def producer_ring(tag, slots, pieces):
+        # tag K: this lane also loads each unit's Q before the unit's K pieces
+        i = 0
+        for k, n in enumerate(units):
+            if tag == "K":
+                if k >= 1 and plant != "no_qempty_wait":
+                    yield from wait("QEmpty", (k - 1) & 1)
+                loads.append(("QFull", "Q", k))
             for j in range(n):
-                yield from v_pieces(j)
+                for c in range(pieces):
+                    s = i % slots
+                    if i >= slots:
+                        yield from wait(f"{tag}E{s}", ((i // slots) + 1) & 1)
+                    loads.append((f"{tag}F{s}", f"{tag}{s}", (k, j, c)))
+                    i += 1
 
     def mma():
-        def issue_s(j):
+        def issue_s(g, k, j):
             for c in range(kp):
-                ck = j * kp + c
-                while not B[f"KF{ck % kst}"].done((ck // kst) & 1):
-                    yield
-                pipe.append(("mma", f"S{j & 1}"))
-                pipe.append(("check", f"K{ck % kst}", (j, c)))   # what the product read
-                pipe.append(("commit", f"KE{ck % kst}"))
-            pipe.append(("commit", f"SF{j & 1}"))
-        while not B["QFull"].done(0):
-            yield
-        if n > 0:
-            yield from issue_s(0)
-        for j in range(n):
-            if j + 1 < n:
-                yield from issue_s(j + 1)
-            while not B[f"PF{j & 1}"].done((j >> 1) & 1):
-                yield
+                i = g * kp + c
+                yield from wait(f"KF{i % kst}", (i // kst) & 1)
+                pipe.append(("mma", f"S{g & 1}", ("S", g)))
+                pipe.append(("check", "Q", k))
+                pipe.append(("check", f"K{i % kst}", (k, j, c)))
+                pipe.append(("commit", f"KE{i % kst}"))
+            pipe.append(("commit", f"SF{g & 1}"))
+
+        def issue_pv(g, k, j):
             for h in range(vp):
-                vh = j * vp + h
-                while not B[f"VF{vh % vst}"].done((vh // vst) & 1):
-                    yield
-                pipe.append(("mma", f"S{j & 1}", "O"))       # P V(j): P from buffer j & 1
-                pipe.append(("check", f"V{vh % vst}", (j, h)))
-                pipe.append(("commit", f"VE{vh % vst}"))
+                i = g * vp + h
+                yield from wait(f"VF{i % vst}", (i // vst) & 1)
+                pipe.append(("check", f"S{g & 1}", ("P", g)))
+                pipe.append(("mma", f"S{g & 1}", "O", ("O", k, j)))
+                pipe.append(("check", f"V{i % vst}", (k, j, h)))
+                pipe.append(("commit", f"VE{i % vst}"))
             pipe.append(("commit", "ODone"))
+        g = 0
+        for k, n in enumerate(units):
+            yield from wait("QFull", k & 1)
+            if n > 0:
+                if plant == "early_qempty" and n == 1:
+                    pipe.append(("commit", "QEmpty"))
+                yield from issue_s(g, k, 0)
+            for j in range(n):
+                if j + 1 < n:
+                    yield from issue_s(g + j + 1, k, j + 1)
+                elif not (plant == "early_qempty" and n == 1):
+                    pipe.append(("commit", "QEmpty"))
+                yield from wait(f"PF{(g + j) & 1}", ((g + j) >> 1) & 1)
+                yield from issue_pv(g + j, k, j)
+            if n == 0:
+                pipe.append(("commit", "QEmpty"))
+            g += n
 
     def busy(region):
         return any(op[0] == "mma" and region in op[1:] for op in pipe)
 
     def softmax():
-        for j in range(n):
-            while not B[f"SF{j & 1}"].done((j >> 1) & 1):
+        g = 0
+        pending = None                 # (unit, last tile) whose O is still to be read out
+        for k, n in enumerate(units):
+            for j in range(n):
+                gj = g + j
+                yield from wait(f"SF{gj & 1}", (gj >> 1) & 1)
+                assert not busy(f"S{gj & 1}"), "score buffer read while a product uses it"
+                assert content.get(f"S{gj & 1}") in (("S", gj), ("P", gj)), "scores of another tile"
                 yield
-            assert not busy(f"S{j & 1}"), "score buffer read while a product uses it"
-            yield
-            rescale = j > 0 and rnd.random() < 0.3
-            if j > 0 and (rescale or j == n - 1):
-                while not B["ODone"].done((j - 1) & 1):
-                    yield
-            if rescale:
-                assert not busy("O"), "O rescaled while a P V is in flight"
-            B[f"PF{j & 1}"].arrive()
-        if n > 0:
-            while not B["ODone"].done((n - 1) & 1):
-                yield
-            assert not busy("O"), "O read out while a P V is in flight"
+                content[f"S{gj & 1}"] = ("P", gj)
+                rescale = j > 0 and rnd.random() < 0.3
+                if j > 0 and (rescale or j == n - 1):
+                    yield from wait("ODone", (gj - 1) & 1)
+                if rescale:
+                    assert not busy("O"), "O rescaled while a P V is in flight"
+                    assert content.get("O") == ("O", k, j - 1), "O rescaled holding another tile's sum"
+                B[f"PF{gj & 1}"].arrive()
+                if pending is not None:
+                    yield from read_out(*pending)
+                    pending = None
+            if n > 0:
+                yield from wait("ODone", (g + n - 1) & 1)
+                if plant == "early_p_full":
+                    pending = (k, n - 1)       # read out after the next arrival
+                else:
+                    yield from read_out(k, n - 1)
+            g += n
+        if pending is not None:
+            yield from read_out(*pending)
 
-    roles = [producer(), producer_v(), mma()] + [softmax() for _ in range(4)]
+    def read_out(k, last):
+        yield
+        assert not busy("O"), "O read out while a P V is in flight"
+        assert content.get("O") == ("O", k, last), "O read out without the unit's last product"
+        yield
+
+    roles = [producer_ring("K", kst, kp), producer_ring("V", vst, vp), mma()] + \
+        [softmax() for _ in range(4)]
     alive = list(range(len(roles)))
-    for _ in range(2_000_000):
+    for _ in range(300_000):
         if not alive and not loads and not pipe:
             return True
         r = rnd.random()
         if loads and (r < 0.2 or not alive):
             bar, key, val = loads.pop(rnd.randrange(len(loads)))
-            if key is not None:
-                slot[key] = val
+            content[key] = val
             B[bar].arrive()
         elif pipe and (r < 0.45 or not alive):
             op = pipe.pop(0)
             if op[0] == "commit":
                 B[op[1]].arrive()
             elif op[0] == "check":
-                assert slot.get(op[1]) == op[2], "a product read a ring slot holding another piece"
+                assert content.get(op[1]) == op[2], f"a product read {op[1]} holding another piece"
+            elif len(op) == 4:
+                content[op[2]] = op[3]
+            elif len(op) == 3:
+                content[op[1]] = op[2]
         elif alive:
             k = rnd.choice(alive)
             try:
@@ -316,11 +351,14 @@ def run_one_tile(n, kst, vst, seed, kp=1, vp=1):
     return False
 
 
+def random_units(rnd):
+    return [rnd.choice([0, 1, 1, 2, 3, 5]) for _ in range(rnd.randint(1, 5))]
+
+
 @pytest.mark.parametrize("seed", range(30))
 def test_one_tile_forward_protocol(seed):
     rnd = random.Random(seed)
-    assert run_one_tile(rnd.choice([0, 1, 2, 3, 5, 9]), rnd.choice([2, 3]), rnd.choice([2, 3]),
-                        seed)
+    assert run_one_tile(random_units(rnd), rnd.choice([2, 3]), rnd.choice([2, 3]), seed)
 
 
 @pytest.mark.parametrize("seed", range(30))
@@ -328,5 +366,20 @@ def test_one_tile_forward_protocol_in_pieces(seed):
     """d = 256: K in four chunks through a ring of four to six, V in two
     halves through a ring of two or three, each ring loaded by its own lane."""
     rnd = random.Random(seed)
-    assert run_one_tile(rnd.choice([0, 1, 2, 3, 5, 9]), rnd.choice([4, 5, 6]), rnd.choice([2, 3]),
-                        seed, kp=4, vp=2)
+    assert run_one_tile(random_units(rnd), rnd.choice([4, 5, 6]), rnd.choice([2, 3]), seed, kp=4, vp=2)
+
+
+@pytest.mark.parametrize("plant", ["no_qempty_wait", "early_qempty", "early_p_full"])
+def test_one_tile_model_catches_a_planted_mistake(plant):
+    caught = 0
+    for seed in range(60):
+        rnd = random.Random(500 + seed)
+        units = [rnd.choice([1, 1, 2, 3]) for _ in range(rnd.randint(2, 5))]
+        try:
+            finished = run_one_tile(units, 2, 2, seed, plant=plant)
+        except AssertionError:
+            caught += 1
+            continue
+        if not finished:      # a hang: a barrier phase completed twice unseen
+            caught += 1
+    assert caught > 0
