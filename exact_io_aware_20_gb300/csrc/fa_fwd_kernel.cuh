@@ -397,19 +397,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mma_commit(bar(L::kKEmpty + s));
       return true;
     };
-    // The step index that selects ring slots and score buffers (and so the
-    // MMA descriptors) is read from lane 0 where it is used: the compiler
-    // then knows it is the same in every lane and keeps the descriptor
-    // arithmetic on the uniform datapath; computed from the unit loop it
-    // did not, and each key tile's products took ~10% longer to issue
-    // (head256 forward 355 -> 380 us).
     bool ok = true;
     int g = 0;                 // key tiles so far
     Unit w;
     for (int k = 0; ok && unit_at(k, w); ++k) {
-      const int n = w.n_kv;
+      // The tile count and the step index that selects ring slots and score
+      // buffers (and so the MMA descriptors) are read from lane 0: the
+      // compiler then knows they are the same in every lane and keeps the
+      // loop and the descriptor arithmetic on the uniform datapath.  Taken
+      // from the unit record as they are, each key tile's products took
+      // 5-10% longer to issue (head256 forward 352 -> 376 us).
+      const int n = __shfl_sync(0xffffffffu, w.n_kv, 0);
       ok = wait_uniform(bar(L::kQFull), k & 1, abort);
-      if (ok && n > 0) ok = issue_s(__shfl_sync(0xffffffffu, g, 0));
+      if (ok && n > 0) ok = issue_s(g);
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {
           if (!issue_s(__shfl_sync(0xffffffffu, g + j + 1, 0))) { ok = false; break; }
@@ -423,7 +423,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // O += P V (the first of a unit overwrites O: every softmax thread
         // reads the previous unit's O out, and waits for the loads, before
         // it turns to this unit's scores, so P_FULL of this tile implies O
-        // is free).
+        // is free).  Inline here: as a separate function the issue sequence
+        // ran ~10% slower (head256 forward 354 -> 393 us).
         const int gj = __shfl_sync(0xffffffffu, g + j, 0);
         const uint32_t a_tmem = (gj & 1) ? tS1 : tS0;
         if constexpr (L::kChunked) {
@@ -483,8 +484,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       // never stored.
       const bool idle = qt * kBR + quarter * 32 >= p.Nq;
       for (int j = 0; j < n_kv; ++j) {
-        // read from lane 0: a known warp-uniform TMEM address (see the MMA warp)
-        const int gj = __shfl_sync(0xffffffffu, g + j, 0);
+        const int gj = g + j;
         const uint32_t tS = ((gj & 1) ? tS1 : tS0) + lane_off;
         if (!wait_uniform(bar(L::kSFull + (gj & 1)), (gj >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
