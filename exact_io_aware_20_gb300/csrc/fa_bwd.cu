@@ -16,6 +16,7 @@ int bwd_list_cap(int d) {
 cudaError_t launch_bwd(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
   if (a.mask.ptr != nullptr) return launch_bwd_blocksparse(pr, a, stream);
   if (pr.d == 128 && !a.deterministic) return launch_bwd_fused(pr, a, stream);
+  if (pr.d == 256) return launch_bwd_pair(pr, a, stream);
   return launch_bwd_for<false>(pr, a, stream);
 }
 

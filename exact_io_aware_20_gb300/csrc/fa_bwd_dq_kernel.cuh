@@ -755,6 +755,364 @@ cudaError_t launch_dq128(const Problem& pr, const BwdArgs& a, cudaStream_t strea
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// d = 256, dense: 128-key tiles, so S and dP are N = 128 products and dQ an
+// N = 256 one (full rate; with 64-key tiles S and dP ran at half rate).
+// Shared memory: Q and dO (64 KB each, for the whole CTA), one K tile (64 KB,
+// read by S_j as four 64-column chunks of d and by dQ_j as two halves of d)
+// and a ring of two 64-column chunks of V.  TMEM: S (128 columns), dP (128;
+// dS written over it in 16 bits), dQ (256).
+// Issue order per key tile j:  dQ(j-1), dP(j), S(j)
+// dQ(j-1) is K_{j-1}'s last reader; its two halves release the K tile's two
+// halves, so K_j loads while dP(j) runs.  dS(j) goes over the dP columns
+// (the warps hold dP(j) in registers by then), so dP(j+1), issued after
+// dQ(j), is the first product to overwrite it.
+// Warps: 0 producer of Q, dO and K; 10 producer of V; 1 MMA issuer; 2..9 dS
+// (a query row per thread; warps w and w + 4 share a TMEM lane quarter and
+// split the 128 key columns in halves).
+constexpr int kDq256Threads = 352;
+
+struct Dq256Layout {
+  static constexpr int kChunk = 128 * 64 * 2;     // [128 rows][64 cols] 16-bit, 128-byte swizzle
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = 4 * kChunk;
+  static constexpr int kKOff = 8 * kChunk;
+  static constexpr int kVOff = 12 * kChunk;       // two slots
+  static constexpr int kBarOff = 14 * kChunk;
+  static constexpr int kQDFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9,
+                       kDPFull = 10, kDSFull = 11, kDQDone = 13, kDrain = 14, kNumBars = 15;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr uint32_t kTS = 0, kTdP = 128, kTdQ = 256, kTmemCols = 512;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+template <bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kDq256Threads, 1)
+bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                 const DqParams p) {
+  using L = Dq256Layout;
+  constexpr int BR = 128, BC = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = CAUSAL ? (p.num_q_tiles - 1 - static_cast<int>(blockIdx.x))
+                        : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kh = h / p.G;
+  int n_kv = (p.Nk + BC - 1) / BC;
+  if (CAUSAL) {
+    const int last_key = min((qt + 1) * BR, p.Nq) - 1 + p.off;
+    n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQDFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+      mbar_init(bar(L::kDSFull + s), 8);     // one arrival per dS warp, alternating by tile
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kDPFull), 1);
+    mbar_init(bar(L::kDQDone), 1);
+    mbar_init(bar(L::kDrain), 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem + L::kTS, tdP = tmem + L::kTdP, tdQ = tmem + L::kTdQ;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ Q, dO, K
+    if (elect_one()) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(L::kQDFull), 8 * L::kChunk);
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tma_load_4d(sbase + L::kQOff + c * L::kChunk, &tm_q, bar(L::kQDFull), c * 64, qt * BR, h, b);
+        tma_load_4d(sbase + L::kDOOff + c * L::kChunk, &tm_do, bar(L::kQDFull), c * 64, qt * BR, h, b);
+      }
+    }
+    __syncwarp();
+    int issued[2] = {0, 0};
+    bool ok = true;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      #pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        // half hh of K_j (chunks 2 hh, 2 hh + 1) once dQ(j - 1) has read K_{j-1}'s
+        if (j >= 1 && !wait_uniform(bar(L::kKEmpty + hh), (j - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(L::kKFull + hh), 2 * L::kChunk);
+          #pragma unroll
+          for (int c = 2 * hh; c < 2 * hh + 2; ++c)
+            tma_load_4d(sbase + L::kKOff + c * L::kChunk, &tm_k, bar(L::kKFull + hh), c * 64, j * BC,
+                        kh, b);
+        }
+        __syncwarp();
+        ++issued[hh];
+      }
+    }
+    drain_wait(bar(L::kQDFull), 0);
+    for (int hh = 0; hh < 2; ++hh)
+      if (issued[hh] > 0) drain_wait(bar(L::kKFull + hh), (issued[hh] - 1) & 1);
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ V
+    if (elect_one()) tma_prefetch_desc(&tm_v);
+    __syncwarp();
+    int i = 0;   // chunks issued
+    for (int j = 0; j < n_kv; ++j) {
+      bool ok = true;
+      #pragma unroll 1
+      for (int c = 0; c < 4; ++c, ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !wait_uniform(bar(L::kVEmpty + s), ((i >> 1) - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(L::kVFull + s), L::kChunk);
+          tma_load_4d(sbase + L::kVOff + s * L::kChunk, &tm_v, bar(L::kVFull + s), c * 64, j * BC,
+                      kh, b);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+    for (int k = max(0, i - 2); k < i; ++k) drain_wait(bar(L::kVFull + (k & 1)), (k >> 1) & 1);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(BR, BC, BF16 ? 1 : 0, 0, 0);   // S, dP
+    constexpr uint32_t kIdQ = idesc_f16(BR, 128, BF16 ? 1 : 0, 0, 1);  // dQ halves (B = K MN-major)
+    const uint64_t q_desc = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+    const uint64_t do_desc = smem_desc_sw128(sbase + L::kDOOff, 16, 1024);
+    const uint64_t k_desc = smem_desc_sw128(sbase + L::kKOff, 16, 1024);
+    const uint64_t v_desc = smem_desc_sw128(sbase + L::kVOff, 16, 1024);
+    const uint64_t k_mn = smem_desc_sw128(sbase + L::kKOff, L::kChunk, 1024);
+    int vi = 0;   // V chunks read
+    // dQ += dS_j K_j: dS (16-bit) in the first 32 columns of each 64-column
+    // half of the dP columns (one half per dS warp); each half of d releases
+    // its half of the K tile
+    auto issue_dq = [&](int j) -> bool {
+      if (!wait_uniform(bar(L::kDSFull + (j & 1)), (j >> 1) & 1, abort)) return false;
+      tc_fence_after();
+      #pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        #pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_ts(tdQ + 128 * hh, tdP + (kk >> 2) * 64 + (kk & 3) * 8,
+                 desc_add(k_mn, hh * 2 * L::kChunk + kk * 2048), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kKEmpty + hh));
+      }
+      return true;
+    };
+    // dP_j = dO V_j^T, V in chunks of d through the ring
+    auto issue_dp = [&](int j) -> bool {
+      #pragma unroll 1
+      for (int c = 0; c < 4; ++c, ++vi) {
+        const int s = vi & 1;
+        if (!wait_uniform(bar(L::kVFull + s), (vi >> 1) & 1, abort)) return false;
+        tc_fence_after();
+        #pragma unroll
+        for (int w = 0; w < 4; ++w)
+          mma_ss(tdP, desc_add(do_desc, c * L::kChunk + w * 32),
+                 desc_add(v_desc, s * L::kChunk + w * 32), kIdS, (c | w) ? 1u : 0u);
+        mma_commit(bar(L::kVEmpty + s));
+      }
+      mma_commit(bar(L::kDPFull));
+      return true;
+    };
+    // S_j = Q K_j^T, K_j's two halves as they land
+    auto issue_s = [&](int j) -> bool {
+      #pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        if (!wait_uniform(bar(L::kKFull + hh), j & 1, abort)) return false;
+        tc_fence_after();
+        #pragma unroll
+        for (int kk = 8 * hh; kk < 8 * hh + 8; ++kk) {
+          const uint32_t c = kk >> 2, w = kk & 3;
+          mma_ss(tS, desc_add(q_desc, c * L::kChunk + w * 32), desc_add(k_desc, c * L::kChunk + w * 32),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+      }
+      mma_commit(bar(L::kSFull));
+      return true;
+    };
+    bool ok = wait_uniform(bar(L::kQDFull), 0, abort);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      if (j >= 1 && !issue_dq(j - 1)) ok = false;
+      else if (!issue_dp(j)) ok = false;
+      else if (!issue_s(j)) ok = false;
+    }
+    if (ok && n_kv > 0) issue_dq(n_kv - 1);
+    mma_commit(bar(L::kDQDone));
+    mma_commit(bar(L::kDrain));
+    drain_wait(bar(L::kDrain), 0);
+  } else {
+    // ------------------------------------------------------------ dS warps
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;          // key columns [64 half, 64 half + 64)
+    const int row = qt * BR + quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const size_t row_idx = (static_cast<size_t>(b) * p.H + h) * p.Nq + (row < p.Nq ? row : 0);
+    const long long dq_off =
+        b * p.dqs.b + h * p.dqs.h + static_cast<long long>(row < p.Nq ? row : 0) * p.dqs.n;
+    const float nL = row < p.Nq ? -p.lse[row_idx] * kDqLog2e : -INFINITY;
+    const float nD = row < p.Nq ? -p.delta[row_idx] : 0.f;
+    const f2 cs = {p.scale_log2, p.scale_log2}, cl = {nL, nL}, cd = {nD, nD};
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!wait_uniform(bar(L::kSFull), j & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      const int col0 = j * BC + 64 * half;
+      const bool masked = (CAUSAL && col0 + 63 > qt * BR + p.off) || (col0 + 64 > p.Nk);
+      float P[64];
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t sr[32];
+        tmem_ld32(tS + lane_off + 64 * half + c0, sr);
+        tmem_ld_wait();
+        reg_fence(sr);
+        #pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const f2 arg = ffma2(f2{__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, cs, cl);
+          P[c0 + c] = ex2_approx(arg.x);
+          P[c0 + c + 1] = ex2_approx(arg.y);
+        }
+        if (masked) {
+          // columns [0, lim) of this chunk are kept (one comparison per score)
+          const int lim = min(p.Nk - col0 - c0, CAUSAL ? row + p.off - col0 - c0 + 1 : 32);
+          #pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c >= lim) P[c0 + c] = 0.f;
+        }
+      }
+      if (!wait_uniform(bar(L::kDPFull), j & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dr[64];
+      tmem_ld32(tdP + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(tdP + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_ld_wait();
+      reg_fence(dr);
+      #pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t w[16];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const f2 ds = fmul2(f2{P[c0 + 2 * c], P[c0 + 2 * c + 1]},
+                              fadd2(f2{__uint_as_float(dr[c0 + 2 * c]),
+                                       __uint_as_float(dr[c0 + 2 * c + 1])}, cd));
+          w[c] = pack2<BF16>(ds.x, ds.y);
+        }
+        // dS (16-bit) over the first 32 columns of this half of dP, read above
+        tmem_st16(tdP + lane_off + 64 * half + c0 / 2, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(bar(L::kDSFull + (j & 1)));
+    }
+    // ------------------------------------------------------------ epilogue
+    uint4* out = reinterpret_cast<uint4*>(p.dq + dq_off + 128 * half);
+    if (ok && n_kv == 0) {
+      if (row < p.Nq) {
+        #pragma unroll
+        for (int i = 0; i < 16; ++i) out[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else if (ok && wait_uniform(bar(L::kDQDone), 0, abort)) {
+      tc_fence_after();
+      #pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tdQ + lane_off + 128 * half + c0, v);
+        tmem_ld_wait();
+        reg_fence(v);
+        uint32_t o[16];
+        #pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * p.scale, __uint_as_float(v[2 * i + 1]) * p.scale);
+        if (row < p.Nq) {
+          #pragma unroll
+          for (int i = 0; i < 4; ++i)
+            out[c0 / 8 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && *abort == 2) atomicOr(p.err, kErrTimeout);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_dq256(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {
+  using L = Dq256Layout;
+  CUtensorMap tq, tk, tv, tdo;
+  cudaError_t e;
+  if ((e = make_tmap_4d(&tq, a.q, 256, pr.Nq, pr.H, pr.B, a.qs, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tdo, a.dout, 256, pr.Nq, pr.H, pr.B, a.dos, 64, 128)) != cudaSuccess)
+    return e;
+  if ((e = make_tmap_4d(&tk, a.k, 256, pr.Nk, pr.Hkv, pr.B, a.ks, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_4d(&tv, a.v, 256, pr.Nk, pr.Hkv, pr.B, a.vs, 64, 128)) != cudaSuccess) return e;
+  auto kern = bwd_dq256_kernel<CAUSAL, BF16>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc)) !=
+        cudaSuccess)
+      return e;
+    attr_set = true;
+  }
+  DqParams p;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq = static_cast<uint16_t*>(a.dq);
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.off = pr.Nk - pr.Nq;
+  p.G = pr.H / pr.Hkv;
+  p.num_q_tiles = (pr.Nq + 127) / 128;
+  p.scale = pr.scale;
+  p.scale_log2 = pr.scale * kDqLog2e;
+  p.mask = BlockMask{};
+  p.dqs = a.dqs;
+  p.err = pr.err;
+  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  const int slot = timing_begin(FA_KERNEL_BWD_DQ, stream);
+  kern<<<grid, kDq256Threads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
+  timing_end(slot, stream);
+  return cudaGetLastError();
+}
+
 template <int D, int KST, bool SPARSE>
 cudaError_t dispatch_dq(const Problem& pr, const BwdArgs& a, cudaStream_t s) {
   if (pr.causal)
@@ -773,6 +1131,13 @@ cudaError_t launch_bwd_dq_for(const Problem& pr, const BwdArgs& a, cudaStream_t 
                      : launch_dq128<true, false, SPARSE>(pr, a, stream);
     return pr.bf16 ? launch_dq128<false, true, SPARSE>(pr, a, stream)
                    : launch_dq128<false, false, SPARSE>(pr, a, stream);
+  }
+  if constexpr (!SPARSE) {
+    if (pr.d == 256) {
+      if (pr.causal)
+        return pr.bf16 ? launch_dq256<true, true>(pr, a, stream) : launch_dq256<true, false>(pr, a, stream);
+      return pr.bf16 ? launch_dq256<false, true>(pr, a, stream) : launch_dq256<false, false>(pr, a, stream);
+    }
   }
   switch (pr.d) {
     case 64: return dispatch_dq<64, 4, SPARSE>(pr, a, stream);

@@ -92,10 +92,6 @@ constexpr int kDqBarrier = 1;
 // Warps that read each unit record (MMA, P / dS, dQ).
 constexpr int kUnitReaders = 13;
 
-// Bit of the device error word: the dynamic shared memory base was not
-// 1024-byte aligned and the layout did not fit behind the aligned base.
-constexpr unsigned int kErrSmemBase = 2u;
-
 // Unit u of the launch's order -> (key tile, kv head, batch).
 __device__ __forceinline__ void fused_unit(const BwdParams& p, int u, int& jt, int& kh, int& b) {
   int grp;

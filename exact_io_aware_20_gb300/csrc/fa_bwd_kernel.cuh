@@ -62,6 +62,10 @@ constexpr int kBC = 128;        // key rows per CTA
 constexpr int kBwdThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Bit of the device error word: the dynamic shared memory base was not
+// 1024-byte aligned and the layout did not fit behind the aligned base.
+constexpr unsigned int kErrSmemBase = 2u;
+
 template <int D, int DH, int BR, int QST>
 struct BwdLayout {
   static constexpr bool kDqT = (BR == 64);

@@ -110,6 +110,9 @@ cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 // d = 128, dense, dQ by atomic adds: the fused five-product kernel.
 cudaError_t launch_bwd_fused(const Problem& p, const BwdArgs& a, cudaStream_t stream);
+// d = 256, dense: dK and dV from the cluster-pair kernel, dQ from the
+// query-outer kernel (no atomics; needs only D in the scratch).
+cudaError_t launch_bwd_pair(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 // Deterministic dQ (query-outer, no atomics); needs D in a.delta.
 cudaError_t launch_bwd_dq(const Problem& p, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq_blocksparse(const Problem& p, const BwdArgs& a, cudaStream_t stream);

@@ -61,15 +61,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for a barrier that threads of another
+// CTA of the cluster arrive on (with release at cluster scope).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (CLUSTER) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -78,15 +91,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // the timer were not advancing (setting *abort = 2, which the kernel reports
 // in the device error word before it exits), or as soon as another thread of
 // the CTA has set *abort; returns false in all three cases.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
                                                 volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   const uint64_t max_rounds = limit_ns / (4 * 32) + 1;
   for (uint64_t round = 0;; ++round) {
     #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns || round >= max_rounds) {
       *abort = 2;
@@ -95,14 +109,16 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
   }
 }
 
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  return mbar_wait_limit(bar, parity, abort, FA_WAIT_LIMIT_NS);
+  return mbar_wait_limit<CLUSTER>(bar, parity, abort, FA_WAIT_LIMIT_NS);
 }
 
 // mbar_wait for a whole warp: true only if every lane saw the phase complete,
 // so the warp stays converged for the .sync.aligned tcgen05 instructions.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, volatile int* abort) {
-  bool ok = mbar_wait(bar, parity, abort);
+  bool ok = mbar_wait<CLUSTER>(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -188,6 +204,67 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- clusters
+// Rank of this CTA within its thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in the CTA of
+// rank `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// 16 bytes into another CTA's shared memory (a shared::cluster address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
+// 16 bytes into another CTA's shared memory whose arrival completes 16
+// transaction bytes on that CTA's mbarrier `bar` (both shared::cluster
+// addresses); the receiver's arrive.expect_tx covers them, and its wait on
+// the barrier makes the data visible.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+      : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (a shared::cluster
+// address), releasing this thread's earlier memory operations at cluster
+// scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+
+// All threads of every CTA of the cluster meet; writes before it (to any
+// CTA's shared memory) are visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

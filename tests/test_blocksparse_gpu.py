@@ -8,7 +8,7 @@ import torch
 import oracle
 from exact_io_aware_20_gb300 import binding
 from exact_io_aware_20_gb300.inputs import Workload, make_block_mask, make_inputs
-from parity import check_forward, check_grads
+from parity import check_forward, check_grads, rel_l2
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -85,7 +85,10 @@ def test_all_ones_mask_is_the_dense_kernel(d, causal):
     so the forward and the deterministic backward agree with it bit for bit.
     (The dense forward at d = 128 runs the two-tile kernel, which sums the
     row weights on the ALU and divides by their exact sum: there the forward
-    is compared within the parity tolerances.)"""
+    is compared within the parity tolerances.  The dense backward at d = 256
+    forms dK and dV in the cluster-pair kernel, with 128-row steps and dS from
+    the 16-bit weights: there dQ, from the same query-outer kernel, is
+    compared bit for bit and dK, dV within the rounding of the weights.)"""
     w = Workload("bs1", 2, 4, 1, 640, d, "f16", causal, 90 + d)
     q, k, v, do = (t.to(DEV) for t in make_inputs(w))
     ones = torch.ones((1, 5, 5), dtype=torch.uint8, device=DEV)
@@ -100,8 +103,13 @@ def test_all_ones_mask_is_the_dense_kernel(d, causal):
         assert (l_s - l_d).abs().max().item() <= 1e-5
     else:
         assert torch.equal(o_s, o_d) and torch.equal(l_s, l_d)
-    for a, b in zip(g_s, g_d):
-        assert torch.equal(a, b)
+    if d == 256:
+        assert torch.equal(g_s[0], g_d[0])
+        for a, b in zip(g_s[1:], g_d[1:]):
+            assert rel_l2(a, b) <= 1e-2
+    else:
+        for a, b in zip(g_s, g_d):
+            assert torch.equal(a, b)
 
 
 def test_empty_mask_gives_zeros():
