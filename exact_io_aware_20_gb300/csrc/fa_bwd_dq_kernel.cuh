@@ -813,6 +813,12 @@ bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int last_key = min((qt + 1) * BR, p.Nq) - 1 + p.off;
     n_kv = last_key < 0 ? 0 : min(n_kv, last_key / BC + 1);
   }
+  // The CTAs of a head start their walk over the key tiles at different
+  // tiles (query tile qt at tile qt mod n_kv): walking in step, every CTA
+  // asked for each tile first, so every tile's loads waited for DRAM; now a
+  // tile is mostly in L2 by the time the next CTA reaches it.  (dQ sums the
+  // tiles in this fixed order, the same on every run.)
+  auto key_tile = [&](int j) { return n_kv > 0 ? (j + qt) % n_kv : 0; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQDFull), 1);
@@ -869,8 +875,8 @@ bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mbar_arrive_expect_tx(bar(L::kKFull + hh), 2 * L::kChunk);
           #pragma unroll
           for (int c = 2 * hh; c < 2 * hh + 2; ++c)
-            tma_load_4d(sbase + L::kKOff + c * L::kChunk, &tm_k, bar(L::kKFull + hh), c * 64, j * BC,
-                        kh, b);
+            tma_load_4d(sbase + L::kKOff + c * L::kChunk, &tm_k, bar(L::kKFull + hh), c * 64,
+                        key_tile(j) * BC, kh, b);
         }
         __syncwarp();
         ++issued[hh];
@@ -895,8 +901,8 @@ bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         if (elect_one()) {
           mbar_arrive_expect_tx(bar(L::kVFull + s), L::kChunk);
-          tma_load_4d(sbase + L::kVOff + s * L::kChunk, &tm_v, bar(L::kVFull + s), c * 64, j * BC,
-                      kh, b);
+          tma_load_4d(sbase + L::kVOff + s * L::kChunk, &tm_v, bar(L::kVFull + s), c * 64,
+                      key_tile(j) * BC, kh, b);
         }
         __syncwarp();
       }
@@ -987,7 +993,7 @@ bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int j = 0; j < n_kv; ++j) {
       if (!wait_uniform(bar(L::kSFull), j & 1, abort)) { ok = false; break; }
       tc_fence_after();
-      const int col0 = j * BC + 64 * half;
+      const int col0 = key_tile(j) * BC + 64 * half;
       const bool masked = (CAUSAL && col0 + 63 > qt * BR + p.off) || (col0 + 64 > p.Nk);
       float P[64];
       #pragma unroll

@@ -340,7 +340,9 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const float* sv = ld_base + (t % 3) * 64;
-      if (t + 1 < n) load_ld(t + 1);
+      // (rank 1 issues the next step's loads after its release arrive below,
+      // which would otherwise wait for them)
+      if (rank == 0 && t + 1 < n) load_ld(t + 1);
       const uint32_t src = tScore + (t & 1) * 128 + lane_off + 64 * half;
       uint32_t pk[32];   // 16-bit pairs of P^T, query columns 2 j and 2 j + 1 of this half
       if (rank == 0) {
@@ -391,6 +393,11 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
           reg_fence(sb);
           p_chunk(sb, 32);
         }
+        // P^T is in TMEM: this CTA's dV may start before the rows below have
+        // left (their stores take longer than the exponentials)
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(bar(L::kPFull + (t & 1)));
         // row r of this half of P^T to rank 1's buffer t % PBUF, once rank 1
         // has read step t - PBUF's from it
         const int pb = t % PBUF, use = t / PBUF;
@@ -423,6 +430,7 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
           __syncwarp();
         }
         mbar_arrive_remote(out_free(pb));
+        if (t + 1 < n) load_ld(t + 1);
         if (!wait_uniform(bar(L::kSFull + (t & 1)), (t >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
         uint32_t da[32], db[32];
@@ -448,10 +456,10 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         tmem_st16(src, &w[0]);
         tmem_st16(src + 16, &w[16]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(bar(L::kPFull + (t & 1)));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive_warp(bar(L::kPFull + (t & 1)));
       if (t + 1 < n) {
         store_ld(t + 1);
         __syncwarp();

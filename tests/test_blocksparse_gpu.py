@@ -86,9 +86,10 @@ def test_all_ones_mask_is_the_dense_kernel(d, causal):
     (The dense forward at d = 128 runs the two-tile kernel, which sums the
     row weights on the ALU and divides by their exact sum: there the forward
     is compared within the parity tolerances.  The dense backward at d = 256
-    forms dK and dV in the cluster-pair kernel, with 128-row steps and dS from
-    the 16-bit weights: there dQ, from the same query-outer kernel, is
-    compared bit for bit and dK, dV within the rounding of the weights.)"""
+    runs its own kernels (the cluster pair for dK and dV, with 128-row steps
+    and dS from the 16-bit weights; a dQ kernel with 128-key tiles summed in a
+    staggered order): there the gradients are compared within the rounding of
+    the weights and of the 16-bit outputs.)"""
     w = Workload("bs1", 2, 4, 1, 640, d, "f16", causal, 90 + d)
     q, k, v, do = (t.to(DEV) for t in make_inputs(w))
     ones = torch.ones((1, 5, 5), dtype=torch.uint8, device=DEV)
@@ -104,8 +105,7 @@ def test_all_ones_mask_is_the_dense_kernel(d, causal):
     else:
         assert torch.equal(o_s, o_d) and torch.equal(l_s, l_d)
     if d == 256:
-        assert torch.equal(g_s[0], g_d[0])
-        for a, b in zip(g_s[1:], g_d[1:]):
+        for a, b in zip(g_s, g_d):
             assert rel_l2(a, b) <= 1e-2
     else:
         for a, b in zip(g_s, g_d):

@@ -159,6 +159,9 @@ def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, 
                 yield
                 assert not queued(r, buf, write_only=False), "TMEM write while a product uses it"
                 content[buf] = ("P16", t)
+                # the L / D values are read until here
+                assert content.get(ld(t)) == ("LD", t), "L / D values of another step"
+                B[r, f"PF{t & 1}"].arrive()       # before the rows are sent
                 yield
                 if t >= pbuf and plant != "no_outfree_wait":
                     yield from wait((0, f"OUT{h}{w}{pb}"), (use - 1) & 1)
@@ -186,10 +189,11 @@ def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, 
                 assert not queued(r, buf, write_only=False), "TMEM write while a product uses it"
                 content[buf] = ("dS16", t)
                 yield
-            # the L / D values are read until here
-            assert content.get(ld(t)) == ("LD", t), "L / D values of another step"
-            if not (plant == "early_pfull" and r == 1):
-                B[r, f"PF{t & 1}"].arrive()
+            if r == 1:
+                # the L / D values are read until here
+                assert content.get(ld(t)) == ("LD", t), "L / D values of another step"
+                if plant != "early_pfull":
+                    B[r, f"PF{t & 1}"].arrive()
             if t + 1 < n:
                 content[ld(t + 1)] = ("LD", t + 1)
             yield
