@@ -143,7 +143,11 @@ size_t fa_bwd_workspace_size_for(int B, int H, int Hkv, int Nq, int d, int deter
  * fused kernel forms all five products of a tile and hands each dQ tile to
  * the tensor memory accelerator as bulk reduce-adds.  The order of those
  * additions varies from run to run, so dQ is reproducible only up to fp32
- * rounding; fa_bwd_deterministic gives the same bits on every run.
+ * rounding; fa_bwd_deterministic gives the same bits on every run.  At
+ * d = 256 (without a block mask) dK and dV come from a kernel run by pairs of
+ * CTAs (a thread-block cluster of two per key tile) and dQ from the
+ * query-outer kernel of fa_bwd_deterministic: no atomics, every output the
+ * same bits on every run, and only D of the workspace is used.
  */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
