@@ -16,13 +16,14 @@
 //  - section 4 "six checks", GQA/MQA: query head h reads key/value head
 //    h / (H / Hkv) by index, with no copy.
 // Under a block mask (block-sparse attention, "FlashAttention: Fast and
-// Memory-Efficient Exact Attention with IO-Awareness", abstract) a CTA walks
-// only the key tiles of its kept mask blocks, from a list built in shared
-// memory before the warps split up.
+// Memory-Efficient Exact Attention with IO-Awareness", abstract) a unit walks
+// only the key tiles of its kept mask blocks: the Q / K producer reads the
+// unit's mask row and publishes the kept tiles as a bit set in a unit record
+// that the other warps read.
 //
 // GB300 design (not the pages' A100 design): a work unit is one 128-row
 // query tile (of one split of the keys, head, batch); a persistent grid of one
-// CTA per SM walks the units (one CTA per unit with a block mask), TMEM, the
+// CTA per SM walks the units (with or without a block mask), TMEM, the
 // barriers and the K / V rings living across units; warp-specialised:
 //   warp 0      TMA producer: each unit's Q, then K_j through a smem ring;
 //   warp 6      TMA producer: V_j through a second ring;
@@ -87,17 +88,22 @@ struct FwdLayout {
   static constexpr int kPFull = kSFull + 2;      // 2
   static constexpr int kODone = kPFull + 2;
   static constexpr int kDrain = kODone + 1;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kUnitFull = kDrain + 1;     // 2: unit records (block mask)
+  static constexpr int kUnitEmpty = kUnitFull + 2; // 2
+  static constexpr int kNumBars = kUnitEmpty + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kListOff = kMiscOff + 16;   // key tiles kept under a block mask
-  static constexpr int kBytes = kListOff + kFwdListCap * 2;
-  static constexpr int kAlloc = kBytes + 1024;   // slack to align the base to 1024
-  static constexpr int kAllocDense = kListOff + 1024;   // without the list
+  // Under a block mask: two unit records {kept tiles, bit set of the kept
+  // key tiles (one bit per 128-key tile, up to kFwdListCap tiles)}
+  static constexpr int kRecOff = kMiscOff + 16;
+  static constexpr int kRecBytes = 16 + kFwdListCap / 8;
+  static constexpr int kAlloc = kRecOff + 2 * kRecBytes + 1024;   // slack to align the base
+  static constexpr int kAllocDense = kRecOff + 1024;              // without the records
   // TMEM columns
   static constexpr uint32_t kS0 = 0, kS1 = BC, kO = 2 * BC;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kO + D + kOnesCols <= kTmemCols, "TMEM budget");
   static_assert(kAllocDense <= 227 * 1024, "shared memory budget");
+  static_assert(kRecBytes % 16 == 0, "unit records are 16-byte aligned");
 };
 
 struct FwdParams {
@@ -133,28 +139,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   uint8_t* smem = smem_raw + (sbase - raw);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  int* list_count = reinterpret_cast<int*>(smem + L::kMiscOff + 8);
-  uint16_t* tile_list = reinterpret_cast<uint16_t*>(smem + L::kListOff);
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool packed = p.mask_rows != p.Nq;
   // Work units (split, query tile, head, batch), numbered with the split
   // fastest, then query tiles (under the mask the longest first), heads,
-  // batches.  Without a block mask the grid is persistent: CTA c takes unit
-  // k * G + c in even rounds k and k * G + G - 1 - c in odd ones (G = grid
-  // size), so that over two rounds of longest-first units every CTA gets
-  // about the same work.  With a block mask every CTA takes one unit.
+  // batches.  The grid is persistent: CTA c takes unit k * G + c in even
+  // rounds k and k * G + G - 1 - c in odd ones (G = grid size), so that over
+  // two rounds of longest-first units every CTA gets about the same work.
   const int ux = p.num_q_tiles * p.splits;
   const long long n_units = static_cast<long long>(ux) * p.H * p.B_;
   auto unit_of = [&](int k) -> long long {
-    if (SPARSE) return k == 0 ? static_cast<long long>(blockIdx.x) : -1;
     const long long G = gridDim.x;
     const long long u = k * G + ((k & 1) ? G - 1 - blockIdx.x : blockIdx.x);
     return u < n_units ? u : -1;
   };
+  // n_kv: key tiles of the unit; lim: the tiles its rows may see (the
+  // causal / length limit), of which a block mask keeps n_kv
   struct Unit {
-    int split, qt, h, b, n_kv, j_base;
+    int split, qt, h, b, n_kv, j_base, lim;
   };
   auto decode = [&](long long u) {
     Unit w;
@@ -177,28 +181,50 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     w.j_base = w.split * p.tiles_per_split;
     if (p.splits > 1) n = max(0, min(n, w.j_base + p.tiles_per_split) - w.j_base);
     w.n_kv = n;
+    w.lim = n;
     return w;
   };
   constexpr bool sparse = SPARSE;
-  if (sparse && warp == 2) {
-    // key tiles of the kept blocks in this query tile's mask row, within n_kv
-    const Unit w = decode(unit_of(0));
-    constexpr int kSub = kMaskBlock / BC;
+  static_assert(!SPARSE || BC == kMaskBlock, "a key tile is a mask block");
+  // Under a block mask a unit walks the kept blocks of its query tile's mask
+  // row.  The Q / K producer reads the row and publishes each unit's record
+  // (the kept count and a bit set of the kept key tiles) in one of two slots;
+  // the other warps take the unit's tiles from the record and release the
+  // slot when they are done with it.
+  auto mask_row = [&](const Unit& w) -> const unsigned char* {
     const int mh = p.mask.heads == 1 ? 0 : w.h;
-    const unsigned char* mrow =
-        p.mask.ptr + (static_cast<size_t>(mh) * p.mask.nbr + w.qt) * p.mask.nbc;
-    const int lim = w.n_kv;
-    const int cnt = compact_steps<kSub>(
-        p.mask.nbc, [&](int e) { return mrow[e] != 0; },
-        [&](int e, int sub) { const int j = e * kSub + sub; return j < lim ? j : -1; },
-        tile_list, kFwdListCap);
-    if (lane == 0) *list_count = min(cnt, kFwdListCap);
-  }
-  // key tile of step j of unit w
-  auto key_tile = [&](const Unit& w, int j) -> int {
-    return sparse ? static_cast<int>(tile_list[j]) : w.j_base + j;
+    return p.mask.ptr + (static_cast<size_t>(mh) * p.mask.nbr + w.qt) * p.mask.nbc;
   };
-
+  auto rec_n = [&](int k) -> volatile int* {
+    return reinterpret_cast<volatile int*>(smem + L::kRecOff + (k & 1) * L::kRecBytes);
+  };
+  auto rec_bits = [&](int k) -> const volatile uint32_t* {
+    return reinterpret_cast<const volatile uint32_t*>(smem + L::kRecOff + (k & 1) * L::kRecBytes + 16);
+  };
+  // the key tiles of unit w in order: next() once per step j (a whole warp)
+  struct TileWalk {
+    const volatile uint32_t* bits;
+    int base, word;
+    uint32_t cur;
+    __device__ __forceinline__ int next(int j) {
+      if constexpr (!SPARSE) {
+        return base + j;
+      } else {
+        while (cur == 0) cur = bits[++word];
+        const int i = __ffs(cur) - 1;
+        cur &= cur - 1;
+        return word * 32 + i;
+      }
+    }
+  };
+  auto walk_of = [&](const Unit& w, int k) {
+    TileWalk t;
+    t.base = w.j_base;
+    t.word = 0;
+    t.bits = sparse ? rec_bits(k) : nullptr;
+    t.cur = sparse ? t.bits[0] : 0u;
+    return t;
+  };
   // the merge of split partials (launched as this grid's dependent) may start
   // its launch now; it waits for this grid's completion before reading
   if (p.splits > 1) grid_launch_dependents();
@@ -219,6 +245,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     }
     mbar_init(bar(L::kODone), 1);
     mbar_init(bar(L::kDrain), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kUnitFull + s), 1);
+      mbar_init(bar(L::kUnitEmpty + s), 6);   // V producer, MMA, four softmax warps
+    }
     *abort = 0;
     fence_barrier_init();
   }
@@ -241,13 +271,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the unit's key tiles: the kept list under a block mask
+  // Unit k of this CTA; under a block mask the kept tiles come from its
+  // record (a whole warp waits for it; false also when the wait gave up).
+  // The Q / K producer makes the records (publish_unit) and does not call this.
   auto unit_at = [&](int k, Unit& w) -> bool {
     const long long u = unit_of(k);
     if (u < 0) return false;
     w = decode(u);
-    if (sparse) w.n_kv = *list_count;
+    if (sparse) {
+      if (!wait_uniform(bar(L::kUnitFull + (k & 1)), (k >> 1) & 1, abort)) return false;
+      w.n_kv = *rec_n(k);
+    }
     return true;
+  };
+  auto release_unit = [&](int k) {
+    if (sparse) mbar_arrive_warp(bar(L::kUnitEmpty + (k & 1)));
   };
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS0 = tmem + L::kS0, tS1 = tmem + L::kS1, tO = tmem + L::kO;
@@ -270,7 +308,42 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     int issued = 0, q_issued = 0;   // K pieces, Q tiles
     bool ok = true;
     Unit w;
-    for (int k = 0; ok && unit_at(k, w); ++k) {
+    for (int k = 0; ok; ++k) {
+      const long long u = unit_of(k);
+      if (u < 0) break;
+      w = decode(u);
+      if (sparse) {
+        // the unit's record, once the six readers are done with unit k - 2's:
+        // the kept tiles of the query tile's mask row within its limit, read
+        // eight 32-block chunks at a time (their loads in flight together)
+        if (k >= 2 && !wait_uniform(bar(L::kUnitEmpty + (k & 1)), ((k >> 1) - 1) & 1, abort)) break;
+        const unsigned char* row = mask_row(w);
+        volatile uint32_t* bits =
+            reinterpret_cast<volatile uint32_t*>(smem + L::kRecOff + (k & 1) * L::kRecBytes + 16);
+        int n = 0;
+        for (int base = 0; base < w.lim; base += 256) {
+          unsigned char v[8];
+          #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int e = base + 32 * c + lane;
+            v[c] = e < w.lim ? row[e] : 0;
+          }
+          #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t m = __ballot_sync(0xffffffffu, v[c] != 0);
+            if (base + 32 * c < w.lim) {
+              if (lane == 0) bits[(base >> 5) + c] = m;
+              n += __popc(m);
+            }
+          }
+        }
+        if (lane == 0) {
+          *rec_n(k) = n;
+          mbar_arrive(bar(L::kUnitFull + (k & 1)));   // (releases lane 0's writes)
+        }
+        __syncwarp();
+        w.n_kv = n;
+      }
       if (k >= 1 && !wait_uniform(bar(L::kQEmpty), (k - 1) & 1, abort)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
@@ -282,7 +355,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       __syncwarp();
       ++q_issued;
       const int kh = w.h / p.G;
+      TileWalk tw = walk_of(w, k);
       for (int j = 0; ok && j < w.n_kv; ++j) {
+        const int jt = tw.next(j);
         #pragma unroll 1
         for (int c = 0; c < (L::kChunked ? L::kNch : 1); ++c) {
           const int s = issued % KST;
@@ -294,12 +369,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             mbar_arrive_expect_tx(bar(L::kKFull + s), L::kKSlot);
             if constexpr (L::kChunked) {
               tma_load_4d(sbase + L::kKOff + s * L::kKSlot, &tm_k, bar(L::kKFull + s), c * 64,
-                          key_tile(w, j) * BC, kh, w.b);
+                          jt * BC, kh, w.b);
             } else {
               #pragma unroll
               for (int cc = 0; cc < L::kNch; ++cc)
                 tma_load_4d(sbase + L::kKOff + s * L::kKSlot + cc * (BC * 128), &tm_k,
-                            bar(L::kKFull + s), cc * 64, key_tile(w, j) * BC, kh, w.b);
+                            bar(L::kKFull + s), cc * 64, jt * BC, kh, w.b);
             }
           }
           __syncwarp();
@@ -319,7 +394,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     Unit w;
     for (int k = 0; ok && unit_at(k, w); ++k) {
       const int kh = w.h / p.G;
+      TileWalk tw = walk_of(w, k);
       for (int j = 0; ok && j < w.n_kv; ++j) {
+        const int jt = tw.next(j);
         #pragma unroll 1
         for (int hv = 0; hv < (L::kChunked ? 2 : 1); ++hv) {
           const int sv = issued % VST;
@@ -333,19 +410,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
               #pragma unroll
               for (int c = 0; c < L::kNch; ++c)
                 tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * ((BC / 2) * 128), &tm_v,
-                            bar(L::kVFull + sv), c * 64, key_tile(w, j) * BC + hv * (BC / 2), kh, w.b);
+                            bar(L::kVFull + sv), c * 64, jt * BC + hv * (BC / 2), kh, w.b);
             } else {
               mbar_arrive_expect_tx(bar(L::kVFull + sv), L::kKVBytes);
               #pragma unroll
               for (int c = 0; c < L::kNch; ++c)
                 tma_load_4d(sbase + L::kVOff + sv * L::kVStage + c * (BC * 128), &tm_v,
-                            bar(L::kVFull + sv), c * 64, key_tile(w, j) * BC, kh, w.b);
+                            bar(L::kVFull + sv), c * 64, jt * BC, kh, w.b);
             }
           }
           __syncwarp();
           ++issued;
         }
       }
+      if (ok) release_unit(k);
     }
     for (int i = max(0, issued - VST); i < issued; ++i)
       drain_wait(bar(L::kVFull + i % VST), (i / VST) & 1);
@@ -408,6 +486,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       // from the unit record as they are, each key tile's products took
       // 5-10% longer to issue (head256 forward 352 -> 376 us).
       const int n = __shfl_sync(0xffffffffu, w.n_kv, 0);
+      release_unit(k);   // (only the count is needed here)
       ok = wait_uniform(bar(L::kQFull), k & 1, abort);
       if (ok && n > 0) ok = issue_s(g);
       for (int j = 0; ok && j < n; ++j) {
@@ -483,6 +562,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       // so its scores are 0 and the P it leaves in TMEM is 0, and its rows are
       // never stored.
       const bool idle = qt * kBR + quarter * 32 >= p.Nq;
+      TileWalk tw = walk_of(w, k);   // (idle warps never read it)
       for (int j = 0; j < n_kv; ++j) {
         const int gj = g + j;
         const uint32_t tS = ((gj & 1) ? tS1 : tS0) + lane_off;
@@ -504,7 +584,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tmem_ld_wait();
         reg_fence(sr);
         float* s = reinterpret_cast<float*>(sr);
-        const int col0 = key_tile(w, j) * BC;
+        const int col0 = tw.next(j) * BC;
         const int min_i = packed ? 0 : qt * kBR;
         const bool need_mask = (CAUSAL && col0 + BC - 1 > min_i + p.off) || (col0 + BC > p.Nk);
         if (need_mask) {
@@ -606,6 +686,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         mbar_arrive(bar(L::kPFull + (gj & 1)));
       }
       if (!ok) break;
+      release_unit(k);
       // ------------------------------------------------------------ epilogue
       const size_t rows_total = static_cast<size_t>(p.B_) * p.H * p.Nq;
       const size_t row_base = (static_cast<size_t>(b) * p.H + h) * p.Nq;
@@ -1286,7 +1367,8 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
     return e;
   auto kern = fwd_kernel<D, BC, CAUSAL, BF16, KST, VST, SPARSE>;
   // without a block mask the list is never touched and not allocated
-  constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;
+  constexpr int kSmem = SPARSE ? L::kAlloc : L::kAllocDense;   // (records only with a block mask)
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static bool attr_set = false;
   if (!attr_set) {
@@ -1333,8 +1415,7 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   p.o_sh = ov.h;
   p.o_sn = ov.n;
   if ((e = make_tmap_4d(&tq, a.q, D, p.Nq, p.H, pr.B, qv, 64, kBR)) != cudaSuccess) return e;
-  // persistent: one CTA per SM walking the units (one CTA per unit with a
-  // block mask, whose key-tile list is built per CTA)
+  // persistent: one CTA per SM walking the units
   static int n_sms = 0;
   if (n_sms == 0) {
     int dev = 0;
@@ -1344,8 +1425,7 @@ cudaError_t launch_variant(const Problem& pr, const FwdArgs& a, cudaStream_t str
   }
   const long long n_units = static_cast<long long>(p.num_q_tiles) * p.splits * p.H * pr.B;
   if (n_units >= (1ll << 31)) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(SPARSE ? n_units : std::min<long long>(n_units, std::max(n_sms, 1))),
-                  1, 1);
+  const dim3 grid(static_cast<unsigned>(std::min<long long>(n_units, std::max(n_sms, 1))), 1, 1);
   const int slot = timing_begin(FA_KERNEL_FWD, stream);
   kern<<<grid, kThreads, kSmem, stream>>>(tq, tk, tv, p);
   timing_end(slot, stream);
@@ -1394,9 +1474,9 @@ cudaError_t launch_fwd_for(const Problem& pr, const FwdArgs& a, cudaStream_t str
     case 64: return dispatch_flags<64, 128, 3, 3, SPARSE>(pr, a, stream);
     case 128: return dispatch_flags<128, 128, 2, 2, SPARSE>(pr, a, stream);
     // d = 256: 128-key tiles through rings of pieces (six K chunks and two
-    // V halves; four K chunks with a block mask, whose key-tile list also
-    // needs shared memory)
-    case 256: return dispatch_flags<256, 128, SPARSE ? 4 : 6, 2, SPARSE>(pr, a, stream);
+    // V halves; five K chunks with a block mask, whose unit records also
+    // need shared memory)
+    case 256: return dispatch_flags<256, 128, SPARSE ? 5 : 6, 2, SPARSE>(pr, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

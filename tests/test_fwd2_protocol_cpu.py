@@ -191,7 +191,7 @@ def test_persistent_forward_protocol(seed):
     assert run(units, seed), f"protocol stalled: units {units}"
 
 
-def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
+def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None, records=False):
     """The one-tile forward (d = 64 / 256, short, split and block-sparse
     paths), persistent: one CTA walks the units of `units` (their key-tile
     counts, 0 allowed) one after another.  Per key tile: S(g+1) is issued
@@ -211,7 +211,12 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
     epilogue that O holds the unit's last product.  plant: None or a mistake
     ("no_qempty_wait", "early_qempty", "early_p_full": a softmax warp arrives
     on P_FULL of a unit's first tile before its read-out of the previous
-    unit's O)."""
+    unit's O; "early_release": a softmax warp releases a unit record before
+    it has walked the unit's tiles).  records: the block-sparse form, in which
+    the Q / K lane publishes each unit's record (its kept tiles) in one of two
+    slots (UNIT_FULL) once the six readers — the V lane, the MMA warp and the
+    four softmax warps — have released the slot's previous unit (UNIT_EMPTY);
+    each reader checks that the slot still holds its unit while it uses it."""
     rnd = random.Random(seed)
     B = {"QFull": Bar(1), "QEmpty": Bar(1), "ODone": Bar(1)}
     for s in range(kst):
@@ -221,7 +226,19 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
     for s in range(2):
         B[f"SF{s}"] = Bar(1)
         B[f"PF{s}"] = Bar(4)           # the model's four softmax warps
+        B[f"UF{s}"] = Bar(1)
+        B[f"UE{s}"] = Bar(6)
     loads, pipe, content = [], [], {}
+
+    def take_record(k):
+        if records:
+            yield from wait(f"UF{k & 1}", (k >> 1) & 1)
+            assert content.get(("rec", k & 1)) == k, "a unit record of another unit"
+
+    def release_record(k):
+        if records:
+            assert content.get(("rec", k & 1)) == k, "a unit record overwritten while in use"
+            B[f"UE{k & 1}"].arrive()
 
     def wait(name, parity):
         while not B[name].done(parity):
@@ -231,6 +248,14 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
         # tag K: this lane also loads each unit's Q before the unit's K pieces
         i = 0
         for k, n in enumerate(units):
+            if tag == "K" and records:
+                if k >= 2:
+                    yield from wait(f"UE{k & 1}", ((k >> 1) - 1) & 1)
+                content[("rec", k & 1)] = k
+                yield
+                B[f"UF{k & 1}"].arrive()
+            if tag == "V":
+                yield from take_record(k)
             if tag == "K":
                 if k >= 1 and plant != "no_qempty_wait":
                     yield from wait("QEmpty", (k - 1) & 1)
@@ -242,6 +267,8 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
                         yield from wait(f"{tag}E{s}", ((i // slots) + 1) & 1)
                     loads.append((f"{tag}F{s}", f"{tag}{s}", (k, j, c)))
                     i += 1
+            if tag == "V":
+                release_record(k)
 
     def mma():
         def issue_s(g, k, j):
@@ -265,6 +292,8 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
             pipe.append(("commit", "ODone"))
         g = 0
         for k, n in enumerate(units):
+            yield from take_record(k)
+            release_record(k)                  # (only the count is needed)
             yield from wait("QFull", k & 1)
             if n > 0:
                 if plant == "early_qempty" and n == 1:
@@ -288,9 +317,16 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
         g = 0
         pending = None                 # (unit, last tile) whose O is still to be read out
         for k, n in enumerate(units):
+            yield from take_record(k)
+            if plant == "early_release":
+                release_record(k)
             for j in range(n):
                 gj = g + j
                 yield from wait(f"SF{gj & 1}", (gj >> 1) & 1)
+                if records:
+                    # (the kernel reads the tile's index from the record here,
+                    # for its mask, after the scores have arrived)
+                    assert content.get(("rec", k & 1)) == k, "a unit record overwritten while in use"
                 assert not busy(f"S{gj & 1}"), "score buffer read while a product uses it"
                 assert content.get(f"S{gj & 1}") in (("S", gj), ("P", gj)), "scores of another tile"
                 yield
@@ -305,6 +341,8 @@ def run_one_tile(units, kst, vst, seed, kp=1, vp=1, plant=None):
                 if pending is not None:
                     yield from read_out(*pending)
                     pending = None
+            if plant != "early_release":
+                release_record(k)
             if n > 0:
                 yield from wait("ODone", (g + n - 1) & 1)
                 if plant == "early_p_full":
@@ -367,6 +405,30 @@ def test_one_tile_forward_protocol_in_pieces(seed):
     halves through a ring of two or three, each ring loaded by its own lane."""
     rnd = random.Random(seed)
     assert run_one_tile(random_units(rnd), rnd.choice([4, 5, 6]), rnd.choice([2, 3]), seed, kp=4, vp=2)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_one_tile_forward_protocol_block_sparse(seed):
+    """Block mask: the unit records between the Q / K lane and the readers."""
+    rnd = random.Random(seed)
+    pieces = rnd.random() < 0.5
+    assert run_one_tile(random_units(rnd) + random_units(rnd), rnd.choice([4, 5]) if pieces else 2,
+                        2, seed, kp=4 if pieces else 1, vp=2 if pieces else 1, records=True)
+
+
+def test_one_tile_model_catches_an_early_record_release():
+    caught = False
+    for seed in range(80):
+        rnd = random.Random(900 + seed)
+        units = [rnd.choice([0, 1, 1, 2]) for _ in range(rnd.randint(4, 8))]
+        try:
+            if not run_one_tile(units, 6, 3, seed, plant="early_release", records=True):
+                caught = True
+        except AssertionError:
+            caught = True
+        if caught:
+            break
+    assert caught
 
 
 @pytest.mark.parametrize("plant", ["no_qempty_wait", "early_qempty", "early_p_full"])
