@@ -134,6 +134,15 @@ struct BwdParams {
   // groups are taken heavy first in the key-tile-fastest order
   unsigned int* units;
   int n_units, n_kv_tiles, n_groups, tail_groups;
+  // One key tile in all (keys <= 128, d = 64): every (head, query tile) has a
+  // single dQ contribution, so bwd_kernel forms D itself from O and dO and
+  // writes dQ (times scale, in the output dtype) directly: one launch for the
+  // whole backward, no accumulator
+  int direct = 0;
+  const uint16_t* o = nullptr;
+  const uint16_t* dout = nullptr;
+  uint16_t* dq = nullptr;
+  Strides os, dos, dqs;
 };
 
 template <int D, int DH, int BR, int QST, bool CAUSAL, bool BF16, bool SPARSE>
@@ -414,7 +423,30 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       for (int u = 0; u < kPer; ++u) {
         const int q = q0 + lane + 32 * u;
         rl[u] = q < p.Nq ? -p.lse[base + q] * kLog2e : -INFINITY;
-        rd[u] = q < p.Nq ? -p.delta[base + q] : 0.f;
+        if (p.direct) {
+          // D = rowsum(dO o O) of query row q, in fp32
+          float acc = 0.f;
+          if (q < p.Nq) {
+            const uint4* orow = reinterpret_cast<const uint4*>(p.o + b * p.os.b + h * p.os.h +
+                                                               static_cast<long long>(q) * p.os.n);
+            const uint4* drow = reinterpret_cast<const uint4*>(p.dout + b * p.dos.b + h * p.dos.h +
+                                                               static_cast<long long>(q) * p.dos.n);
+            #pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+              const uint4 x = orow[c], y = drow[c];
+              const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+              #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 a = unpack2<BF16>(xs[e]), g = unpack2<BF16>(ys[e]);
+                acc = fmaf(a.x, g.x, acc);
+                acc = fmaf(a.y, g.y, acc);
+              }
+            }
+          }
+          rd[u] = -acc;
+        } else {
+          rd[u] = q < p.Nq ? -p.delta[base + q] : 0.f;
+        }
       }
     };
     auto store_ld = [&](int t) {
@@ -621,7 +653,22 @@ bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         }
       } else {
         // lane r = query row q0 + r; v[c] = dQ[q0 + r][c]
-        if (q0 + r < p.Nq) {
+        if (p.direct) {
+          // the row's one contribution: scale * dQ in the output dtype
+          if (q0 + r < p.Nq) {
+            uint4* out = reinterpret_cast<uint4*>(p.dq + b * p.dqs.b + h * p.dqs.h +
+                                                  static_cast<long long>(q0 + r) * p.dqs.n);
+            #pragma unroll
+            for (int c = 0; c < kCols / 8; ++c) {
+              uint32_t w[4];
+              #pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack2<BF16>(__uint_as_float(v[8 * c + 2 * e]) * p.scale,
+                                   __uint_as_float(v[8 * c + 2 * e + 1]) * p.scale);
+              out[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else if (q0 + r < p.Nq) {
           float4* base = reinterpret_cast<float4*>(p.dq_acc + (head_row + q0 + r) * D);
           #pragma unroll
           for (int c = 0; c < kCols / 4; ++c)
@@ -1240,15 +1287,23 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   static_assert(!WIDE || (D == 128 && DH == 128 && BR == 128), "wide kernel shape");
   cudaError_t e;
   const size_t rows = static_cast<size_t>(pr.B) * pr.H * pr.Nq;
+  // One key tile (d = 64): the main kernel forms D and writes dQ itself, when
+  // every query tile has a step (under the mask the first tile's rows see no
+  // key once Nq - Nk >= 128, and no step would write their dQ = 0)
+  const bool direct = D == 64 && !WIDE && !SPARSE && pr.Nk <= kBC &&
+                      (!CAUSAL || pr.Nq - pr.Nk < BR);
   // 1. preprocess
-  int slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
-  constexpr int kPreRows = pre_rows_per_block<D>();
-  bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + kPreRows - 1) / kPreRows),
-                            kPreWarps * 32, 0, stream>>>(
-      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
-      a.deterministic ? nullptr : a.dq_acc, rows, pr.H, pr.Nq, a.os, a.dos, nullptr);
-  timing_end(slot, stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  int slot = -1;
+  if (!direct) {
+    slot = timing_begin(FA_KERNEL_BWD_PRE, stream);
+    constexpr int kPreRows = pre_rows_per_block<D>();
+    bwd_preprocess<D, BF16><<<static_cast<unsigned>((rows + kPreRows - 1) / kPreRows),
+                              kPreWarps * 32, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.delta,
+        a.deterministic ? nullptr : a.dq_acc, rows, pr.H, pr.Nq, a.os, a.dos, nullptr);
+    timing_end(slot, stream);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // 2. main kernel
   CUtensorMap tq, tk, tv, tdo;
   if ((e = make_tmap_4d(&tq, a.q, D, pr.Nq, pr.H, pr.B, a.qs, 64, BR)) != cudaSuccess) return e;
@@ -1286,7 +1341,14 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.err = pr.err;
-  p.with_dq = a.deterministic ? 0 : 1;
+  p.with_dq = (a.deterministic && !direct) ? 0 : 1;
+  p.direct = direct ? 1 : 0;
+  p.o = static_cast<const uint16_t*>(a.o);
+  p.dout = static_cast<const uint16_t*>(a.dout);
+  p.dq = static_cast<uint16_t*>(a.dq);
+  p.os = a.os;
+  p.dos = a.dos;
+  p.dqs = a.dqs;
   // the dense 128-row kernel forms dK and dV only (dS^T lives in TMEM)
   if (WIDE && !SPARSE && p.with_dq) return cudaErrorInvalidValue;
   p.mask = a.mask;
@@ -1315,7 +1377,9 @@ cudaError_t launch_variant(const Problem& pr, const BwdArgs& a, cudaStream_t str
   kern<<<grid, kThreadsMain, kSmem, stream>>>(tq, tk, tv, tdo, p);
   timing_end(slot, stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // 3. dQ: the query-outer kernel (deterministic) or the accumulator's conversion
+  // 3. dQ: written by the main kernel (one key tile), the query-outer kernel
+  // (deterministic) or the accumulator's conversion
+  if (direct) return cudaSuccess;
   if (a.deterministic) return launch_bwd_dq(pr, a, stream);
   const size_t n8 = rows * D / 8;
   const unsigned blocks = static_cast<unsigned>(
