@@ -63,6 +63,7 @@ KERNEL_SOURCES = {
 PROFILE_CASES = {
     "gqa8k_b1": (WORKLOADS["gqa8k"].with_(B=1), False),
     "gpt_layer_b2": (WORKLOADS["gpt_layer"].with_(B=2), False),
+    "gpt_layer_causal_b2": (WORKLOADS["gpt_layer_causal"].with_(B=2), False),
     "d64": (Workload("d64", 1, 16, 16, 4096, 64, "bf16", False, 7), False),
     "head256_b1": (WORKLOADS["head256"].with_(B=1), False),
     "head256_b1_det": (WORKLOADS["head256"].with_(B=1), True),
