@@ -574,26 +574,45 @@ def main():
     binding.device_status()
 
     # ------------------------------------------------ device-timed region
-    binding.timing_enable(4 * args.steps + 8)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks, NvmlPoller(local) as nvml:
-        barrier()
-        torch.cuda.synchronize()
-        step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ev0.record(stream)
-        for i in range(args.steps):
-            step()
-            step_evs[i].record(stream)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-    binding.device_status()
-    # each step's own time (the line's value is over the whole region)
-    step_ms = [ev0.elapsed_time(step_evs[0])] + \
-        [step_evs[i - 1].elapsed_time(step_evs[i]) for i in range(1, args.steps)]
-    kernel_times = binding.timing_read()
-    binding.timing_enable(0)
-    ms_total = ev0.elapsed_time(ev1)
+    def timed_region():
+        binding.timing_enable(4 * args.steps + 8)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clocks, NvmlPoller(local) as nvml:
+            barrier()
+            torch.cuda.synchronize()
+            step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            ev0.record(stream)
+            for i in range(args.steps):
+                step()
+                step_evs[i].record(stream)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+        binding.device_status()
+        # each step's own time (the line's value is over the whole region)
+        step_ms = [ev0.elapsed_time(step_evs[0])] + \
+            [step_evs[i - 1].elapsed_time(step_evs[i]) for i in range(1, args.steps)]
+        kernel_times = binding.timing_read()
+        binding.timing_enable(0)
+        return ev0.elapsed_time(ev1), step_ms, kernel_times, clocks, nvml
+
+    def throttled(clocks, nvml) -> list:
+        """Clock-event reasons that void a measurement (a power cap does not)."""
+        seen = set((nvml.summary() or {}).get("reasons", [])) | set(clocks.summary().get("reasons", []))
+        bad = sorted(seen & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"})
+        if world > 1:    # every rank takes the same decision
+            import torch.distributed as dist
+            t = torch.tensor([1.0 if bad else 0.0], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            if t.item() > 0 and not bad:
+                bad = ["on another rank"]
+        return bad
+
+    ms_total, step_ms, kernel_times, clocks, nvml = timed_region()
+    remeasured = throttled(clocks, nvml)
+    if remeasured:
+        # a slowdown during the region: measure once more and report that one
+        ms_total, step_ms, kernel_times, clocks, nvml = timed_region()
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms_total], device=dev)
@@ -764,6 +783,7 @@ def main():
                 "serial_value": round(world * flops_step / (ms_e2e_serial * 1e-3) / 1e12, 2)},
         "gpu_launches": gpu_launches,
         "clocks": clk,
+        **({"remeasured_after": remeasured} if remeasured else {}),
         "timed_region_s": round(ms_total * 1e-3, 4),
     }
     if world == 1 and not args.no_per_config:
