@@ -407,15 +407,14 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- decode regime
-def run_decode(args):
+def decode_result(steps: int, warmup: int, nq: int = 1) -> dict:
     """Short-query forward over a long key cache (decoding after a prefix):
     memory-bound, so the metric is GB/s of Q, K, V read and O, L written
     against the measured copy bandwidth.  Times fa_fwd_splitkv (key axis
     split over CTAs, partials merged) and fa_fwd_qk (one pass)."""
-    torch.cuda.set_device(0)
     from exact_io_aware_20_gb300 import binding
     binding.load()
-    B, H, Hkv, Nq, Nk, d = 8, 32, 8, args.decode_nq, 8192, 128
+    B, H, Hkv, Nq, Nk, d = 8, 32, 8, nq, 8192, 128
     w = Workload("decode", B, H, Hkv, Nq, d, "bf16", True, 1006)
     q, k, v, _ = make_inputs(w, "cuda", Nk=Nk)
     o = torch.empty_like(q)
@@ -427,28 +426,33 @@ def run_decode(args):
     res = {}
     for name, fn in (("splitkv", lambda: binding.forward_splitkv(q, k, v, True, w.scale, 0, o, lse, ws)),
                      ("one_pass", lambda: binding.forward(q, k, v, True, w.scale, o, lse))):
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(max(warmup, 3)):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.steps):
+        for _ in range(steps):
             fn()
         e1.record()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
+        ms = e0.elapsed_time(e1) / steps
         res[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
                      "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
     binding.device_status()
-    print(json.dumps({
+    return {
         "metric": "decode attention forward GB/s (Q,K,V read + O,L written)", "unit": "GB/s",
-        "value": res["splitkv"]["GB/s"], "higher_is_better": True, "steps": args.steps,
+        "value": res["splitkv"]["GB/s"], "higher_is_better": True, "steps": steps,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"decode: B={B} Hq={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} bf16, "
                                f"causal (bottom-right), inputs larger than L2 ({nbytes >> 20} MiB)"},
         "peak": {"hbm_gbs": peaks["hbm_gbs"], "source": src},
         "splitkv": res["splitkv"], "one_pass": res["one_pass"],
-        "splits_auto": need and int(need // (B * H * Nq * (d + 1) * 4)) or 1}), flush=True)
+        "splits_auto": need and int(need // (B * H * Nq * (d + 1) * 4)) or 1}
+
+
+def run_decode(args):
+    torch.cuda.set_device(0)
+    print(json.dumps(decode_result(args.steps, args.warmup, args.decode_nq)), flush=True)
     return 0
 
 
@@ -465,17 +469,16 @@ def kept_pairs(mask: torch.Tensor, N: int, causal: bool) -> int:
     return below * 128 * 128 + diag * (128 * 129 // 2)
 
 
-def run_blocksparse(args):
-    """fa_fwd_blocksparse + fa_bwd_blocksparse on the gqa8k shapes under a
+def blocksparse_result(workload: str, density: float, steps: int, warmup: int) -> dict:
+    """fa_fwd_blocksparse + fa_bwd_blocksparse on a workload's shapes under a
     seeded random block mask (one pattern for all heads): TFLOP/s counted on
     the kept (query, key) pairs only, and the time against the dense step."""
-    torch.cuda.set_device(0)
     from exact_io_aware_20_gb300 import binding
     from exact_io_aware_20_gb300.inputs import make_block_mask
     binding.load()
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[workload]
     q, k, v, do = make_inputs(w, "cuda")
-    mask = make_block_mask(1, w.N, w.N, args.density, w.seed, "cuda")
+    mask = make_block_mask(1, w.N, w.N, density, w.seed, "cuda")
     pairs = kept_pairs(mask, w.N, w.causal) * w.B * w.H
     flops = 4.0 * w.d * pairs * 3.5          # forward 4d, backward 2.5x that, per kept pair
     o = torch.empty_like(q)
@@ -494,34 +497,41 @@ def run_blocksparse(args):
 
     res = {}
     for name, fn in (("sparse", sparse_step), ("dense", dense_step)):
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(max(warmup, 3)):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.steps):
+        for _ in range(steps):
             fn()
         e1.record()
         torch.cuda.synchronize()
-        res[name] = e0.elapsed_time(e1) / args.steps
+        res[name] = e0.elapsed_time(e1) / steps
     binding.device_status()
     peaks, src = load_peaks()
     value = flops / (res["sparse"] * 1e-3) / 1e12
     dense_pairs = w.B * w.H * (w.N * (w.N + 1) // 2 if w.causal else w.N * w.N)
-    print(json.dumps({
+    del q, k, v, do, o, lse, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return {
         "metric": "block-sparse attention fwd+bwd TFLOP/s (kept pairs)", "unit": "TFLOP/s",
-        "value": round(value, 1), "higher_is_better": True, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(res["sparse"], 4), "dtype": "bf16",
+        "value": round(value, 1), "higher_is_better": True, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(res["sparse"], 4), "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"{w.name} (B={w.B} Hq={w.H} Hkv={w.Hkv} N={w.N} d={w.d}, "
                                f"causal={w.causal}) under a random 128x128 block mask, "
-                               f"density {args.density}, shared by all heads; inputs larger "
+                               f"density {density}, shared by all heads; inputs larger "
                                f"than L2"},
         "kept_fraction": round(pairs / dense_pairs, 4),
         "dense_ms_per_step": round(res["dense"], 4),
         "speedup_vs_dense": round(res["dense"] / res["sparse"], 3),
-        "frac_of_burst": round(value / peaks["bf16_tflops"], 4), "peak_source": src}),
-        flush=True)
+        "frac_of_burst": round(value / peaks["bf16_tflops"], 4), "peak_source": src}
+
+
+def run_blocksparse(args):
+    torch.cuda.set_device(0)
+    print(json.dumps(blocksparse_result(args.workload, args.density, args.steps, args.warmup)),
+          flush=True)
     return 0
 
 
@@ -790,6 +800,19 @@ def main():
         line["bwd_deterministic"] = time_deterministic_bwd(w, q, k, v, o, lse, do, dq, dk, dv, ws,
                                                            stream, peaks)
         line["per_config"] = per_config(dev, peaks, peak_src)
+        # the measurement plan's other regimes, in compact form: decode
+        # (split-KV over an 8192-key cache) and block-sparse (the gqa8k
+        # shapes under random block masks)
+        dec = decode_result(20, 3)
+        line["decode"] = {"GB/s": dec["value"], "frac_hbm": dec["splitkv"]["frac_hbm"],
+                          "ms": dec["splitkv"]["ms"], "one_pass_GB/s": dec["one_pass"]["GB/s"],
+                          "splits": dec["splits_auto"], "workload": dec["config"]["workload"]}
+        line["blocksparse"] = {}
+        for dens in (0.1, 0.25):
+            bs = blocksparse_result("gqa8k", dens, 5, 3)
+            line["blocksparse"][str(dens)] = {
+                "tflops_kept_pairs": bs["value"], "ms_per_step": bs["ms_per_step"],
+                "speedup_vs_dense": bs["speedup_vs_dense"], "kept_fraction": bs["kept_fraction"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(base, args.cpu_seconds)
     print(json.dumps(line), flush=True)
