@@ -24,9 +24,9 @@
 // the rows (its 32 keys, its 64 queries) that dS warp w of rank 1 reads, with
 // st.async stores that complete on that warp's own barrier in rank 1, so the
 // sender never waits for the data to land; the receiver takes its rows into
-// registers as soon as they have arrived and releases them at once.  Every product is an
-// M = 128, N >= 128 tcgen05.mma (full rate), and the two CTAs carry the same
-// tensor work per step.
+// registers as soon as they have arrived and releases them at once.  Every
+// product is an M = 128, N >= 128 tcgen05.mma (full rate), and the two CTAs
+// carry the same tensor work per step.
 // Each CTA holds its stationary tile (K or V, 64 KB) and a ring of six
 // 64-column chunks (96 KB) through which both of its streamed operands pass
 // in the order they are read: the score operand (Q or dO) of step t, then
