@@ -39,13 +39,17 @@ def test_backward_sweep(d, causal, dtype, H, Hkv, N):
                 f"bwd d{d} causal{causal} {dtype} H{H}/{Hkv} N{N}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [383, 640, 1000])
-def test_backward_several_tiles_gqa(N):
+def test_backward_several_tiles_gqa(N, d):
+    """Several key and query tiles, three query heads per kv head, two
+    batches: every head dim's unit walk (key tiles x heads x query tiles, the
+    heavy-first order under the mask) and its ragged last tiles."""
     for causal in (False, True):
-        w = Workload("multi", 2, 6, 2, N, 128, "bf16", causal, 7 + N)
+        w = Workload("multi", 2, 6, 2, N, d, "bf16", causal, 7 + N + d)
         (q, k, v, do), (o, lse, dq, dk, dv) = run_fwd_bwd(w)
         dq_r, dk_r, dv_r = oracle.backward(q, k, v, do, causal, w.scale)
-        check_grads([("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)], f"bwd N{N} c{causal}")
+        check_grads([("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)], f"bwd d{d} N{N} c{causal}")
 
 
 def test_backward_tiny_workload():
