@@ -11,7 +11,9 @@ What pins what:
   invariants        rows of P sum to 1 and P = exp(S - L) (read off with
                     V = I), L equals a long-double logsumexp, permutation of
                     keys, shift of all keys by one vector, GQA equals MHA with
-                    repeated K/V, D = rowsum(dO o O)
+                    repeated K/V, D = rowsum(dO o O); summed over the keys,
+                    dV equals the summed dO of the rows that see a key and
+                    dK is zero
   derivatives       central finite differences of sum(O o dO)
   library routines  torch fp64 softmax/matmul and torch.autograd gradients
   bottom-right mask Nq != Nk rows, including rows with no allowed key
@@ -258,6 +260,25 @@ def pin_delta_and_extras(lib):
         np.testing.assert_allclose(delta, (do * of).sum(-1), rtol=0, atol=1e-13)
 
 
+def pin_gradient_sums(lib):
+    """Sums over the keys of a group's gradients: sum_k dV_k = the sum of dO
+    over the rows that see a key (every row of P sums to 1, dV = P^T dO) and
+    sum_k dK_k = 0 (every row of dS = P o (dP - D) sums to 0, because
+    sum_k P_ik dP_ik = dO_i . O_i = D_i), with and without the mask, Nq != Nk
+    included."""
+    rng = _rng(21)
+    for causal, Nq, Nk in ((False, 11, 11), (True, 11, 11), (True, 9, 6), (True, 6, 9)):
+        G, d = 3, 5
+        q, k, v = _rand(rng, G, Nq, d), _rand(rng, Nk, d), _rand(rng, Nk, d)
+        do = _rand(rng, G, Nq, d)
+        _, dk, dv = oracle.backward_group(q, k, v, do, causal, 0.7, lib)
+        seen = np.array([any(_allowed(i, kk, Nq, Nk, causal) for kk in range(Nk))
+                         for i in range(Nq)], dtype=np.float64)
+        np.testing.assert_allclose(dv.sum(0), (do * seen[None, :, None]).sum((0, 1)), rtol=0,
+                                   atol=1e-12)
+        np.testing.assert_allclose(dk.sum(0), np.zeros(d), rtol=0, atol=1e-12)
+
+
 def _fd_check(lib, G, Nq, Nk, d, causal, seed):
     rng = _rng(seed)
     q, k, v = _rand(rng, G, Nq, d), _rand(rng, Nk, d), _rand(rng, Nk, d)
@@ -462,6 +483,7 @@ def pin_blockmask_torch(lib):
 ALL_PINS = [pin_identical_keys, pin_zero_queries, pin_dominant_score, pin_causal_first_row,
             pin_two_keys_forward, pin_two_keys_backward, pin_rows_are_probabilities,
             pin_permutation_and_shift, pin_gqa_equals_repeated_mha, pin_delta_and_extras,
+            pin_gradient_sums,
             pin_finite_differences, pin_torch_fp64, pin_bottom_right_mask, pin_rows_match_group,
             pin_row_slabs_sum_to_group, pin_blockmask_all_ones_is_dense,
             pin_blockmask_single_block, pin_blockmask_torch]
