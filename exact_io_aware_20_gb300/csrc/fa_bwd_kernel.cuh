@@ -21,11 +21,13 @@
 //
 // Three kernels: preprocess (D and a zeroed fp32 dQ accumulator), a main
 // kernel, and a conversion of the accumulator to the output dtype (with the
-// softmax scale applied).  The main kernels here: bwd_kernel (d = 64 and
-// 256) and bwd128_kernel (d = 128: the key-outer half of the reproducible
-// backward, and the block-sparse backward).  The default dense d = 128
-// backward runs the fused kernel of fa_bwd_fused_kernel.cuh, which uses the
-// preprocess and conversion kernels of this file.
+// softmax scale applied).  The main kernels here: bwd_kernel (d = 64, and
+// d = 256 under a block mask) and bwd128_kernel (d = 128: the key-outer half
+// of the reproducible backward, and the block-sparse backward).  The default
+// dense d = 128 backward runs the fused kernel of fa_bwd_fused_kernel.cuh,
+// which uses the preprocess and conversion kernels of this file; the dense
+// d = 256 backward runs the cluster pair of fa_bwd_pair_kernel.cuh (dK, dV)
+// and the query-outer dQ kernel of fa_bwd_dq_kernel.cuh.
 //
 // bwd_kernel, one CTA per (batch, key/value head, 128-key tile[, half of
 // d when d = 256]); 10 warps:
