@@ -7,8 +7,8 @@ namespace fa {
 
 namespace {
 
-// buffers of received P^T on rank 1
-constexpr int kPairPBuf = 2;
+// buffers of received P^T on rank 1 (one: two more ring slots, 5% faster)
+constexpr int kPairPBuf = 1;
 
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_pair(const Problem& pr, const BwdArgs& a, cudaStream_t stream) {

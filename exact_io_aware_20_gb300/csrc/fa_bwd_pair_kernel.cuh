@@ -21,18 +21,24 @@
 // rank 0 sends P^T (16-bit, 32 KB a step) to rank 1's shared memory through
 // distributed shared memory, and nothing goes back but a release of the
 // buffer.  The exchange runs warp to warp: softmax warp w of rank 0 writes
-// the rows (its 32 keys, its 64 queries) that dS warp w of rank 1 reads, with
-// st.async stores that complete on that warp's own barrier in rank 1, so the
-// sender never waits for the data to land; the receiver takes its rows into
-// registers as soon as they have arrived and releases them at once.  Every
+// the rows (its 32 keys, its 64 queries) that dS warp w of rank 1 reads into
+// its own copy of the buffer, and one lane sends them as a single 4 KB bulk
+// copy that completes on that warp's own barrier in rank 1 (16-byte stores
+// into the other CTA's shared memory move ~17 B/clk, ~1,900 cycles for a
+// step's 32 KB on the critical path; the copy engine is faster); the receiver
+// takes its rows into registers as soon as they have arrived and releases
+// them at once.  Every
 // product is an M = 128, N >= 128 tcgen05.mma (full rate), and the two CTAs
 // carry the same tensor work per step.
-// Each CTA holds its stationary tile (K or V, 64 KB) and a ring of six
-// 64-column chunks (96 KB) through which both of its streamed operands pass
-// in the order they are read: the score operand (Q or dO) of step t, then
-// the accumulator operand (dO or Q) of step t - 1, and so on, so that loads
-// run 1.5 products ahead; rank 1 also holds two buffers of received P^T, so
-// that rank 0 writes step t + 1's while rank 1 still reads step t's.
+// Each CTA holds its stationary tile (K or V, 64 KB) and a ring of
+// 64-column chunks through which both of its streamed operands pass in the
+// order they are read: the score operand (Q or dO) of step t, then the
+// accumulator operand (dO or Q) of step t - 1, and so on; rank 1 also holds
+// PBUF buffers of received P^T and rank 0 its own copy of them, from which
+// the bulk copies read.  With one buffer the ring has eight slots (128 KB,
+// two products ahead): rank 0 writes step t + 1's rows once rank 1 has read
+// step t's, which it does first thing, and the two extra slots measured 5%
+// faster than a second buffer.
 // TMEM: accumulator (256 columns, two 128-column halves of d) | two score
 // buffers (128 columns; the 16-bit P^T or dS^T is written over the first 32
 // columns of each 64-column half and read there as the A operand).
@@ -52,9 +58,9 @@ namespace {
 
 constexpr int kPairThreads = 320;
 
-// PBUF: buffers of received P^T on rank 1 (1 or 2); the rest of rank 1's
-// shared memory is ring, and rank 0 has a ring of the same size (a deeper
-// one measured no faster).
+// PBUF: buffers of received P^T on rank 1 (1 or 2), each also held by rank
+// 0 as the source of its bulk copies; the rest of each CTA's shared memory
+// is ring.
 template <int PBUF>
 struct PairLayout {
   static constexpr int kChunk = 128 * 64 * 2;      // [128 rows][64 cols] 16-bit, 128-byte swizzle
@@ -62,7 +68,8 @@ struct PairLayout {
   static constexpr int kRing0 = kRing1;            // ring slots of rank 0
   static constexpr int kStatOff = 0;               // K (rank 0) or V (rank 1), 4 chunks of d
   static constexpr int kRingOff = 4 * kChunk;      // the operand ring
-  static constexpr int kPOff = kRingOff + kRing1 * kChunk;  // rank 1: P^T, PBUF x 2 query halves
+  static constexpr int kPOff = kRingOff + kRing1 * kChunk;  // P^T, PBUF x 2 query halves (rank 1
+                                                            // receives, rank 0 stages)
   static constexpr int kLDOff = kRingOff + 10 * kChunk;     // [2 halves][3 steps][64]: -L*log2e or -D
   static constexpr int kBarOff = kLDOff + 2 * 3 * 64 * 4;
   // IN_FULL / OUT_FREE: [softmax / dS warp (warp - 2)][P^T buffer, stride 2]
@@ -80,6 +87,7 @@ struct PairLayout {
   static_assert(kBytes + 1008 <= kAlloc, "shared memory budget (any 16-byte-aligned base)");
   static_assert(kRing0 % 2 == 0 && kRing1 % 2 == 0, "operand chunks come in aligned pairs");
   static_assert(kPOff + PBUF * 2 * kChunk <= kLDOff, "rank 1 layout");
+  static_assert(kRingOff + kRing0 * kChunk <= kPOff, "rank 0 keeps its own copy of the P^T buffers");
   static_assert(PBUF == 1 || PBUF == 2, "P^T buffers");
 };
 
@@ -299,6 +307,11 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t p_row0 = (rank == 0 ? mapa_shared(sbase + L::kPOff, peer) : sbase + L::kPOff) +
                             half * L::kChunk + r * 128;
     auto p_row = [&](int pb) { return p_row0 + pb * (2 * L::kChunk); };
+    // ... and on rank 0 the same row of its own copy of that buffer, where
+    // the row is written before the warp's rows go out as one bulk copy
+    auto p_stage = [&](int pb) {
+      return sbase + L::kPOff + pb * (2 * L::kChunk) + half * L::kChunk + r * 128;
+    };
     // ... and the warp's channel for that buffer: rank 1's IN_FULL (where
     // the sender's bytes land) and rank 0's OUT_FREE (where the reader
     // releases the rows)
@@ -404,6 +417,8 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive_warp(bar(L::kPFull + (t & 1)));
         // row r of this half of P^T to rank 1's buffer t % PBUF, once rank 1
         // has read step t - PBUF's from it
+        // rank 1 has read step t - PBUF's rows, so the bulk copy that took
+        // them there has also finished reading this CTA's copy of buffer pb
         const int pb = t % PBUF, use = t / PBUF;
         if (t >= PBUF && !wait_uniform<true>(out_free(pb), (use - 1) & 1, abort)) {
           ok = false;
@@ -411,8 +426,13 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         #pragma unroll
         for (int v = 0; v < 8; ++v)
-          st_async_v4(p_row(pb) + ((v ^ (r & 7)) * 16), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
-                      pk[4 * v + 3], in_full(pb));
+          st_shared_v4(p_stage(pb) + ((v ^ (r & 7)) * 16), pk[4 * v], pk[4 * v + 1],
+                       pk[4 * v + 2], pk[4 * v + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        // the warp's 32 rows are one 4 KB block in both CTAs
+        if (lane == 0) bulk_copy_to_cluster(p_row(pb), p_stage(pb), L::kRowsBytes, in_full(pb));
+        __syncwarp();
       } else {
         // row r of this half of P^T, sent by rank 0: into registers and the
         // rows released before this step's dP^T is waited for

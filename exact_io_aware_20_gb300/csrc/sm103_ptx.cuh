@@ -252,6 +252,29 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
       : "memory");
 }
 
+// 16 bytes into this CTA's shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from this CTA's shared memory to another CTA's of the cluster (dst and bar
+// are shared::cluster addresses); the bytes complete on that CTA's mbarrier
+// `bar`, which is also the only sign that the source has been read.  The
+// source must be written through the generic proxy and fenced
+// (fence_proxy_async_smem) before the copy is issued.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (a shared::cluster
 // address), releasing this thread's earlier memory operations at cluster
 // scope.

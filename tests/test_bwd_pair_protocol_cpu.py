@@ -14,9 +14,11 @@ Each CTA's two streamed operands pass through one ring of chunk slots (ten
 on rank 0; on rank 1 what the P^T buffers leave) in the order its MMA warp
 reads them (the accumulator product reads an aligned pair of slots).  The
 exchange runs warp to warp through one or two buffers: sender warp (h, w) of
-rank 0 writes step t's rows into buffer t % PBUF, which receiver warp (h, w)
-of rank 1 reads; the stores complete on the receiver's IN_FULL of that
-buffer, whose phase also needs the receiver's own expect_tx (made for step
+rank 0 writes step t's rows into its own copy of buffer t % PBUF and sends
+them as one bulk copy into rank 1's, which receiver warp (h, w) of rank 1
+reads (the copy's source must hold the rows until the copy lands, and only
+rank 1's release of the buffer tells rank 0 that it has); the bytes complete
+on the receiver's IN_FULL of that buffer, whose phase also needs the receiver's own expect_tx (made for step
 t + PBUF before it releases step t's rows on rank 0's OUT_FREE).  The model is at
 warp granularity: OUT_FREE, which the kernel counts in threads, counts the
 warp here.
@@ -28,10 +30,12 @@ import pytest
 from test_bwd_protocol_cpu import Bar
 
 
-def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, limit=400_000):
+def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, land_p=0.1,
+             limit=400_000):
     """Returns True when both CTAs finish; False on a hang (the roles stop
     making progress); raises AssertionError on a wrong read.  slow: rank 1's
-    dS warps get a fifth of the other roles' turns."""
+    dS warps get a fifth of the other roles' turns; land_p: the chance per
+    turn that an exchanged block of rows lands."""
     rnd = random.Random(seed)
     B = {}
     for r in (0, 1):
@@ -163,9 +167,13 @@ def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, 
                 assert content.get(ld(t)) == ("LD", t), "L / D values of another step"
                 B[r, f"PF{t & 1}"].arrive()       # before the rows are sent
                 yield
+                if plant == "stage_before_outfree":
+                    content[0, "stage", h, w, pb] = ("P", t)
+                    yield
                 if t >= pbuf and plant != "no_outfree_wait":
                     yield from wait((0, f"OUT{h}{w}{pb}"), (use - 1) & 1)
-                rx.append((h, w, pb, t))       # the stores land (and complete IN_FULL) later
+                content[0, "stage", h, w, pb] = ("P", t)   # this CTA's copy of the rows
+                rx.append((h, w, pb, t))       # one bulk copy: reads that copy, lands later
                 yield
             else:
                 if plant != "no_infull_wait":
@@ -203,6 +211,8 @@ def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, 
     def land(i):
         h, w, pb, t = rx.pop(i)
         assert expect[h, w, pb] >= t // pbuf + 1, "rows landed before the receiver expected them"
+        assert content.get((0, "stage", h, w, pb)) == ("P", t), \
+            "the bulk copy's source was overwritten before the copy had read it"
         content[1, "pin", h, w, pb] = ("P", t)
         B[1, f"IN{h}{w}{pb}"].arrive()
 
@@ -237,7 +247,7 @@ def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, 
             return True
         x = rnd.random()
         r = rnd.randrange(2)
-        if rx and x < 0.1:
+        if rx and rnd.random() < land_p:
             land(rnd.randrange(len(rx)))
         elif loads[r] and x < 0.2:
             land_load(r, rnd.randrange(len(loads[r])))
@@ -263,14 +273,15 @@ def run_pair(n, seed, plant=None, ld_slots=3, ring=(10, 6), pbuf=2, slow=False, 
 
 
 @pytest.mark.parametrize("seed", range(40))
-@pytest.mark.parametrize("ring,pbuf", [((10, 6), 2), ((10, 8), 1)])
+@pytest.mark.parametrize("ring,pbuf", [((10, 6), 2), ((10, 8), 1), ((8, 8), 1), ((6, 6), 2)])
 def test_pair_protocol(seed, ring, pbuf):
     n = [1, 2, 3, 5, 8][seed % 5]
     assert run_pair(n, seed, ring=ring, pbuf=pbuf, slow=seed % 4 == 3)
 
 
 @pytest.mark.parametrize("plant", ["no_outfree_wait", "no_infull_wait", "early_pfull",
-                                   "score_early", "two_ld_slots", "release_first", "odd_ring"])
+                                   "score_early", "two_ld_slots", "release_first", "odd_ring",
+                                   "stage_before_outfree"])
 def test_pair_protocol_catches(plant):
     """Each planted mistake produces a wrong read or a hang on some seed."""
     caught = False
@@ -278,7 +289,8 @@ def test_pair_protocol_catches(plant):
         try:
             ok = run_pair(6, seed, plant=None if plant in ("two_ld_slots", "odd_ring") else plant,
                           ld_slots=2 if plant == "two_ld_slots" else 3,
-                          ring=(10, 5) if plant == "odd_ring" else (10, 6), slow=seed % 2 == 1)
+                          ring=(10, 5) if plant == "odd_ring" else (10, 6), slow=seed % 2 == 1,
+                          land_p=0.1 if seed % 3 else 0.01)
         except AssertionError:
             caught = True
             break
