@@ -1076,6 +1076,10 @@ bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncwarp();
     tmem_dealloc(tmem, L::kTmemCols);
   }
+  // launched as the dK / dV pair kernel's programmatic dependent (it needs
+  // none of that kernel's results, only D): this grid ends only after that
+  // one has, so whatever follows on the stream sees dK and dV as well
+  grid_dependency_wait();
 }
 
 template <bool CAUSAL, bool BF16>
@@ -1112,11 +1116,23 @@ cudaError_t launch_dq256(const Problem& pr, const BwdArgs& a, cudaStream_t strea
   p.mask = BlockMask{};
   p.dqs = a.dqs;
   p.err = pr.err;
-  dim3 grid(p.num_q_tiles, pr.H, pr.B);
+  // Always right behind the dK / dV pair kernel, which issues
+  // grid_launch_dependents at its start: this grid's CTAs take the SMs that
+  // kernel's last, partly filled wave leaves idle.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_q_tiles, pr.H, pr.B);
+  cfg.blockDim = dim3(kDq256Threads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const int slot = timing_begin(FA_KERNEL_BWD_DQ, stream);
-  kern<<<grid, kDq256Threads, L::kAlloc, stream>>>(tq, tk, tv, tdo, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, p);
   timing_end(slot, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 template <int D, int KST, bool SPARSE>

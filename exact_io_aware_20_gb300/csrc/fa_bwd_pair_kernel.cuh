@@ -111,6 +111,10 @@ bwd256_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+  // the dQ kernel that follows (launched as this grid's programmatic
+  // dependent; it reads none of this kernel's results) may start filling
+  // the SMs this grid's last wave leaves idle
+  grid_launch_dependents();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
