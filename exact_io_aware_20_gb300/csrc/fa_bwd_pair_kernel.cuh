@@ -24,10 +24,11 @@
 // the rows (its 32 keys, its 64 queries) that dS warp w of rank 1 reads into
 // its own copy of the buffer, and one lane sends them as a single 4 KB bulk
 // copy that completes on that warp's own barrier in rank 1 (16-byte stores
-// into the other CTA's shared memory move ~17 B/clk, ~1,900 cycles for a
-// step's 32 KB on the critical path; the copy engine is faster); the receiver
-// takes its rows into registers as soon as they have arrived and releases
-// them at once.  Every
+// into the other CTA's shared memory, ~17 B/clk per SM, held the warps for
+// the whole ~1,900 cycles of a step's 32 KB; the bulk copy moves them no
+// faster, but the warps write ~80 B/clk locally and go on to the next step);
+// the receiver takes its rows into registers as soon as they have arrived
+// and releases them at once.  Every
 // product is an M = 128, N >= 128 tcgen05.mma (full rate), and the two CTAs
 // carry the same tensor work per step.
 // Each CTA holds its stationary tile (K or V, 64 KB) and a ring of
